@@ -1,0 +1,47 @@
+"""Byte and FLOP accounting for the decode-attention roofline.
+
+The algorithmic unit of work is one cached position of one K/V head: its key
+row and value row are read once (2 * D elements) and every one of the G query
+heads sharing that K/V head spends 2 * D multiply-adds on it (q . k and p * v),
+i.e. 4 * D * G FLOPs.  Padding beyond a sequence's length is not counted,
+matching "The Basics of Transformer Inference", the item "Using ragged HBM
+reads and Paged Attention" (only the non-padding part of the cache needs to be
+read).
+"""
+from __future__ import annotations
+
+
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
+                       elem_bytes: int) -> int:
+    """Cache bytes one token adds: keys and values, for every layer and K/V
+    head ("Machine Learning Engineering and AI Systems at Scale", section
+    "The key and value cache": two, times layers, K/V heads, head dimension
+    and bytes per element)."""
+    return 2 * layers * kv_heads * head_dim * elem_bytes
+
+
+def kv_cache_bytes(layers: int, kv_heads: int, head_dim: int, elem_bytes: int,
+                   batch: int, tokens: int) -> int:
+    """Whole-cache bytes for `batch` sequences of `tokens` cached tokens."""
+    return kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes) * batch * tokens
+
+
+def kv_bytes_read(attn_lens, Hkv: int, D: int, elem_bytes: int = 2) -> int:
+    """Algorithmic K+V bytes one decode-attention call reads (one layer)."""
+    total = int(sum(int(x) for x in attn_lens))
+    return total * Hkv * D * 2 * elem_bytes
+
+
+def attn_flops(attn_lens, Hq: int, D: int) -> int:
+    """Algorithmic FLOPs of one call: 2*D for q.k plus 2*D for p*v per query
+    head and position."""
+    total = int(sum(int(x) for x in attn_lens))
+    return 4 * Hq * D * total
+
+
+def step_io_bytes(B: int, Hq: int, Hkv: int, D: int) -> dict:
+    """Per-step host<->device bytes of the end-to-end call: q, k_new, v_new
+    and the two int32 length vectors in; the fp32 output back."""
+    h2d = B * Hq * D * 2 + 2 * B * Hkv * D * 2 + 2 * B * 4
+    d2h = B * Hq * D * 4
+    return {"h2d": h2d, "d2h": d2h}

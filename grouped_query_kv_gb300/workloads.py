@@ -1,0 +1,133 @@
+"""Seeded synthetic decode workloads.
+
+This module only draws inputs (random numbers and lengths); it holds none of
+the attention arithmetic, so that the CUDA library and the CPU oracle can be
+fed the same tensors without sharing any of the method's code.
+
+The shapes follow the workloads the pages discuss: PaLM-8B / PaLM-540B
+multi-query attention ("Efficiently Scaling Transformer Inference",
+section 3 "Attention Layer Partitioning" and section 5 "Experiments": 48
+query heads of width 256 sharing one K/V head) and Llama-2-70B grouped-query
+attention ("Tensor Parallelism: Splitting Operations Across GPUs", section
+"The GQA ceiling: a worked memory audit": 64 query heads, 8 K/V heads, head
+width 128).  No page uses a dataset; the values are N(0,1) draws rounded to
+bf16, which stand in for projected activations.
+
+Length convention.  ``attn_lens[b]`` is the number of cached positions the
+attention reads after this step's new token has been appended; the append
+writes row ``attn_lens[b] - 1`` (the number of tokens cached before it).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import List, Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    Lmax: int
+    scale: float
+    # attention lengths: a fixed list, a single value for every sequence, or
+    # None with `ragged=True` for uniform draws in [1, Lmax]
+    lens: Optional[tuple] = None
+    ragged: bool = False
+    k_scale: float = 1.0
+    note: str = ""
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+
+def _sweep() -> List[Workload]:
+    out = []
+    for hkv in (32, 8, 1):
+        for b in (1, 8, 64, 256):
+            out.append(Workload(
+                name=f"sweep_hkv{hkv}_b{b}", B=b, Hq=32, Hkv=hkv, D=128,
+                Lmax=4096, scale=1.0 / math.sqrt(128), lens=(4096,),
+                note="MHA vs GQA vs MQA sweep at D=128, Hq=32, length 4096"))
+    return out
+
+
+WORKLOADS = {w.name: w for w in [
+    Workload("tiny_mqa", B=2, Hq=4, Hkv=1, D=64, Lmax=64, scale=1.0 / 8.0,
+             lens=(8, 34),
+             note="tiny MQA: cached lengths [7, 33], one append then one "
+                  "attention over [8, 34]"),
+    Workload("palm8b_mqa", B=64, Hq=16, Hkv=1, D=256, Lmax=2048,
+             scale=1.0 / 16.0, lens=(2048,),
+             note="PaLM-8B-shaped MQA decode, every sequence at length 2048"),
+    Workload("llama70b_gqa_ragged", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
+             scale=1.0 / math.sqrt(128), ragged=True,
+             note="Llama-70B-shaped GQA decode, lengths uniform in [1, 8192]"),
+    Workload("palm540b_long_mqa", B=8, Hq=48, Hkv=1, D=256, Lmax=32768,
+             scale=1.0 / 16.0, lens=(32768,), k_scale=0.5,
+             note="PaLM-540B-shaped long-context MQA decode, k scaled by 0.5"),
+] + _sweep()}
+
+# the five configurations in the order the benchmark suite lists them
+CONFIG_ORDER = ["tiny_mqa", "palm8b_mqa", "llama70b_gqa_ragged",
+                "palm540b_long_mqa"] + [w.name for w in _sweep()]
+
+
+def attn_lens(w: Workload, seed: int = 0) -> torch.Tensor:
+    """int32 [B] attention lengths (drawn on the CPU so they never depend on
+    the device the values are drawn on)."""
+    if w.ragged:
+        g = torch.Generator().manual_seed(seed + 7919)
+        return torch.randint(1, w.Lmax + 1, (w.B,), generator=g,
+                             dtype=torch.int64).to(torch.int32)
+    if len(w.lens) == 1:
+        return torch.full((w.B,), w.lens[0], dtype=torch.int32)
+    assert len(w.lens) == w.B
+    return torch.tensor(w.lens, dtype=torch.int32)
+
+
+def _normal_bf16(shape, gen, device, mul=1.0):
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if mul != 1.0:
+        x.mul_(mul)
+    return x.to(torch.bfloat16)
+
+
+def make_inputs(w: Workload, seed: int = 0, device="cpu", lens=None):
+    """Draw one decode step's inputs.
+
+    Returns a dict of tensors on `device`:
+      q        bf16 [B, Hq, D]
+      k_cache  bf16 [B, Hkv, Lmax, D]   (every row drawn, padding included)
+      v_cache  bf16 [B, Hkv, Lmax, D]
+      k_new    bf16 [B, Hkv, D]         this step's new token
+      v_new    bf16 [B, Hkv, D]
+      append_pos int32 [B]              row the append writes (= attn_lens-1)
+      attn_lens  int32 [B]              positions the attention reads
+    """
+    device = torch.device(device)
+    gen = torch.Generator(device=device).manual_seed(seed)
+    al = attn_lens(w, seed) if lens is None else torch.as_tensor(lens, dtype=torch.int32)
+    assert al.shape == (w.B,)
+    assert int(al.min()) >= 1 and int(al.max()) <= w.Lmax
+    q = _normal_bf16((w.B, w.Hq, w.D), gen, device)
+    k_cache = _normal_bf16((w.B, w.Hkv, w.Lmax, w.D), gen, device, w.k_scale)
+    v_cache = _normal_bf16((w.B, w.Hkv, w.Lmax, w.D), gen, device)
+    k_new = _normal_bf16((w.B, w.Hkv, w.D), gen, device, w.k_scale)
+    v_new = _normal_bf16((w.B, w.Hkv, w.D), gen, device)
+    return dict(q=q, k_cache=k_cache, v_cache=v_cache, k_new=k_new,
+                v_new=v_new, append_pos=(al - 1).to(device),
+                attn_lens=al.to(device))
+
+
+def bf16_bits(t: torch.Tensor):
+    """uint16 numpy view of a bf16 tensor's bits (copied to the host)."""
+    import numpy as np
+    assert t.dtype == torch.bfloat16
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -1,0 +1,104 @@
+"""Plant plausible mistakes in a copy of the oracle's C source, compile each
+copy, and check that the independent pins reject it.  This is evidence that
+the pins can tell a wrong oracle from a right one (CPU only)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+
+def _bits(x):
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _unbits(b):
+    t = torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def pins_pass(orc) -> bool:
+    """A compact battery of the independent pins; False on the first miss."""
+    rng = np.random.default_rng(99)
+    B, Hq, Hkv, D, L = 3, 8, 2, 32, 24
+    q = _bits(rng.standard_normal((B, Hq, D)))
+    k = _bits(rng.standard_normal((B, Hkv, L, D)))
+    v = _bits(rng.standard_normal((B, Hkv, L, D)))
+    lens = np.array([24, 7, 1], np.int32)
+    scale = 1.0 / math.sqrt(D)
+    try:
+        out = orc.gqa_decode(q, k, v, lens, scale=scale)
+    except ValueError:
+        return False
+    # library special case
+    for b in range(B):
+        n = int(lens[b])
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(_unbits(q[b:b + 1]))[:, :, None, :],
+            torch.from_numpy(_unbits(k[b:b + 1, :, :n])),
+            torch.from_numpy(_unbits(v[b:b + 1, :, :n])),
+            scale=scale, enable_gqa=True)[0, :, 0].numpy()
+        if not np.allclose(out[b], ref, rtol=1e-12, atol=1e-13):
+            return False
+    # length one returns V[0]
+    if not np.array_equal(out[2], _unbits(v[2, np.arange(Hq) // 4, 0])):
+        return False
+    # rows past the length are never read
+    k2, v2 = k.copy(), v.copy()
+    k2[1, :, 7:] = 0x7FC0
+    v2[1, :, 7:] = 0x7F80
+    if not np.array_equal(orc.gqa_decode(q, k2, v2, lens, scale=scale), out):
+        return False
+    # append: exactly one row per (b, kvh) changes, to the new values
+    kc, vc = k.copy(), v.copy()
+    kn = _bits(rng.standard_normal((B, Hkv, D)))
+    vn = _bits(rng.standard_normal((B, Hkv, D)))
+    pos = np.array([3, 0, 23], np.int32)
+    kr, vr = kc.copy(), vc.copy()
+    kr[np.arange(B), :, pos] = kn
+    vr[np.arange(B), :, pos] = vn
+    try:
+        orc.kv_append(kc, vc, kn, vn, pos)
+    except ValueError:
+        return False
+    return np.array_equal(kc, kr) and np.array_equal(vc, vr)
+
+
+MUTANTS = {
+    "interleaved head mapping": ("const int64_t kvh = h / G;",
+                                 "const int64_t kvh = h % Hkv;"),
+    "dropped scale": ("s_buf[j] = scale * dot;", "s_buf[j] = dot;"),
+    "normaliser without max shift": ("denom += exp(s_buf[j] - m);",
+                                     "denom += exp(s_buf[j]);"),
+    "flipped sign in weights": ("double p = exp(s_buf[j] - m) / denom;",
+                                "double p = exp(m - s_buf[j]) / denom;"),
+    "keys and values swapped": (
+        "oracle_bf16_to_double(V[j * D + d]);",
+        "oracle_bf16_to_double(K[j * D + d]);"),
+    "wrong query row": ("const uint16_t *qh = q + (b * Hq + h) * D;",
+                        "const uint16_t *qh = q + (b * Hq + kvh) * D;"),
+    "reads one row past the length": (
+        "const int64_t len = seq_lens[b];",
+        "const int64_t len = seq_lens[b] + (seq_lens[b] < Lmax);"),
+    "append one row late": ("int64_t pos = seq_lens[b];",
+                            "int64_t pos = seq_lens[b] + (seq_lens[b] + 1 < Lmax);"),
+    "append swaps k and v": ("v_cache[dst] = v_new[src];",
+                             "v_cache[dst] = k_new[src];"),
+}
+
+
+def test_unmodified_oracle_passes_the_battery():
+    assert pins_pass(oracle.Oracle())
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.source_text()
+    assert src.count(old) >= 1, "mutation anchor not found: " + name
+    so = oracle.compile_variant(src.replace(old, new), str(tmp_path))
+    assert not pins_pass(oracle.Oracle(so)), name

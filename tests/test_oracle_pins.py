@@ -1,0 +1,342 @@
+"""Pins for the CPU oracle: every check here is independent of the oracle's
+own code (closed forms, a library routine, an explicit brute-force formula,
+invariants of the mathematics).  Marked `not gpu`; runs in seconds.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+from scipy.special import expit
+
+import oracle
+
+
+def bits(x):
+    """bf16 bits of a float tensor/array (round to nearest even via torch)."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def unbits(b):
+    """bf16 bits -> float64 through torch's own conversion (a library path)."""
+    t = torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def rand_case(rng, B, Hq, Hkv, D, Lmax, lens=None, kmul=1.0):
+    q = bits(rng.standard_normal((B, Hq, D)))
+    k = bits(kmul * rng.standard_normal((B, Hkv, Lmax, D)))
+    v = bits(rng.standard_normal((B, Hkv, Lmax, D)))
+    if lens is None:
+        lens = rng.integers(1, Lmax + 1, size=B)
+    return q, k, v, np.asarray(lens, dtype=np.int32)
+
+
+# --------------------------------------------------------------- bf16 decode
+
+def test_bf16_widening_matches_torch():
+    rng = np.random.default_rng(1)
+    pats = rng.integers(0, 1 << 16, size=4000).astype(np.uint16)
+    # drop NaN patterns (exponent all ones, mantissa non-zero)
+    pats = pats[~(((pats & 0x7F80) == 0x7F80) & ((pats & 0x007F) != 0))]
+    special = np.array([0x0000, 0x8000, 0x3F80, 0xBF80, 0x4000, 0xC000, 0x0001,
+                        0x007F, 0x0080, 0x7F7F, 0xFF7F, 0x7F80, 0xFF80],
+                       dtype=np.uint16)
+    pats = np.concatenate([pats, special])
+    ref = unbits(pats)
+    got = np.array([oracle.bf16_to_double(int(p)) for p in pats])
+    assert np.array_equal(got, ref)
+    assert oracle.bf16_to_double(0x3F80) == 1.0
+    assert oracle.bf16_to_double(0xC000) == -2.0
+    assert oracle.bf16_to_double(0x0001) == 2.0 ** -133  # smallest subnormal
+
+
+# --------------------------------------------------------------- closed forms
+
+def test_length_one_returns_first_value_row_exactly():
+    rng = np.random.default_rng(2)
+    q, k, v, _ = rand_case(rng, 3, 8, 2, 64, 16)
+    lens = np.ones(3, dtype=np.int32)
+    out = oracle.gqa_decode(q, k, v, lens, scale=0.125)
+    G = 4
+    for b in range(3):
+        for h in range(8):
+            assert np.array_equal(out[b, h], unbits(v[b, h // G, 0]))
+
+
+def test_identical_keys_give_mean_of_values():
+    rng = np.random.default_rng(3)
+    B, Hq, Hkv, D, L = 2, 6, 3, 32, 40
+    q, k, v, _ = rand_case(rng, B, Hq, Hkv, D, L)
+    k[:] = k[:, :, :1, :]           # every position carries the same key
+    lens = np.array([40, 17], dtype=np.int32)
+    out = oracle.gqa_decode(q, k, v, lens, scale=0.3)
+    vf = unbits(v)
+    for b in range(B):
+        for h in range(Hq):
+            want = vf[b, h // 2, :lens[b]].mean(axis=0)
+            np.testing.assert_allclose(out[b, h], want, rtol=0, atol=1e-14)
+
+
+def test_one_dominant_logit_returns_that_value_row():
+    # s_{j*} exceeds every other score by >= 800, so exp(-800) underflows to
+    # zero in double and the softmax is exactly one-hot.
+    B, Hq, Hkv, D, L = 1, 2, 1, 16, 12
+    rng = np.random.default_rng(4)
+    q = np.zeros((B, Hq, D), np.float32)
+    q[0, :, 0] = 1.0
+    k = np.zeros((B, Hkv, L, D), np.float32)
+    jstar = 7
+    k[0, 0, jstar, 0] = 1024.0
+    v = rng.standard_normal((B, Hkv, L, D))
+    out = oracle.gqa_decode(bits(q), bits(k), bits(v), np.array([L], np.int32),
+                            scale=1.0)
+    for h in range(Hq):
+        assert np.array_equal(out[0, h], unbits(bits(v))[0, 0, jstar])
+
+
+@pytest.mark.parametrize("which", ["scale", "query"])
+def test_zero_logits_give_mean_of_values(which):
+    rng = np.random.default_rng(5)
+    q, k, v, lens = rand_case(rng, 2, 4, 1, 64, 30)
+    scale = 0.125
+    if which == "scale":
+        scale = 0.0
+    else:
+        q[:] = 0
+    out = oracle.gqa_decode(q, k, v, lens, scale=scale)
+    vf = unbits(v)
+    for b in range(2):
+        want = vf[b, 0, :lens[b]].mean(axis=0)
+        for h in range(4):
+            np.testing.assert_allclose(out[b, h], want, rtol=0, atol=1e-14)
+
+
+def test_two_positions_follow_the_logistic_closed_form():
+    # softmax over two scores is (sigma(s0 - s1), sigma(s1 - s0)), with sigma
+    # the logistic function (scipy's expit).
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, D, L = 2, 4, 2, 16, 5
+    q, k, v, _ = rand_case(rng, B, Hq, Hkv, D, L)
+    lens = np.full(B, 2, np.int32)
+    scale = 0.37
+    out = oracle.gqa_decode(q, k, v, lens, scale=scale)
+    qf, kf, vf = unbits(q), unbits(k), unbits(v)
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // 2
+            s0 = scale * float(np.dot(qf[b, h], kf[b, kvh, 0]))
+            s1 = scale * float(np.dot(qf[b, h], kf[b, kvh, 1]))
+            want = expit(s0 - s1) * vf[b, kvh, 0] + expit(s1 - s0) * vf[b, kvh, 1]
+            np.testing.assert_allclose(out[b, h], want, rtol=1e-13, atol=1e-14)
+
+
+def test_empty_sequence_gives_zero_row():
+    rng = np.random.default_rng(7)
+    q, k, v, _ = rand_case(rng, 3, 4, 2, 16, 8)
+    lens = np.array([0, 5, 0], np.int32)
+    out = oracle.gqa_decode(q, k, v, lens, scale=0.25)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0)
+    assert np.any(out[1] != 0)
+
+
+# --------------------------------------------------- library special case
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,Lmax", [
+    (2, 4, 1, 64, 37),      # MQA
+    (3, 8, 2, 32, 50),      # GQA, group 4
+    (2, 6, 6, 16, 21),      # MHA
+    (1, 48, 1, 256, 9),     # PaLM-540B head shape
+    (2, 64, 8, 128, 19),    # Llama-2-70B head shape
+])
+def test_matches_torch_sdpa_in_float64(B, Hq, Hkv, D, Lmax):
+    rng = np.random.default_rng(B * 1000 + Hq * 10 + D)
+    q, k, v, lens = rand_case(rng, B, Hq, Hkv, D, Lmax)
+    lens[0] = Lmax
+    scale = 1.0 / math.sqrt(D)
+    out = oracle.gqa_decode(q, k, v, lens, scale=scale)
+    qt = torch.from_numpy(unbits(q))
+    kt = torch.from_numpy(unbits(k))
+    vt = torch.from_numpy(unbits(v))
+    for b in range(B):
+        L = int(lens[b])
+        ref = F.scaled_dot_product_attention(
+            qt[b:b + 1, :, None, :], kt[b:b + 1, :, :L], vt[b:b + 1, :, :L],
+            scale=scale, enable_gqa=(Hq != Hkv))
+        np.testing.assert_allclose(out[b], ref[0, :, 0].numpy(), rtol=1e-12,
+                                   atol=1e-13)
+
+
+# ------------------------------------------------------------- brute force
+
+def test_brute_force_explicit_weights_tiny():
+    # p_j = 1 / sum_i exp(s_i - s_j): a different arrangement of the softmax,
+    # summed exactly with math.fsum, on every row of a tiny case.
+    rng = np.random.default_rng(8)
+    for trial in range(6):
+        B = int(rng.integers(1, 4)); Hkv = int(rng.integers(1, 3))
+        G = int(rng.integers(1, 3)); Hq = Hkv * G
+        D = int(rng.integers(1, 9)); Lmax = int(rng.integers(1, 9))
+        q, k, v, lens = rand_case(rng, B, Hq, Hkv, D, Lmax)
+        scale = float(rng.uniform(0.05, 1.5))
+        out = oracle.gqa_decode(q, k, v, lens, scale=scale)
+        qf, kf, vf = unbits(q), unbits(k), unbits(v)
+        for b in range(B):
+            for h in range(Hq):
+                kvh = h // G
+                L = int(lens[b])
+                s = [scale * math.fsum(qf[b, h, d] * kf[b, kvh, j, d] for d in range(D))
+                     for j in range(L)]
+                p = [1.0 / math.fsum(math.exp(s[i] - s[j]) for i in range(L))
+                     for j in range(L)]
+                for d in range(D):
+                    want = math.fsum(p[j] * vf[b, kvh, j, d] for j in range(L))
+                    assert abs(out[b, h, d] - want) <= 1e-13 * max(1.0, abs(want))
+
+
+# --------------------------------------------------------------- invariants
+
+def test_joint_permutation_of_positions_leaves_output_unchanged():
+    rng = np.random.default_rng(9)
+    q, k, v, lens = rand_case(rng, 3, 8, 2, 64, 33)
+    out = oracle.gqa_decode(q, k, v, lens, scale=0.125)
+    k2, v2 = k.copy(), v.copy()
+    for b in range(3):
+        L = int(lens[b])
+        perm = rng.permutation(L)
+        k2[b, :, :L] = k[b][:, perm]
+        v2[b, :, :L] = v[b][:, perm]
+    out2 = oracle.gqa_decode(q, k2, v2, lens, scale=0.125)
+    np.testing.assert_allclose(out2, out, rtol=1e-12, atol=1e-14)
+
+
+def test_gqa_equals_mha_with_each_kv_head_repeated_over_its_group():
+    # pins the contiguous grouping kvh = h // G (not h % Hkv)
+    rng = np.random.default_rng(10)
+    B, Hq, Hkv, D, L = 2, 12, 3, 32, 25
+    q, k, v, lens = rand_case(rng, B, Hq, Hkv, D, L)
+    k[:, 1] = bits(3.0 * unbits(k[:, 1]) + 1.0)   # make the KV heads unlike
+    out = oracle.gqa_decode(q, k, v, lens, scale=0.2)
+    G = Hq // Hkv
+    k_rep = np.repeat(k, G, axis=1)
+    v_rep = np.repeat(v, G, axis=1)
+    out_mha = oracle.gqa_decode(q, k_rep, v_rep, lens, scale=0.2)
+    assert np.array_equal(out, out_mha)
+    # and the interleaved mapping would differ
+    k_tile = np.tile(k, (1, G, 1, 1))
+    v_tile = np.tile(v, (1, G, 1, 1))
+    out_wrong = oracle.gqa_decode(q, k_tile, v_tile, lens, scale=0.2)
+    assert not np.allclose(out_wrong, out)
+
+
+def test_batch_rows_are_independent():
+    rng = np.random.default_rng(11)
+    q, k, v, lens = rand_case(rng, 4, 4, 2, 16, 20)
+    out = oracle.gqa_decode(q, k, v, lens, scale=0.25)
+    q2, k2, v2, lens2 = q.copy(), k.copy(), v.copy(), lens.copy()
+    q2[2] = bits(rng.standard_normal(q2[2].shape))
+    k2[2] = bits(rng.standard_normal(k2[2].shape))
+    v2[2] = bits(rng.standard_normal(v2[2].shape))
+    lens2[2] = 1 + (lens[2] % 20)
+    out2 = oracle.gqa_decode(q2, k2, v2, lens2, scale=0.25)
+    for b in (0, 1, 3):
+        assert np.array_equal(out[b], out2[b])
+
+
+def test_rows_past_the_length_are_never_read():
+    rng = np.random.default_rng(12)
+    q, k, v, lens = rand_case(rng, 3, 4, 1, 32, 24)
+    lens = np.array([5, 24, 1], np.int32)
+    out = oracle.gqa_decode(q, k, v, lens, scale=0.2)
+    k2, v2 = k.copy(), v.copy()
+    for b in range(3):
+        k2[b, :, lens[b]:] = 0x7FC0   # NaN
+        v2[b, :, lens[b]:] = 0x7F80   # +inf
+    out2 = oracle.gqa_decode(q, k2, v2, lens, scale=0.2)
+    assert np.array_equal(out, out2)
+
+
+def test_values_enter_linearly():
+    # scaling V by 2 (exact in bf16) doubles the output; shifting every value
+    # row by a constant vector t (small integers, exact in bf16) shifts it by t
+    rng = np.random.default_rng(13)
+    B, Hq, Hkv, D, L = 2, 4, 2, 16, 30
+    q, k, _, lens = rand_case(rng, B, Hq, Hkv, D, L)
+    vi = rng.integers(-8, 9, size=(B, Hkv, L, D)).astype(np.float32)
+    t = rng.integers(-16, 17, size=D).astype(np.float32)
+    base = oracle.gqa_decode(q, k, bits(vi), lens, scale=0.3)
+    doubled = oracle.gqa_decode(q, k, bits(2 * vi), lens, scale=0.3)
+    shifted = oracle.gqa_decode(q, k, bits(vi + t), lens, scale=0.3)
+    np.testing.assert_allclose(doubled, 2 * base, rtol=1e-14, atol=1e-13)
+    np.testing.assert_allclose(shifted, base + t, rtol=0, atol=1e-12)
+
+
+def test_output_is_a_convex_combination_of_value_rows():
+    rng = np.random.default_rng(14)
+    q, k, v, lens = rand_case(rng, 3, 8, 4, 64, 40, kmul=4.0)
+    out = oracle.gqa_decode(q, k, v, lens, scale=0.5)
+    vf = unbits(v)
+    for b in range(3):
+        for h in range(8):
+            rows = vf[b, h // 2, :lens[b]]
+            assert np.all(out[b, h] <= rows.max(axis=0) + 1e-12)
+            assert np.all(out[b, h] >= rows.min(axis=0) - 1e-12)
+
+
+# ----------------------------------------------------- bookkeeping / errors
+
+def test_pairs_threads_and_full_agree_bitwise():
+    rng = np.random.default_rng(15)
+    q, k, v, lens = rand_case(rng, 3, 8, 2, 32, 40)
+    full = oracle.gqa_decode(q, k, v, lens, scale=0.2)
+    mt = oracle.gqa_decode(q, k, v, lens, scale=0.2, nthreads=4)
+    assert np.array_equal(full, mt)
+    pairs = np.array([[0, 3], [2, 7], [1, 0]])
+    part = oracle.gqa_decode(q, k, v, lens, scale=0.2, pairs=pairs, nthreads=2)
+    for b, h in pairs:
+        assert np.array_equal(part[b, h], full[b, h])
+
+
+def test_bad_arguments_are_rejected():
+    rng = np.random.default_rng(16)
+    q, k, v, lens = rand_case(rng, 2, 6, 4, 16, 8)   # 6 % 4 != 0
+    with pytest.raises(ValueError):
+        oracle.gqa_decode(q, k, v, lens, scale=1.0)
+    q, k, v, lens = rand_case(rng, 2, 4, 2, 16, 8)
+    lens[1] = 9                                        # > Lmax
+    with pytest.raises(ValueError):
+        oracle.gqa_decode(q, k, v, lens, scale=1.0)
+    lens[1] = -1
+    with pytest.raises(ValueError):
+        oracle.gqa_decode(q, k, v, lens, scale=1.0)
+
+
+# ---------------------------------------------------------------- kv append
+
+def test_kv_append_matches_index_assignment_and_touches_nothing_else():
+    rng = np.random.default_rng(17)
+    B, Hkv, L, D = 3, 2, 10, 16
+    k = bits(rng.standard_normal((B, Hkv, L, D)))
+    v = bits(rng.standard_normal((B, Hkv, L, D)))
+    kn = bits(rng.standard_normal((B, Hkv, D)))
+    vn = bits(rng.standard_normal((B, Hkv, D)))
+    pos = np.array([0, 9, 4], np.int32)
+    k_ref, v_ref = k.copy(), v.copy()
+    k_ref[np.arange(B), :, pos] = kn          # numpy fancy indexing
+    v_ref[np.arange(B), :, pos] = vn
+    oracle.kv_append(k, v, kn, vn, pos)
+    assert np.array_equal(k, k_ref) and np.array_equal(v, v_ref)
+
+
+@pytest.mark.parametrize("bad", [-1, 10])
+def test_kv_append_rejects_rows_outside_the_cache(bad):
+    rng = np.random.default_rng(18)
+    k = bits(rng.standard_normal((2, 1, 10, 8)))
+    v = k.copy()
+    kn = bits(rng.standard_normal((2, 1, 8)))
+    before = k.copy()
+    with pytest.raises(ValueError):
+        oracle.kv_append(k, v, kn, kn, np.array([3, bad], np.int32))
+    assert np.array_equal(k, before)
