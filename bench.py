@@ -1,0 +1,429 @@
+"""Decode-attention benchmark: one step = kv_append + gqa_decode_attn over a
+seeded synthetic batch shaped like the PaLM-8B multi-query decode
+(B=64, Hq=16, Hkv=1, D=256, 2048 cached positions) unless --workload says
+otherwise.  Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--no-cpu-baseline]
+
+Metric: KV-cache bytes the attention reads per second (only positions below
+each sequence's length count), with decode sequence-steps per second beside
+it.  Timing: W untimed steps, then exactly K steps between CUDA events on the
+launching stream, each step reading a different copy of the cache (copies
+together >= 4x L2) so reads come from HBM.  Steps are replayed as CUDA graphs
+(one for the append, one for the attention call), with an event pair around
+every attention launch for the per-launch duration used by the roofline.
+Under torchrun every rank runs its own batch (weak scaling, no collective in
+the data path); the barrier and the max over ranks stay.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV-cache read GB/s (fraction of GB300 HBM peak); decode-attn seq-steps/s"
+DEFAULT_WORKLOAD = "palm8b_mqa"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------ clocks sampler
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, seed, target_s, max_seqs=None):
+    """Time the oracle (all host cores) on whole sequences of the workload.
+    Returns (seconds, sequences, kv_bytes, threads)."""
+    import dataclasses
+
+    import oracle
+    from grouped_query_kv_gb300 import accounting
+    from grouped_query_kv_gb300 import workloads as wl
+
+    threads = os.cpu_count() or 1
+    lens_all = wl.attn_lens(w, seed)
+
+    def run(nb):
+        sub = dataclasses.replace(w, B=nb, lens=None, ragged=False)
+        x = wl.make_inputs(sub, seed=seed, device="cpu", lens=lens_all[:nb])
+        q, k, v = (wl.bf16_bits(x[n]) for n in ("q", "k_cache", "v_cache"))
+        lens = x["attn_lens"].numpy()
+        t = time.perf_counter()
+        oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads)
+        dt = time.perf_counter() - t
+        return dt, accounting.kv_bytes_read(lens, w.Hkv, w.D)
+
+    dt1, by1 = run(1)
+    nb = max(1, min(w.B if max_seqs is None else max_seqs,
+                    int(math.ceil(target_s / max(dt1, 1e-6)))))
+    if nb > 1:
+        dt, by = run(nb)
+    else:
+        dt, by = dt1, by1
+    return dt, nb, by, threads
+
+
+def reference_arm(a, w):
+    """The reference arm is the CPU oracle as it stands, timed on this machine's
+    host cores over a bounded sample of the workload each step (whole
+    sequences, all heads), sized so that W + K steps take about two minutes."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    per_step = min(3.0, 120.0 / max(1, a.steps + a.warmup))
+    _, nb, _, threads = oracle_sample(w, a.seed, per_step)
+    times, by = [], 0
+    for i in range(a.warmup + a.steps):
+        dt, _, by, _ = _oracle_fixed(w, a.seed, nb, threads)
+        if i >= a.warmup:
+            times.append(dt)
+    tot = sum(times)
+    gbs = by * len(times) / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B_sampled": nb, "B": w.B, "Hq": w.Hq,
+                   "Hkv": w.Hkv, "D": w.D, "Lmax": w.Lmax},
+        "seq_steps_per_s": nb * len(times) / tot,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "%d of %d sequences (all heads) per step; %s" %
+                                   (nb, w.B, cpu_model())},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+_FIXED_CACHE = {}
+
+
+def _oracle_fixed(w, seed, nb, threads):
+    import dataclasses
+
+    import oracle
+    from grouped_query_kv_gb300 import accounting
+    from grouped_query_kv_gb300 import workloads as wl
+    key = (w.name, seed, nb)
+    if key not in _FIXED_CACHE:
+        lens_all = wl.attn_lens(w, seed)
+        sub = dataclasses.replace(w, B=nb, lens=None, ragged=False)
+        x = wl.make_inputs(sub, seed=seed, device="cpu", lens=lens_all[:nb])
+        _FIXED_CACHE[key] = tuple(wl.bf16_bits(x[n]) for n in ("q", "k_cache", "v_cache")) + \
+            (x["attn_lens"].numpy(),)
+    q, k, v, lens = _FIXED_CACHE[key]
+    t = time.perf_counter()
+    oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads)
+    return time.perf_counter() - t, nb, accounting.kv_bytes_read(lens, w.Hkv, w.D), threads
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def gpu_arm(a, w):
+    import torch
+    import torch.distributed as dist
+
+    import grouped_query_kv_gb300 as g
+    from grouped_query_kv_gb300 import accounting
+    from grouped_query_kv_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    lib = g.lib()
+    peak, peak_kind = measured_peaks()
+
+    # ---- inputs: `ncopies` caches so consecutive steps never hit in L2
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    cache_bytes = 2 * w.B * w.Hkv * w.Lmax * w.D * 2
+    ncopies = max(1, int(math.ceil(4 * l2 / cache_bytes)))
+    ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
+    x = wl.make_inputs(w, seed=a.seed + 1000 * rank, device=dev)
+    caches = [(x["k_cache"], x["v_cache"])]
+    for r in range(1, ncopies):
+        caches.append((x["k_cache"].clone(), x["v_cache"].clone()))
+    lens = x["attn_lens"]
+    pos = x["append_pos"]
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    kv_bytes = accounting.kv_bytes_read(lens.cpu().tolist(), w.Hkv, w.D)
+
+    stream = torch.cuda.Stream(device=dev)
+    sp = ctypes_void(stream.cuda_stream)
+    P = lambda t: ctypes_void(t.data_ptr())  # noqa: E731
+    q_p, kn_p, vn_p, l_p, pos_p, out_p = map(P, (x["q"], x["k_new"], x["v_new"], lens, pos, out))
+
+    def call_append(r):
+        rc = lib.kv_append(P(caches[r][0]), P(caches[r][1]), kn_p, vn_p, pos_p,
+                           w.B, w.Hkv, w.D, w.Lmax, sp)
+        assert rc == 0, lib.kvattn_last_error()
+
+    def call_attn(r):
+        rc = lib.gqa_decode_attn(q_p, P(caches[r][0]), P(caches[r][1]), l_p, out_p,
+                                 w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+        assert rc == 0, lib.kvattn_last_error()
+
+    with torch.cuda.stream(stream):
+        for r in range(ncopies):           # first calls allocate the workspace
+            call_append(r)
+            call_attn(r)
+    stream.synchronize()
+    g.check_device_error(stream)
+
+    graphs_a, graphs_b = [], []
+    for r in range(ncopies):
+        ga, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, stream=stream):
+            call_append(r)
+        with torch.cuda.graph(gb, stream=stream):
+            call_attn(r)
+        graphs_a.append(ga)
+        graphs_b.append(gb)
+    torch.cuda.synchronize(dev)
+
+    # ---- warm-up, then exactly K timed steps
+    with torch.cuda.stream(stream):
+        for i in range(a.warmup):
+            graphs_a[i % ncopies].replay()
+            graphs_b[i % ncopies].replay()
+    stream.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(a.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(a.steps):
+            r = i % ncopies
+            graphs_a[r].replay()
+            ev[i][0].record(stream)
+            graphs_b[r].replay()
+            ev[i][1].record(stream)
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    g.check_device_error(stream)
+    ms_total = t0.elapsed_time(t1)
+    attn_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / a.steps
+    value = world * kv_bytes * a.steps / (ms_total / 1e3) / 1e9
+    attn_mean = statistics.mean(attn_ms)
+    achieved = kv_bytes / (attn_mean / 1e3) / 1e9
+
+    # ---- end to end through the public Python API with host buffers
+    io = accounting.step_io_bytes(w.B, w.Hq, w.Hkv, w.D)
+    hq = x["q"].cpu().pin_memory()
+    hkn = x["k_new"].cpu().pin_memory()
+    hvn = x["v_new"].cpu().pin_memory()
+    hpos = pos.cpu().pin_memory()
+    hlens = lens.cpu().pin_memory()
+    hout = torch.empty_like(out, device="cpu").pin_memory()
+    dq, dkn, dvn = torch.empty_like(x["q"]), torch.empty_like(x["k_new"]), torch.empty_like(x["v_new"])
+    dpos, dlens = torch.empty_like(pos), torch.empty_like(lens)
+    n_e2e = max(1, a.e2e_steps)
+
+    def e2e_step(i):
+        r = i % ncopies
+        dq.copy_(hq, non_blocking=True)
+        dkn.copy_(hkn, non_blocking=True)
+        dvn.copy_(hvn, non_blocking=True)
+        dpos.copy_(hpos, non_blocking=True)
+        dlens.copy_(hlens, non_blocking=True)
+        g.kv_append(caches[r][0], caches[r][1], dkn, dvn, dpos, stream=stream)
+        g.gqa_decode_attn(dq, caches[r][0], caches[r][1], dlens, w.scale, out=out, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            e2e_step(i)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(n_e2e):
+            e2e_step(i)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_val = world * kv_bytes / (e2e_ms / 1e3) / 1e9
+    g.check_device_error(stream)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "Lmax": w.Lmax, "seq_len": int(lens.max().item()),
+                   "kv_bytes_per_step": kv_bytes,
+                   "l2": "inputs larger than L2: %d rotating cache copies, %.0f MB (%.1fx L2)"
+                         % (ncopies, ncopies * cache_bytes / 1e6, ncopies * cache_bytes / l2),
+                   "step": "kv_append + gqa_decode_attn, CUDA-graph replays",
+                   "numerics": "bf16 in, fp32 accumulate and out",
+                   "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
+        "seq_steps_per_s": world * w.B * a.steps / (ms_total / 1e3),
+        "us_per_attn_call": 1e3 * attn_mean,
+        "hbm_fraction": achieved / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "gqa_decode_attn call (split-KV kernel + combine)",
+                     "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind
+                     if peak_kind == "measured" else "fallback 6800 GB/s"},
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
+                "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms,
+                "api": "grouped_query_kv_gb300.kv_append + gqa_decode_attn (eager)"},
+        "gpu_launches": 3 * a.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not a.no_cpu_baseline:
+        dt, nb, by, threads = oracle_sample(w, a.seed, a.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": by / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d sequences (all heads), %.1f s, double precision; %s"
+                      % (nb, w.B, dt, cpu_model())}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def ctypes_void(v):
+    import ctypes
+    return ctypes.c_void_p(v)
+
+
+def main():
+    a = parse()
+    from grouped_query_kv_gb300 import workloads as wl
+    if a.workload not in wl.WORKLOADS:
+        print("unknown workload %r; one of %s" % (a.workload, ", ".join(wl.CONFIG_ORDER)),
+              file=sys.stderr)
+        return 2
+    w = wl.WORKLOADS[a.workload]
+    if a.warmup < 3:
+        a.warmup = 3
+    if a.impl == "reference":
+        return reference_arm(a, w)
+    return gpu_arm(a, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,192 @@
+"""grouped_query_kv_gb300 -- Python binding of libkvattn (GB300 decode
+attention over a grouped-query / multi-query KV cache).
+
+The binding only marshals arguments: it checks dtypes, shapes, devices and
+contiguity of torch tensors, and passes raw device pointers and the current
+CUDA stream to the C ABI declared in ``include/kvattn.h``.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback, and importing the entry points fails loudly if the compiled
+library is missing (build it with ``python -m grouped_query_kv_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "kv_append", "gqa_decode_attn", "check_device_error", "get_plan",
+    "set_tuning", "release", "KvAttnError", "library_path", "lib",
+    "KVATTN_OK", "KVATTN_ERR_INVALID_ARG", "KVATTN_ERR_UNSUPPORTED",
+    "KVATTN_ERR_CUDA", "KVATTN_ERR_OOM", "KVATTN_ERR_DEVICE_BOUNDS",
+    "KVATTN_ERR_TIMEOUT", "EXPORTED_SYMBOLS",
+]
+
+KVATTN_OK = 0
+KVATTN_ERR_INVALID_ARG = 1
+KVATTN_ERR_UNSUPPORTED = 2
+KVATTN_ERR_CUDA = 3
+KVATTN_ERR_OOM = 4
+KVATTN_ERR_DEVICE_BOUNDS = 5
+KVATTN_ERR_TIMEOUT = 6
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libkvattn.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class KvAttnError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__("%s (%d): %s" % (_status_name(status), status, detail))
+
+
+class kvattn_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("tile_positions", ctypes.c_int),
+                ("heads_per_cta", ctypes.c_int), ("head_groups", ctypes.c_int),
+                ("stages", ctypes.c_int), ("threads", ctypes.c_int),
+                ("num_ctas", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_int64)]
+
+
+# name -> (restype, argtypes); mirrors include/kvattn.h
+_VP = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "kv_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    "gqa_decode_attn": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
+                             ctypes.c_float, _VP]),
+    "kvattn_status_string": (ctypes.c_char_p, [_I]),
+    "kvattn_last_error": (ctypes.c_char_p, []),
+    "kvattn_check_device_error": (_I, [_VP]),
+    "kvattn_release": (None, []),
+    "kvattn_set_tuning": (_I, [_I, _I]),
+    "kvattn_get_plan": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(kvattn_plan)]),
+}
+EXPORTED_SYMBOLS = tuple(_SIGS)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(
+                    "libkvattn.so is not built (%s); run "
+                    "`python -m grouped_query_kv_gb300.build`" % _LIB_PATH)
+            h = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+    return _lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return lib().kvattn_status_string(status).decode()
+    except Exception:  # library not loadable: still give a readable error
+        return "status"
+
+
+def _check(status: int):
+    if status != KVATTN_OK:
+        raise KvAttnError(status, lib().kvattn_last_error().decode())
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor (got %s)" % (name, t.device))
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, seq_lens, stream=None):
+    """Write the new token's K/V rows into row seq_lens[b] of the caches.
+
+    k_cache, v_cache: bf16 [B, Hkv, Lmax, D] (in place); k_new, v_new: bf16
+    [B, Hkv, D]; seq_lens: int32 [B], tokens cached before this one (not
+    modified).
+    """
+    import torch
+    _need(k_cache, "k_cache", torch.bfloat16)
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must be [B, Hkv, Lmax, D]")
+    B, Hkv, Lmax, D = k_cache.shape
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lmax, D))
+    _need(k_new, "k_new", torch.bfloat16, (B, Hkv, D))
+    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    _check(lib().kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                           _ptr(seq_lens), B, Hkv, D, Lmax, _stream_ptr(stream)))
+
+
+def gqa_decode_attn(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None):
+    """out[b,h] = softmax(scale * q[b,h] . K[b,h//G]^T) . V[b,h//G] over the
+    first seq_lens[b] cached positions.
+
+    q: bf16 [B, Hq, D]; caches: bf16 [B, Hkv, Lmax, D]; seq_lens: int32 [B];
+    out: optional fp32 [B, Hq, D] (allocated if None).  Returns out.
+    """
+    import torch
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    B, Hq, D = q.shape
+    _need(k_cache, "k_cache", torch.bfloat16)
+    if k_cache.dim() != 4 or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError("k_cache must be [B, Hkv, Lmax, D] matching q")
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lmax, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, (B, Hq, D))
+    _check(lib().gqa_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                 _ptr(out), B, Hq, Hkv, D, Lmax, float(scale),
+                                 _stream_ptr(stream)))
+    return out
+
+
+def check_device_error(stream=None):
+    """Synchronise the stream and raise KvAttnError if the device flagged one."""
+    _check(lib().kvattn_check_device_error(_stream_ptr(stream)))
+
+
+def get_plan(B, Hq, Hkv, D, Lmax, num_sms=0) -> dict:
+    p = kvattn_plan()
+    _check(lib().kvattn_get_plan(B, Hq, Hkv, D, Lmax, num_sms, ctypes.byref(p)))
+    return {name: getattr(p, name) for name, _ in kvattn_plan._fields_}
+
+
+def set_tuning(force_path: int = 0, num_ctas: int = 0):
+    _check(lib().kvattn_set_tuning(force_path, num_ctas))
+
+
+def release():
+    lib().kvattn_release()

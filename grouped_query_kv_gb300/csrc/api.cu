@@ -1,0 +1,330 @@
+// api.cu -- the C ABI declared in include/kvattn.h: argument checks, the
+// split plan, TMA descriptors, per-(device, stream) workspaces and launches.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/kvattn.h"
+#include "internal.h"
+
+using namespace kvattn;
+
+// The sticky device error word (one copy per device, as for every __device__
+// variable).  Kernels receive its address as a plain pointer.
+__device__ unsigned int g_kvattn_device_error;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+int fail(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(KVATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::mutex g_mu;
+int g_force_path = 0;
+int g_force_ctas = 0;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    unsigned int *err = nullptr;
+};
+std::map<int, DeviceState> g_dev;
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+// cuTensorMapEncodeTiled, fetched through the runtime so the library needs no
+// link-time dependency on the driver library.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    return KVATTN_OK;
+}
+
+// Per-device lazy set-up (under g_mu).
+int device_state(int dev, DeviceState **out) {
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        cudaError_t e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&s.err), g_kvattn_device_error);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        s.ready = true;
+    }
+    *out = &s;
+    return KVATTN_OK;
+}
+
+int get_encoder() {
+    if (g_encode) return KVATTN_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(KVATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return KVATTN_OK;
+}
+
+// 3-D map over one cache: dims (D, Lmax, B*Hkv), box (64, tile, 1),
+// 128-byte swizzle; rows past Lmax read as zeros.
+int encode_cache_map(CUtensorMap *m, const void *base, int D, int Lmax, int BH, int tile) {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Lmax, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * (cuuint64_t)Lmax};
+    cuuint32_t box[3] = {64, (cuuint32_t)tile, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return KVATTN_OK;
+}
+
+struct Plan {
+    kvattn_plan pub;
+    int heads_per_seg;
+};
+
+int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
+    (void)Lmax;
+    const int G = Hq / Hkv;
+    kvattn_plan &p = pl->pub;
+    memset(&p, 0, sizeof p);
+    p.path = 1;
+    pl->heads_per_seg = fma_heads_per_seg(G);
+    p.heads_per_cta = pl->heads_per_seg;
+    p.head_groups = (G + pl->heads_per_seg - 1) / pl->heads_per_seg;
+    p.tile_positions = fma_tile(D);
+    p.stages = fma_stages(D);
+    p.threads = fma_threads();
+    p.smem_bytes = fma_smem_bytes(D, pl->heads_per_seg);
+    int ctas = g_force_ctas > 0 ? g_force_ctas : num_sms;
+    p.num_ctas = ctas;
+    p.workspace_bytes = (int64_t)2 * ctas * pl->heads_per_seg * (D + 2) * (int64_t)sizeof(float);
+    (void)B;
+    return KVATTN_OK;
+}
+
+int check_sizes(int B, int Hq, int Hkv, int D, int Lmax) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0)
+        return fail(KVATTN_ERR_INVALID_ARG, "sizes must be positive (B=%d Hq=%d Hkv=%d D=%d Lmax=%d)",
+                    B, Hq, Hkv, D, Lmax);
+    if (Hq % Hkv != 0)
+        return fail(KVATTN_ERR_INVALID_ARG, "Hq (%d) is not a multiple of Hkv (%d)", Hq, Hkv);
+    if (D != 64 && D != 128 && D != 256)
+        return fail(KVATTN_ERR_UNSUPPORTED, "head dimension D=%d not in {64, 128, 256}", D);
+    if (B > 65535 || Hkv > 4096 || Hq > 8192 || Lmax > (1 << 24))
+        return fail(KVATTN_ERR_UNSUPPORTED,
+                    "sizes beyond limits (B<=65535, Hkv<=4096, Hq<=8192, Lmax<=2^24)");
+    return KVATTN_OK;
+}
+
+int get_workspace(int dev, cudaStream_t stream, size_t bytes, void **ptr) {
+    Workspace &w = g_ws[std::make_pair(dev, stream)];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            cudaError_t e = cudaFree(w.ptr);  // synchronises the device first
+            w.ptr = nullptr;
+            w.bytes = 0;
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+        }
+        size_t want = bytes < (1u << 20) ? (1u << 20) : bytes;
+        cudaError_t e = cudaMalloc(&w.ptr, want);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            (void)cudaGetLastError();
+            return fail(KVATTN_ERR_OOM, "workspace allocation of %zu bytes failed", want);
+        }
+        w.bytes = want;
+    }
+    *ptr = w.ptr;
+    return KVATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvattn_status_string(int status) {
+    switch (status) {
+        case KVATTN_OK: return "KVATTN_OK";
+        case KVATTN_ERR_INVALID_ARG: return "KVATTN_ERR_INVALID_ARG";
+        case KVATTN_ERR_UNSUPPORTED: return "KVATTN_ERR_UNSUPPORTED";
+        case KVATTN_ERR_CUDA: return "KVATTN_ERR_CUDA";
+        case KVATTN_ERR_OOM: return "KVATTN_ERR_OOM";
+        case KVATTN_ERR_DEVICE_BOUNDS: return "KVATTN_ERR_DEVICE_BOUNDS";
+        case KVATTN_ERR_TIMEOUT: return "KVATTN_ERR_TIMEOUT";
+        default: return "KVATTN_ERR_UNKNOWN";
+    }
+}
+
+const char *kvattn_last_error(void) { return t_last_error; }
+
+int kvattn_set_tuning(int force_path, int num_ctas) {
+    if (force_path < 0 || force_path > 2 || num_ctas < 0 || num_ctas > 65535)
+        return fail(KVATTN_ERR_INVALID_ARG, "kvattn_set_tuning: value out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_force_path = force_path;
+    g_force_ctas = num_ctas;
+    return KVATTN_OK;
+}
+
+int kvattn_get_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, kvattn_plan *plan) {
+    t_last_error[0] = 0;
+    if (!plan) return fail(KVATTN_ERR_INVALID_ARG, "plan is null");
+    int rc = check_sizes(B, Hq, Hkv, D, Lmax);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (num_sms <= 0) {
+        int dev;
+        if ((rc = current_device(&dev))) return rc;
+        DeviceState *ds;
+        if ((rc = device_state(dev, &ds))) return rc;
+        num_sms = ds->num_sms;
+    }
+    Plan pl;
+    if ((rc = make_plan(B, Hq, Hkv, D, Lmax, num_sms, &pl))) return rc;
+    *plan = pl.pub;
+    return KVATTN_OK;
+}
+
+int kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+              const int32_t *seq_lens, int B, int Hkv, int D, int Lmax, kvattn_stream_t stream) {
+    t_last_error[0] = 0;
+    if (!k_cache || !v_cache || !k_new || !v_new || !seq_lens)
+        return fail(KVATTN_ERR_INVALID_ARG, "kv_append: null pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(KVATTN_ERR_INVALID_ARG, "kv_append: pointers must be 16-byte aligned");
+    int rc = check_sizes(B, Hkv, Hkv, D, Lmax);
+    if (rc) return rc;
+    int dev;
+    if ((rc = current_device(&dev))) return rc;
+    DeviceState *ds;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if ((rc = device_state(dev, &ds))) return rc;
+    }
+    cudaError_t e = launch_kv_append(k_cache, v_cache, k_new, v_new, seq_lens, B, Hkv, D, Lmax,
+                                     ds->err, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    return KVATTN_OK;
+}
+
+int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *seq_lens, float *out, int B, int Hq, int Hkv, int D, int Lmax,
+                    float scale, kvattn_stream_t stream_) {
+    t_last_error[0] = 0;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out)
+        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_attn: null pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_attn: pointers must be 16-byte aligned");
+    if (!std::isfinite(scale))
+        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_attn: scale must be finite");
+    int rc = check_sizes(B, Hq, Hkv, D, Lmax);
+    if (rc) return rc;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    int dev;
+    if ((rc = current_device(&dev))) return rc;
+    DeviceState *ds;
+    Plan pl;
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if ((rc = device_state(dev, &ds))) return rc;
+        if ((rc = get_encoder())) return rc;
+        if ((rc = make_plan(B, Hq, Hkv, D, Lmax, ds->num_sms, &pl))) return rc;
+        if ((rc = get_workspace(dev, stream, (size_t)pl.pub.workspace_bytes, &ws))) return rc;
+    }
+    const kvattn_plan &P = pl.pub;
+
+    CUtensorMap tmk, tmv;
+    if ((rc = encode_cache_map(&tmk, k_cache, D, Lmax, B * Hkv, P.tile_positions))) return rc;
+    if ((rc = encode_cache_map(&tmv, v_cache, D, Lmax, B * Hkv, P.tile_positions))) return rc;
+
+    DecodeParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.ws_o = static_cast<float *>(ws);
+    p.ws_ml = p.ws_o + (size_t)2 * P.num_ctas * pl.heads_per_seg * D;
+    p.err = ds->err;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.Lmax = Lmax;
+    p.G = Hq / Hkv;
+    p.heads_per_seg = pl.heads_per_seg;
+    p.head_groups = P.head_groups;
+    p.tile = P.tile_positions;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+
+    cudaError_t e = fma_prepare(D, pl.heads_per_seg, P.smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    e = launch_decode_fma(tmk, tmv, p, P.num_ctas, P.smem_bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    e = launch_combine(p, P.num_ctas, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    return KVATTN_OK;
+}
+
+int kvattn_check_device_error(kvattn_stream_t stream) {
+    t_last_error[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_kvattn_device_error, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_kvattn_device_error, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        return fail((int)word, "device reported %s", kvattn_status_string((int)word));
+    }
+    return KVATTN_OK;
+}
+
+void kvattn_release(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto &kv : g_ws) {
+        if (kv.second.ptr) {
+            cudaSetDevice(kv.first.first);
+            cudaFree(kv.second.ptr);
+        }
+    }
+    g_ws.clear();
+    cudaSetDevice(cur);
+}
+
+}  // extern "C"

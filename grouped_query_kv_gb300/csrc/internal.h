@@ -1,0 +1,59 @@
+// internal.h -- declarations shared by the library's translation units
+// (host launchers and the parameter blocks the kernels receive).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace kvattn {
+
+// Error codes written into the sticky per-device word (same values as the
+// public kvattn_status enum).
+enum : unsigned int { DEV_ERR_BOUNDS = 5u, DEV_ERR_TIMEOUT = 6u };
+
+// One decode-attention call, as the split-KV kernels and the combine see it.
+//
+// Work decomposition ("segments" and "tiles").  A segment is one
+// (sequence b, K/V head kvh, head group hg): the query heads
+// [kvh*G + hg*heads_per_seg, ...) that read K/V head kvh.  Segment (b,kvh,hg)
+// owns ntiles(b) = max(1, ceil(len_b / tile)) tiles of `tile` consecutive
+// cached positions.  All tiles of all segments, in (b, kvh, hg, t) order,
+// form one flat list that is cut into num_ctas equal contiguous ranges, one
+// per CTA of the persistent grid.  A segment cut by a range boundary is
+// computed in pieces whose (m, l, o) partials go to the workspace and are
+// merged by the combine kernel.
+struct DecodeParams {
+    const uint16_t *q;        // bf16 [B, Hq, D]
+    const int32_t *seq_lens;  // [B]
+    float *out;               // [B, Hq, D]
+    float *ws_o;              // [2*num_ctas, heads_per_seg, D]  partial o (unnormalised)
+    float *ws_ml;             // [2*num_ctas, heads_per_seg, 2]  partial (m, l), m in log2 units
+    unsigned int *err;        // sticky device error word
+    int B, Hq, Hkv, D, Lmax;
+    int G;                    // Hq / Hkv
+    int heads_per_seg;        // query heads one segment serves
+    int head_groups;          // ceil(G / heads_per_seg)
+    int tile;                 // positions per tile
+    float scale_log2;         // scale * log2(e)
+};
+
+// Host launchers (return cudaError_t of the launch).
+cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                             const int32_t *seq_lens, int B, int Hkv, int D, int Lmax,
+                             unsigned int *err, cudaStream_t stream);
+
+// FMA split-KV kernel; heads_per_seg must be the value plan_fma() returned.
+cudaError_t launch_decode_fma(const CUtensorMap &tmk, const CUtensorMap &tmv,
+                              const DecodeParams &p, int num_ctas, int smem_bytes,
+                              cudaStream_t stream);
+int fma_heads_per_seg(int G);
+int fma_tile(int D);
+int fma_stages(int D);
+int fma_smem_bytes(int D, int heads_per_seg);
+int fma_threads();
+cudaError_t fma_prepare(int D, int heads_per_seg, int smem_bytes);
+
+cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream);
+
+}  // namespace kvattn

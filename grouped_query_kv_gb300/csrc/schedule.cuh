@@ -1,0 +1,147 @@
+// schedule.cuh -- the persistent grid's split of the flat tile list.
+//
+// Every segment (b, kvh, hg) owns ntiles(len_b) tiles; the list of all tiles
+// in (b, kvh, hg, t) order is cut into ctas_eff = min(gridDim.x, total)
+// contiguous ranges [c*total/ctas_eff, (c+1)*total/ctas_eff).  Because
+// ctas_eff <= total, every range is non-empty.  Lengths live on the device,
+// so each CTA locates its own start with a block-wide scan over seq_lens (no
+// host synchronisation; ragged batches balance to within one tile per CTA).
+#pragma once
+
+#include <cstdint>
+#include "internal.h"
+
+namespace kvattn {
+
+// A sequence whose length is outside [1, Lmax] still owns one tile, with no
+// valid positions (zero output row; out-of-range lengths also raise the
+// device error word).
+__device__ __forceinline__ int seq_ntiles(int len, int Lmax, int tile) {
+    return (len <= 0 || len > Lmax) ? 1 : (len + tile - 1) / tile;
+}
+
+__device__ __forceinline__ int seq_valid_len(int len, int Lmax) {
+    return (len < 0 || len > Lmax) ? 0 : len;
+}
+
+struct SchedStart {
+    long long total;    // tiles in the whole call
+    long long g_begin;  // this CTA's first tile
+    long long g_end;    // one past its last tile
+    int ctas_eff;
+    int found;          // 1 if this CTA has work
+    int b, seg, t;      // coordinates of g_begin: sequence, segment within b, tile
+};
+
+struct SchedScratch {
+    long long part[32];
+    SchedStart res;
+};
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ long long warp_incl_scan_ll(long long v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// Locate CTA `c`'s tile range.  Every thread of the block must call it
+// (blockDim.x a multiple of 32, at most 1024); the result is left in sh->res.
+__device__ inline void sched_locate(const int32_t *__restrict__ lens, int B, int Lmax, int tile,
+                             int segs_per_b, int c, int grid, SchedScratch *sh) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+
+    long long mine = 0;
+    for (int b = tid; b < B; b += nthr) mine += seq_ntiles(lens[b], Lmax, tile);
+    mine = warp_sum_ll(mine);
+    if (lane == 0) sh->part[warp] = mine;
+    __syncthreads();
+    if (tid == 0) {
+        long long tot = 0;
+        for (int w = 0; w < nwarps; ++w) tot += sh->part[w];
+        tot *= segs_per_b;
+        SchedStart r;
+        r.total = tot;
+        r.ctas_eff = (int)(tot < (long long)grid ? tot : (long long)grid);
+        r.found = 0;
+        r.b = r.seg = r.t = 0;
+        if (c < r.ctas_eff) {
+            r.g_begin = (long long)c * tot / r.ctas_eff;
+            r.g_end = (long long)(c + 1) * tot / r.ctas_eff;
+        } else {
+            r.g_begin = r.g_end = tot;
+        }
+        sh->res = r;
+    }
+    __syncthreads();
+    const long long g_begin = sh->res.g_begin;
+    const bool active = c < sh->res.ctas_eff;
+    __syncthreads();
+    if (!active) return;
+
+    long long carry = 0;
+    for (int base = 0; base < B; base += nthr) {
+        const int b = base + tid;
+        const int nt = (b < B) ? seq_ntiles(lens[b], Lmax, tile) : 0;
+        const long long v = (long long)nt * segs_per_b;
+        const long long incl = warp_incl_scan_ll(v);
+        if (lane == 31) sh->part[warp] = incl;
+        __syncthreads();
+        long long woff = 0, chunk = 0;
+        for (int w = 0; w < nwarps; ++w) {
+            const long long pw = sh->part[w];
+            if (w < warp) woff += pw;
+            chunk += pw;
+        }
+        const long long excl = carry + woff + incl - v;
+        if (b < B && excl <= g_begin && g_begin < excl + v) {
+            const long long rem = g_begin - excl;
+            sh->res.b = b;
+            sh->res.seg = (int)(rem / nt);
+            sh->res.t = (int)(rem % nt);
+            sh->res.found = 1;
+        }
+        __syncthreads();
+        carry += chunk;
+        if (carry > g_begin) break;  // uniform: carry is the same in every thread
+    }
+    __syncthreads();
+}
+
+// Walks the tile list in the same order in every thread that uses it.
+struct TileIter {
+    const int32_t *lens;
+    int B, Lmax, tile, segs_per_b;
+    int b, seg, t, nt, len;
+
+    __device__ __forceinline__ void init(const int32_t *lens_, int B_, int Lmax_, int tile_,
+                                         int segs_per_b_, const SchedStart &s) {
+        lens = lens_; B = B_; Lmax = Lmax_; tile = tile_; segs_per_b = segs_per_b_;
+        b = s.b; seg = s.seg; t = s.t;
+        len = lens[b];
+        nt = seq_ntiles(len, Lmax, tile);
+    }
+    __device__ __forceinline__ bool last_tile_of_segment() const { return t == nt - 1; }
+    __device__ __forceinline__ void next() {
+        if (++t < nt) return;
+        t = 0;
+        if (++seg < segs_per_b) return;
+        seg = 0;
+        if (++b < B) {
+            len = lens[b];
+            nt = seq_ntiles(len, Lmax, tile);
+        }
+    }
+};
+
+}  // namespace kvattn

@@ -1,0 +1,172 @@
+/*
+ * kvattn.h -- C ABI of libkvattn: the generation-phase (decode) attention
+ * step over a grouped-query / multi-query KV cache, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation.  During generation each sequence adds one token per step.
+ * Its key and value projections are written into a per-layer KV cache, and
+ * its query then forms q_i . k_j products against every cached key without
+ * recomputing earlier tokens ("The Basics of Transformer Inference" -- How To
+ * Scale Your Model, part 7 -- the paragraph that introduces the KV cache).
+ * Each query head runs its own softmax and its own weighted sum of values
+ * ("Tensor Parallelism: Splitting Operations Across GPUs", section
+ * "Splitting attention by head, and why decode is where it hurts").  Query
+ * heads are grouped onto shared K/V heads in contiguous groups of
+ * G = Hq / Hkv ("Tensor Parallelism ...", section "The GQA ceiling: a worked
+ * memory audit"; multi-query attention, Hkv = 1, in "Efficiently Scaling
+ * Transformer Inference", section 3 "Attention Layer Partitioning"):
+ *
+ *     kvh        = h / G
+ *     s_j        = scale * sum_d q[b,h,d] * K[b,kvh,j,d],  0 <= j < seq_lens[b]
+ *     out[b,h,:] = sum_j softmax_j(s) * V[b,kvh,j,:]
+ *
+ * Only the non-padding part of each sequence's cache is read ("The Basics of
+ * Transformer Inference", item "Using ragged HBM reads and Paged Attention").
+ *
+ * Conventions for every call below.
+ *  - All tensor arguments are DEVICE pointers to contiguous row-major memory
+ *    owned by the caller.  The library never frees or retains them beyond the
+ *    call's stream work.
+ *  - bf16 is IEEE binary32's upper 16 bits (passed as void*); fp32 is float.
+ *  - Every pointer must be 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream) and do
+ *    not synchronise the host, except that the first attention call on a
+ *    (device, stream) pair, or a call needing a larger workspace than any
+ *    before on that pair, allocates device memory (cudaMalloc; it may
+ *    serialise with other device work).  Make such a first call before
+ *    capturing a stream into a CUDA graph.
+ *  - Host-detected errors return a non-zero kvattn_status and launch nothing;
+ *    kvattn_last_error() then gives a one-line reason (thread-local).
+ *  - Device-detected errors (a length outside the cache) never fault or trap:
+ *    the offending sequence is skipped and a sticky per-device error word is
+ *    set, read and cleared by kvattn_check_device_error().
+ *  - Thread-safe: internal caches are guarded by a mutex.  Calls on the same
+ *    stream run in order; calls on different streams use separate
+ *    workspaces.
+ */
+#ifndef KVATTN_H
+#define KVATTN_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVATTN_API __attribute__((visibility("default")))
+#else
+#define KVATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, spelled without CUDA headers. */
+typedef struct CUstream_st *kvattn_stream_t;
+
+typedef enum {
+    KVATTN_OK = 0,
+    KVATTN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, Hq % Hkv != 0, non-finite scale */
+    KVATTN_ERR_UNSUPPORTED = 2,   /* D not in {64, 128, 256}, or sizes beyond the library's limits */
+    KVATTN_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (see kvattn_last_error) */
+    KVATTN_ERR_OOM = 4,           /* workspace allocation failed */
+    KVATTN_ERR_DEVICE_BOUNDS = 5, /* device saw seq_lens[b] outside the cache (sticky word) */
+    KVATTN_ERR_TIMEOUT = 6        /* a bounded device wait gave up (sticky word) */
+} kvattn_status;
+
+/*
+ * kv_append -- write this step's new key/value rows into the cache.
+ *
+ * Follows "The Basics of Transformer Inference", the KV-cache paragraph:
+ * each token's key and value projections are written into the cache once.
+ *
+ *   k_cache, v_cache : bf16 [B, Hkv, Lmax, D], modified in place
+ *   k_new, v_new     : bf16 [B, Hkv, D], the new token's rows
+ *   seq_lens         : int32 [B] (device), the number of tokens cached
+ *                      BEFORE this one; row seq_lens[b] is written.  The
+ *                      array is not modified -- the caller advances it.
+ *   B, Hkv, D, Lmax  : sizes; D in {64, 128, 256}
+ *
+ * Bit-exact copy; nothing outside row seq_lens[b] of each (b, kvh) changes.
+ * A sequence with seq_lens[b] < 0 or >= Lmax is skipped on the device and
+ * sets KVATTN_ERR_DEVICE_BOUNDS in the sticky error word.
+ */
+KVATTN_API int kv_append(void *k_cache, void *v_cache, const void *k_new,
+              const void *v_new, const int32_t *seq_lens, int B, int Hkv,
+              int D, int Lmax, kvattn_stream_t stream);
+
+/*
+ * gqa_decode_attn -- one decode step of grouped-query attention.
+ *
+ * Computes, for every sequence b and query head h (kvh = h / (Hq / Hkv)),
+ *   out[b,h,:] = softmax_j(scale * q[b,h,:] . K[b,kvh,j,:]) . V[b,kvh,j,:]
+ * over positions 0 <= j < seq_lens[b] (see the header comment for the
+ * passages this follows).
+ *
+ *   q                : bf16 [B, Hq, D]
+ *   k_cache, v_cache : bf16 [B, Hkv, Lmax, D]
+ *   seq_lens         : int32 [B] (device), positions attended per sequence,
+ *                      0 <= seq_lens[b] <= Lmax (after this step's append)
+ *   out              : fp32 [B, Hq, D], written in full
+ *   B, Hq, Hkv, D    : sizes; Hq % Hkv == 0; D in {64, 128, 256}
+ *   Lmax             : positions allocated per (b, kvh) in the caches
+ *   scale            : finite softmax scale (typically 1/sqrt(D))
+ *
+ * A sequence with seq_lens[b] == 0 gets an all-zero output row.  One with
+ * seq_lens[b] outside [0, Lmax] gets an all-zero row and sets
+ * KVATTN_ERR_DEVICE_BOUNDS in the sticky error word.
+ * Limits: B <= 65535, Hkv <= 4096, Hq <= 8192, Lmax <= 2^24.
+ */
+KVATTN_API int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *seq_lens, float *out, int B, int Hq,
+                    int Hkv, int D, int Lmax, float scale,
+                    kvattn_stream_t stream);
+
+/* Static string naming a status code. */
+KVATTN_API const char *kvattn_status_string(int status);
+
+/* Detail of the last host-side error on the calling thread ("" if none). */
+KVATTN_API const char *kvattn_last_error(void);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's sticky
+ * error word (KVATTN_OK if no device-side error was seen since the last
+ * check), or KVATTN_ERR_CUDA if synchronisation itself failed.
+ */
+KVATTN_API int kvattn_check_device_error(kvattn_stream_t stream);
+
+/*
+ * Frees every workspace the library holds on every device (after a device
+ * synchronisation).  Later calls allocate again on demand.
+ */
+KVATTN_API void kvattn_release(void);
+
+/*
+ * Test and ablation knobs (process-wide; 0 restores the automatic choice).
+ *   force_path : 0 auto, 1 CUDA-core FMA kernel, 2 tensor-core kernel
+ *   num_ctas   : 0 auto, else the persistent grid size of the attention
+ *                kernel (a small value forces long multi-CTA splits)
+ * Returns KVATTN_ERR_INVALID_ARG for values out of range.
+ */
+KVATTN_API int kvattn_set_tuning(int force_path, int num_ctas);
+
+/* How a call with these sizes would run (host-side planning only; no GPU
+ * work).  num_sms <= 0 queries the current device. */
+typedef struct {
+    int path;            /* 1 FMA, 2 tensor core */
+    int tile_positions;  /* positions per pipeline tile */
+    int heads_per_cta;   /* query heads one CTA pass serves */
+    int head_groups;     /* passes per (b, kvh): ceil(G / heads_per_cta) */
+    int stages;          /* shared-memory pipeline depth */
+    int threads;         /* threads per CTA */
+    int num_ctas;        /* persistent grid size */
+    int smem_bytes;      /* dynamic shared memory per CTA */
+    int64_t workspace_bytes; /* partial (m, l, o) buffer this call needs */
+} kvattn_plan;
+
+KVATTN_API int kvattn_get_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms,
+                    kvattn_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVATTN_H */

@@ -1,0 +1,143 @@
+"""GPU parity: the CUDA path through the C ABI against the double oracle on
+the same seeded inputs.  kv_append must be bit-exact (the whole caches are
+compared, so every row it must not touch is checked too); attention must be
+within max|err| <= 2e-3 and <= 1e-2 * max|V|."""
+import numpy as np
+import pytest
+import torch
+
+import grouped_query_kv_gb300 as g
+import oracle
+from grouped_query_kv_gb300 import workloads as wl
+
+from helpers import assert_close, bits, oracle_threads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from grouped_query_kv_gb300 import build
+    build.build()
+    oracle.build()
+    g.set_tuning(0, 0)
+    yield
+    g.set_tuning(0, 0)
+
+
+def run_step(w, seed=0, lens=None, sample_b=None):
+    """kv_append then gqa_decode_attn on the GPU (whole batch), compared with
+    the oracle on every sequence, or on the sequences listed in sample_b."""
+    dev = torch.device("cuda")
+    x = wl.make_inputs(w, seed=seed, device=dev, lens=lens)
+    bsel = list(range(w.B)) if sample_b is None else sorted(int(b) for b in sample_b)
+    idx = torch.tensor(bsel, device=dev)
+    k_ref = bits(x["k_cache"].index_select(0, idx))
+    v_ref = bits(x["v_cache"].index_select(0, idx))
+    pos = x["append_pos"].cpu().numpy()[bsel]
+    oracle.kv_append(k_ref, v_ref, bits(x["k_new"])[bsel], bits(x["v_new"])[bsel], pos)
+    g.kv_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], x["append_pos"])
+    out = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale)
+    g.check_device_error()
+    assert np.array_equal(bits(x["k_cache"].index_select(0, idx)), k_ref), "kv_append: K differs"
+    assert np.array_equal(bits(x["v_cache"].index_select(0, idx)), v_ref), "kv_append: V differs"
+    lens_np = x["attn_lens"].cpu().numpy()[bsel]
+    ref = oracle.gqa_decode(bits(x["q"])[bsel], k_ref, v_ref, lens_np, w.scale,
+                            nthreads=oracle_threads())
+    return assert_close(out.index_select(0, idx), ref, v_ref, lens_np)
+
+
+def test_tiny_mqa_append_then_attend():
+    run_step(wl.WORKLOADS["tiny_mqa"])
+
+
+@pytest.mark.parametrize("name", ["palm8b_mqa", "llama70b_gqa_ragged", "palm540b_long_mqa"])
+def test_full_size_configs_every_output(name):
+    run_step(wl.WORKLOADS[name])
+
+
+@pytest.mark.parametrize("name", [n for n in wl.CONFIG_ORDER if n.startswith("sweep")])
+def test_sweep_points(name):
+    w = wl.WORKLOADS[name]
+    if w.B * w.Hkv * w.Lmax * w.D * 2 * 2 > (1 << 30):
+        rng = np.random.default_rng(1)
+        run_step(w, sample_b=rng.choice(w.B, 4, replace=False))
+    else:
+        run_step(w)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (6, 3), (12, 4), (20, 4), (16, 2), (48, 1), (64, 8)])
+def test_head_shapes_and_ragged_edges(D, Hq, Hkv):
+    # lengths around tile boundaries (64 / 128 positions), 1, and Lmax
+    Lmax = 300
+    lens = [1, 63, 64, 65, 127, 128, 129, 300, 255, 2][: 10]
+    w = wl.Workload("edge", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, Lmax=Lmax,
+                    scale=1.0 / np.sqrt(D), lens=tuple(lens))
+    run_step(w, seed=D + Hq)
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 5, 17, 152, 1000])
+def test_split_pieces_combine_for_any_grid(ctas):
+    # forcing the persistent grid size moves the cuts between CTAs, so
+    # segments get split into 1..many pieces and merged by the combine
+    w = wl.Workload("split", B=5, Hq=16, Hkv=2, D=128, Lmax=2000, scale=0.09,
+                    lens=(2000, 1, 700, 1333, 129))
+    g.set_tuning(0, ctas)
+    try:
+        run_step(w, seed=ctas)
+    finally:
+        g.set_tuning(0, 0)
+
+
+def test_empty_sequences_give_zero_rows():
+    dev = torch.device("cuda")
+    w = wl.Workload("empty", B=3, Hq=8, Hkv=2, D=128, Lmax=256, scale=0.1, lens=(5, 5, 5))
+    x = wl.make_inputs(w, seed=3, device=dev)
+    lens = torch.tensor([0, 17, 0], dtype=torch.int32, device=dev)
+    out = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], lens, w.scale)
+    g.check_device_error()
+    o = out.cpu()
+    assert torch.all(o[0] == 0) and torch.all(o[2] == 0)
+    ref = oracle.gqa_decode(bits(x["q"]), bits(x["k_cache"]), bits(x["v_cache"]),
+                            lens.cpu().numpy(), w.scale)
+    assert_close(out, ref, bits(x["v_cache"]), [0, 17, 0])
+
+
+def test_out_of_range_lengths_are_flagged_not_faulted():
+    dev = torch.device("cuda")
+    w = wl.Workload("bad", B=3, Hq=4, Hkv=1, D=64, Lmax=64, scale=0.1, lens=(5, 5, 5))
+    x = wl.make_inputs(w, seed=4, device=dev)
+    bad = torch.tensor([10, 65, -3], dtype=torch.int32, device=dev)
+    out = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], bad, w.scale)
+    with pytest.raises(g.KvAttnError) as ei:
+        g.check_device_error()
+    assert ei.value.status == g.KVATTN_ERR_DEVICE_BOUNDS
+    o = out.cpu()
+    assert torch.all(o[1] == 0) and torch.all(o[2] == 0)
+    g.check_device_error()  # the word was cleared
+    # append past the end: skipped, flagged, cache untouched
+    before = bits(x["k_cache"])
+    g.kv_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"],
+                torch.tensor([64, 0, 63], dtype=torch.int32, device=dev))
+    with pytest.raises(g.KvAttnError):
+        g.check_device_error()
+    after = bits(x["k_cache"])
+    assert np.array_equal(after[0], before[0])
+    assert np.array_equal(after[1, :, 0], bits(x["k_new"])[1])
+    assert np.array_equal(after[2, :, 63], bits(x["k_new"])[2])
+
+
+def test_side_stream_and_repeatability():
+    dev = torch.device("cuda")
+    w = wl.Workload("rep", B=4, Hq=32, Hkv=4, D=128, Lmax=1024, scale=0.088,
+                    lens=(1024, 77, 512, 900))
+    x = wl.make_inputs(w, seed=5, device=dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        a = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale)
+        b = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale)
+    s.synchronize()
+    g.check_device_error(s)
+    assert torch.equal(a, b)
