@@ -57,6 +57,8 @@ _SIGS = {
     "kv_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "gqa_decode_attn": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                              ctypes.c_float, _VP]),
+    "gqa_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
+                                     ctypes.c_float, _VP]),
     "kvattn_status_string": (ctypes.c_char_p, [_I]),
     "kvattn_last_error": (ctypes.c_char_p, []),
     "kvattn_check_device_error": (_I, [_VP]),

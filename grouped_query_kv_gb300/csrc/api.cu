@@ -173,6 +173,52 @@ int get_workspace(int dev, cudaStream_t stream, size_t bytes, void **ptr) {
 
 }  // namespace
 
+// Entry points for the allocation-free variant (noalloc.cu): they reuse the
+// checks, the descriptor encoding and the error word above without touching
+// the workspace cache.
+namespace kvattn {
+
+int api_fail(int status, const char *msg) { return fail(status, "%s", msg); }
+
+int api_check_args(const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *seq_lens, const float *out, int B, int Hq, int Hkv, int D,
+                   int Lmax, float scale) {
+    t_last_error[0] = 0;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out)
+        return fail(KVATTN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(KVATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(KVATTN_ERR_INVALID_ARG, "scale must be finite");
+    return check_sizes(B, Hq, Hkv, D, Lmax);
+}
+
+int api_forced_ctas() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_force_ctas;
+}
+
+int api_encode_cache_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k_cache,
+                          const void *v_cache, int D, int Lmax, int BH, int tile) {
+    int rc;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if ((rc = get_encoder())) return rc;
+    }
+    if ((rc = encode_cache_map(tmk, k_cache, D, Lmax, BH, tile))) return rc;
+    return encode_cache_map(tmv, v_cache, D, Lmax, BH, tile);
+}
+
+int api_error_word(unsigned int **word) {
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(word), g_kvattn_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    return KVATTN_OK;
+}
+
+int api_cuda_fail(cudaError_t e, const char *what) { return cuda_fail(e, what); }
+
+}  // namespace kvattn
+
 extern "C" {
 
 const char *kvattn_status_string(int status) {

@@ -325,20 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float ls = warp_sumf(l_part[g]);
             if (lane == 0) red_l[warp * GC + g] = ls;
         }
-        if (warp == 0) {
+        // fixed summation order (warp 0, then 1, 2, 3): bitwise reproducible
+#pragma unroll 1
+        for (int w = 0; w < 4; ++w) {
+            if (warp == w) {
 #pragma unroll
-            for (int g = 0; g < GC; ++g)
+                for (int g = 0; g < GC; ++g)
 #pragma unroll
-                for (int k = 0; k < C::DL; ++k) o_red[g * D + dcol + k] = o[g][k];
+                    for (int k = 0; k < C::DL; ++k) {
+                        float *dst = &o_red[g * D + dcol + k];
+                        *dst = (w == 0) ? o[g][k] : *dst + o[g][k];
+                    }
+            }
+            named_bar_sync(kBarConsumers, kConsumers);
         }
-        named_bar_sync(kBarConsumers, kConsumers);
-        if (warp != 0) {
-#pragma unroll
-            for (int g = 0; g < GC; ++g)
-#pragma unroll
-                for (int k = 0; k < C::DL; ++k) atomicAdd(&o_red[g * D + dcol + k], o[g][k]);
-        }
-        named_bar_sync(kBarConsumers, kConsumers);
         if (complete) {
             for (int x = tid; x < gvalid * D; x += kConsumers) {
                 const int g = x / D, d = x % D;

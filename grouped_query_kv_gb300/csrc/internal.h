@@ -56,4 +56,15 @@ cudaError_t fma_prepare(int D, int heads_per_seg, int smem_bytes);
 
 cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream);
 
+// Shared with the allocation-free entry point (defined in api.cu).
+int api_fail(int status, const char *msg);
+int api_check_args(const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *seq_lens, const float *out, int B, int Hq, int Hkv, int D,
+                   int Lmax, float scale);
+int api_forced_ctas();
+int api_encode_cache_maps(CUtensorMap *tmk, CUtensorMap *tmv, const void *k_cache,
+                          const void *v_cache, int D, int Lmax, int BH, int tile);
+int api_error_word(unsigned int **word);
+int api_cuda_fail(cudaError_t e, const char *what);
+
 }  // namespace kvattn

@@ -120,6 +120,32 @@ KVATTN_API int gqa_decode_attn(const void *q, const void *k_cache, const void *v
                     int Hkv, int D, int Lmax, float scale,
                     kvattn_stream_t stream);
 
+/*
+ * gqa_decode_attn_noalloc -- the same computation as gqa_decode_attn, for
+ * callers that must not have the library allocate device memory (for
+ * example a server that gives all free GPU memory to its own pool at
+ * start-up, or a loop that cannot afford the device synchronisation a
+ * cudaFree brings).  The paper has no counterpart: this is a property of
+ * the library, not of the method.
+ *
+ * Same arguments, layouts and errors as gqa_decode_attn.  It always runs the
+ * CUDA-core split-KV kernel and keeps the partial results of split sequences
+ * in a fixed 4 MiB device array that is part of the library (one per GPU,
+ * held until the process exits); it never calls cudaMalloc or cudaFree.
+ * The array's address is looked up on the first call made on each device
+ * (with that device current); make that first call before capturing work on
+ * the device into anything.  All calls on a device share the array: calls
+ * whose GPU work overlaps (different streams with no ordering) race and may
+ * return wrong results.  A call whose partials would not fit (2 x grid CTAs x
+ * heads per pass x (D + 2) floats > 4 MiB, e.g. after kvattn_set_tuning
+ * forced a very large grid) returns KVATTN_ERR_UNSUPPORTED and launches
+ * nothing.
+ */
+KVATTN_API int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
+                                       const void *v_cache, const int32_t *seq_lens,
+                                       float *out, int B, int Hq, int Hkv, int D,
+                                       int Lmax, float scale, kvattn_stream_t stream);
+
 /* Static string naming a status code. */
 KVATTN_API const char *kvattn_status_string(int status);
 
