@@ -113,25 +113,61 @@ int encode_cache_map(CUtensorMap *m, const void *base, int D, int Lmax, int BH, 
 struct Plan {
     kvattn_plan pub;
     int heads_per_seg;
+    int np;  // tensor-core path: heads per pass rounded up to 16
 };
 
+// Path choice: the tensor-core kernel when a K/V head serves G >= 8 query
+// heads (every position then meets a dense G x D block of work) and D is 128
+// or 256; the CUDA-core kernel otherwise.
 int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
     (void)Lmax;
+    (void)B;
     const int G = Hq / Hkv;
     kvattn_plan &p = pl->pub;
     memset(&p, 0, sizeof p);
-    p.path = 1;
-    pl->heads_per_seg = fma_heads_per_seg(G);
+    const bool tc_ok = (D == 128 || D == 256);
+    int path = (G >= 8 && tc_ok) ? 2 : 1;
+    if (g_force_path == 1) path = 1;
+    if (g_force_path == 2) {
+        if (!tc_ok)
+            return fail(KVATTN_ERR_UNSUPPORTED, "tensor-core path needs D in {128, 256} (D=%d)", D);
+        path = 2;
+    }
+    p.path = path;
+    if (path == 2) {
+        pl->heads_per_seg = tc_heads_per_seg(G, D);
+        pl->np = tc_np(G, D);
+        p.tile_positions = tc_tile();
+        p.stages = tc_stages(D, pl->np);
+        p.threads = tc_threads();
+        p.smem_bytes = tc_smem_bytes(D, pl->np);
+    } else {
+        pl->heads_per_seg = fma_heads_per_seg(G);
+        pl->np = 0;
+        p.tile_positions = fma_tile(D);
+        p.stages = fma_stages(D);
+        p.threads = fma_threads();
+        p.smem_bytes = fma_smem_bytes(D, pl->heads_per_seg);
+    }
     p.heads_per_cta = pl->heads_per_seg;
     p.head_groups = (G + pl->heads_per_seg - 1) / pl->heads_per_seg;
-    p.tile_positions = fma_tile(D);
-    p.stages = fma_stages(D);
-    p.threads = fma_threads();
-    p.smem_bytes = fma_smem_bytes(D, pl->heads_per_seg);
-    int ctas = g_force_ctas > 0 ? g_force_ctas : num_sms;
+    const int ctas = g_force_ctas > 0 ? g_force_ctas : num_sms;
     p.num_ctas = ctas;
     p.workspace_bytes = (int64_t)2 * ctas * pl->heads_per_seg * (D + 2) * (int64_t)sizeof(float);
-    (void)B;
+    return KVATTN_OK;
+}
+
+// 2-D map over q viewed as [B*Hq rows, D]: box (64, np), 128-byte swizzle.
+int encode_q_map(CUtensorMap *m, const void *base, int D, int rows, int np) {
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)np};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVATTN_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (%d)", (int)r);
     return KVATTN_OK;
 }
 
@@ -334,9 +370,18 @@ int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     p.tile = P.tile_positions;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
-    cudaError_t e = fma_prepare(D, pl.heads_per_seg, P.smem_bytes);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-    e = launch_decode_fma(tmk, tmv, p, P.num_ctas, P.smem_bytes, stream);
+    cudaError_t e;
+    if (P.path == 2) {
+        CUtensorMap tmq;
+        if ((rc = encode_q_map(&tmq, q, D, B * Hq, pl.np))) return rc;
+        e = tc_prepare(D, pl.np);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        e = launch_decode_tc(tmk, tmv, tmq, p, pl.np, P.num_ctas, stream);
+    } else {
+        e = fma_prepare(D, pl.heads_per_seg, P.smem_bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        e = launch_decode_fma(tmk, tmv, p, P.num_ctas, P.smem_bytes, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     e = launch_combine(p, P.num_ctas, stream);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");

@@ -4,7 +4,9 @@
 //            out = sum_s w_s o_s / sum_s w_s l_s.
 // Block (c, y) owns the segment containing CTA c's range start when that
 // start lies strictly inside a segment and CTA c-1's start does not (c is
-// the first cut inside it); y picks a slice of the segment's heads.
+// the first cut inside it); y picks a slice of kOutPerBlock of the segment's
+// heads x D outputs, one output per thread, so the partial loads of many
+// outputs are in flight at once.
 #include "internal.h"
 #include "schedule.cuh"
 
@@ -12,7 +14,8 @@ namespace kvattn {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
+constexpr int kOutPerBlock = kThreads;
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -20,8 +23,7 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(kThreads)
-    combine_kernel(const DecodeParams p, int heads_per_block) {
+__global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p) {
     __shared__ SchedScratch sched;
     const int c = blockIdx.x;
     const int segs_per_b = p.Hkv * p.head_groups;
@@ -41,39 +43,40 @@ __global__ void __launch_bounds__(kThreads)
     const int hg = st.seg % p.head_groups;
     const int h0 = kvh * p.G + hg * p.heads_per_seg;
     const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
-    const int gb = blockIdx.y * heads_per_block;
-    const int ge = min(gvalid, gb + heads_per_block);
     const int D = p.D;
     const int first_slot = (g_prev == S0) ? 2 * (c - 1) : 2 * (c - 1) + 1;
     const int npieces = 1 + (c_last - c + 1);
+    const int x = blockIdx.y * kOutPerBlock + threadIdx.x;   // output index within segment
+    if (blockIdx.y * kOutPerBlock >= gvalid * D) return;      // uniform per block
+    const int g = x / D, d = x % D;
+    const bool active = x < gvalid * D;
 
-    for (int x = threadIdx.x; x < (ge - gb) * D; x += kThreads) {
-        const int g = gb + x / D, d = x % D;
-        float mstar = -INFINITY;
+    // each thread forms its own weights; the (m, l) loads are shared by the
+    // D consecutive threads of one head and served as broadcasts
+    float num = 0.f, den = 0.f;
+    float mstar = -INFINITY;
+    for (int k = 0; k < npieces; ++k) {
+        const int slot = (k == 0) ? first_slot : 2 * (c + k - 1);
+        if (active) mstar = fmaxf(mstar, p.ws_ml[((size_t)slot * p.heads_per_seg + g) * 2]);
+    }
+    if (active && mstar != -INFINITY) {
+#pragma unroll 4
         for (int k = 0; k < npieces; ++k) {
             const int slot = (k == 0) ? first_slot : 2 * (c + k - 1);
-            mstar = fmaxf(mstar, p.ws_ml[((size_t)slot * p.heads_per_seg + g) * 2]);
+            const size_t ml = ((size_t)slot * p.heads_per_seg + g) * 2;
+            const float w = ex2(p.ws_ml[ml] - mstar);
+            den = fmaf(w, p.ws_ml[ml + 1], den);
+            num = fmaf(w, p.ws_o[((size_t)slot * p.heads_per_seg + g) * D + d], num);
         }
-        float num = 0.f, den = 0.f;
-        if (mstar != -INFINITY) {
-            for (int k = 0; k < npieces; ++k) {
-                const int slot = (k == 0) ? first_slot : 2 * (c + k - 1);
-                const size_t ml = ((size_t)slot * p.heads_per_seg + g) * 2;
-                const float w = ex2(p.ws_ml[ml] - mstar);
-                den = fmaf(w, p.ws_ml[ml + 1], den);
-                num = fmaf(w, p.ws_o[((size_t)slot * p.heads_per_seg + g) * D + d], num);
-            }
-        }
-        p.out[((size_t)st.b * p.Hq + h0 + g) * D + d] = (den > 0.f) ? num / den : 0.f;
     }
+    if (active) p.out[((size_t)st.b * p.Hq + h0 + g) * D + d] = (den > 0.f) ? num / den : 0.f;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream) {
-    const int hpb = p.heads_per_seg <= 8 ? p.heads_per_seg : 4;
-    dim3 grid(num_ctas, (p.heads_per_seg + hpb - 1) / hpb);
-    combine_kernel<<<grid, kThreads, 0, stream>>>(p, hpb);
+    dim3 grid(num_ctas, (p.heads_per_seg * p.D + kOutPerBlock - 1) / kOutPerBlock);
+    combine_kernel<<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -54,6 +54,19 @@ int fma_smem_bytes(int D, int heads_per_seg);
 int fma_threads();
 cudaError_t fma_prepare(int D, int heads_per_seg, int smem_bytes);
 
+// Tensor-core (tcgen05) split-KV kernel for D in {128, 256}; np = query heads
+// per pass rounded up to a multiple of 16 (tc_np).
+int tc_np(int G, int D);
+int tc_heads_per_seg(int G, int D);
+int tc_tile();
+int tc_threads();
+int tc_smem_bytes(int D, int np);
+int tc_stages(int D, int np);
+cudaError_t tc_prepare(int D, int np);
+cudaError_t launch_decode_tc(const CUtensorMap &tmk, const CUtensorMap &tmv,
+                             const CUtensorMap &tmq, const DecodeParams &p, int np, int num_ctas,
+                             cudaStream_t stream);
+
 cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream);
 
 // Shared with the allocation-free entry point (defined in api.cu).

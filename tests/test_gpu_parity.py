@@ -141,3 +141,53 @@ def test_side_stream_and_repeatability():
     s.synchronize()
     g.check_device_error(s)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (4, 1), (12, 1), (16, 2), (96, 1), (128, 2)])
+def test_each_path_on_each_head_shape(path, D, Hq, Hkv):
+    # path 1 = CUDA-core kernel, 2 = tensor-core kernel, forced for any G
+    lens = (700, 1, 129, 256, 1000, 383)
+    w = wl.Workload("forced", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, Lmax=1000,
+                    scale=1.0 / np.sqrt(D), lens=lens)
+    g.set_tuning(path, 0)
+    try:
+        assert g.get_plan(w.B, Hq, Hkv, D, w.Lmax, num_sms=152)["path"] == path
+        run_step(w, seed=7 * path + D + Hq)
+    finally:
+        g.set_tuning(0, 0)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_non_finite_padding_is_never_used(path):
+    # rows at and past each length hold NaN keys and infinite values; the
+    # pages' "only read the non-padding part" means none of it may leak
+    dev = torch.device("cuda")
+    w = wl.Workload("nanpad", B=4, Hq=16, Hkv=2, D=128, Lmax=600, scale=0.088,
+                    lens=(600, 5, 130, 257))
+    x = wl.make_inputs(w, seed=11, device=dev)
+    for b, n in enumerate(w.lens):
+        x["k_cache"][b, :, n:] = float("nan")
+        x["v_cache"][b, :, n:] = float("inf")
+    g.set_tuning(path, 0)
+    try:
+        out = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale)
+        g.check_device_error()
+    finally:
+        g.set_tuning(0, 0)
+    lens_np = x["attn_lens"].cpu().numpy()
+    ref = oracle.gqa_decode(bits(x["q"]), bits(x["k_cache"]), bits(x["v_cache"]), lens_np,
+                            w.scale)
+    assert_close(out, ref, bits(x["v_cache"]), lens_np)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 152, 600])
+def test_tensor_core_split_pieces(ctas):
+    w = wl.Workload("tcsplit", B=3, Hq=48, Hkv=1, D=256, Lmax=5000, scale=1 / 16,
+                    lens=(5000, 130, 2047), k_scale=0.5)
+    g.set_tuning(2, ctas)
+    try:
+        run_step(w, seed=ctas + 1)
+    finally:
+        g.set_tuning(0, 0)
