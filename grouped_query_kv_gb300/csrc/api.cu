@@ -153,7 +153,8 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
     p.head_groups = (G + pl->heads_per_seg - 1) / pl->heads_per_seg;
     const int ctas = g_force_ctas > 0 ? g_force_ctas : num_sms;
     p.num_ctas = ctas;
-    p.workspace_bytes = (int64_t)2 * ctas * pl->heads_per_seg * (D + 2) * (int64_t)sizeof(float);
+    p.workspace_bytes = (int64_t)2 * ctas * pl->heads_per_seg * (D + 2) * (int64_t)sizeof(float) +
+                        (int64_t)ctas * 16;
     return KVATTN_OK;
 }
 
@@ -362,6 +363,7 @@ int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     p.out = out;
     p.ws_o = static_cast<float *>(ws);
     p.ws_ml = p.ws_o + (size_t)2 * P.num_ctas * pl.heads_per_seg * D;
+    p.split = reinterpret_cast<int *>(p.ws_ml + (size_t)2 * P.num_ctas * pl.heads_per_seg * 2);
     p.err = ds->err;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.Lmax = Lmax;
     p.G = Hq / Hkv;

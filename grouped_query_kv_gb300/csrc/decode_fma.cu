@@ -113,8 +113,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
     }
+    pdl_launch_dependents();
+    pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
     sched_locate(p.seq_lens, p.B, p.Lmax, T, segs_per_b, blockIdx.x, gridDim.x, sched);
     const SchedStart st = sched->res;
+    if (tid == 0) sched_split_record(p.seq_lens, p.Lmax, T, blockIdx.x, st, p.split);
     if (!st.found || st.g_begin >= st.g_end) return;
     const long long ntiles = st.g_end - st.g_begin;
 
@@ -365,8 +368,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int GC>
 cudaError_t launch_t(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeParams &p,
                      int num_ctas, int smem_bytes, cudaStream_t stream) {
-    decode_fma_kernel<D, GC><<<num_ctas, kThreads, smem_bytes, stream>>>(tmk, tmv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_fma_kernel<D, GC>, tmk, tmv, p);
 }
 
 // Raises the kernel's dynamic shared-memory limit once per process and

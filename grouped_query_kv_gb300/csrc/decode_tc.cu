@@ -44,6 +44,7 @@ constexpr int kSmemLimit = 232448;  // 227 KB per CTA
 constexpr float kTau = 8.0f;        // log2 headroom before the running max must move
 constexpr int kBarSoftmax = 1;      // named barrier: the 128 softmax threads
 constexpr int kBarEnd = 2;          // named barrier: warps 1-5 before TMEM is freed
+constexpr uint32_t kMmaIdleLimit = 1u << 23;  // ~seconds of polling with nothing ready
 
 __host__ __device__ constexpr int pow2_at_least(int x) {
     int p = 32;
@@ -181,8 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmv);
         prefetch_tmap(&tmq);
     }
+    pdl_launch_dependents();
+    pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
     sched_locate(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, blockIdx.x, gridDim.x, sched);
     const SchedStart st = sched->res;
+    if (tid == 0) sched_split_record(p.seq_lens, p.Lmax, kT, blockIdx.x, st, p.split);
     if (!st.found || st.g_begin >= st.g_end) return;
     const long long ntiles = st.g_end - st.g_begin;
 
@@ -264,106 +268,128 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ================================================================== MMA
+    // One thread issues both streams -- QK of tile iq and PV of tile ip --
+    // whichever has its inputs ready (non-blocking tests), PV first because
+    // it releases ring chunks.  Issuing PV only after the next tile's QK
+    // would keep each V chunk in the ring until the next K chunk arrived
+    // from HBM, i.e. one memory latency per tile.
     if (warp == 1) {
         if (lane == 0) {
             TileIter itq, itp;
             itq.init(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, st);
             itp.init(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, st);
+            long long iq = 0, ip = 0;
             int piece_q = 0, piece_pv = 0, qcur = 0;
+            uint32_t idle = 0;
             bool ok = true;
-            for (long long i = 0; i <= ntiles && ok; ++i) {
-                if (i < ntiles) {
-                    if (i == 0 || itq.t == 0) {
-                        qcur = piece_q & 1;
-                        if (!wait_bar(&bs.q_full[qcur], (uint32_t)((piece_q >> 1) & 1), abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        ++piece_q;
-                    }
-                    const int sb = (int)(i & 1);
-                    if (i >= 2 &&
-                        !wait_bar(&bs.s_empty[sb], (uint32_t)(((i >> 1) - 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d_s = tmem + sb * NP;
-#pragma unroll
-                    for (int c = 0; c < KCH; ++c) {
-                        const long long idx = i * 2 * KCH + c;
-                        const int slot = (int)(idx % NCH);
-                        if (!wait_bar(&bs.chunk_full[slot], (uint32_t)((idx / NCH) & 1), abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a0 = ring_s + slot * kChunk;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const int kq = c * 8 + kk;
-                            const uint64_t ad =
-                                smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
-                            const uint64_t bd = smem_desc(
-                                qbuf_s + qcur * C::QB + (kq >> 2) * (NP * 128) + (kq & 3) * 32, 16,
-                                1024, 2);
-                            umma_bf16(d_s, ad, bd, C::IDESC_QK, kq != 0);
-                        }
-                        umma_commit(&bs.chunk_empty[slot]);
-                    }
-                    if (!ok) break;
-                    umma_commit(&bs.s_full[sb]);
-                    if (itq.last_tile_of_segment() || i == ntiles - 1) umma_commit(&bs.q_empty[qcur]);
-                    if (i < ntiles - 1) itq.next();
-                }
-                if (i >= 1) {
-                    const long long j = i - 1;
+            while (ip < ntiles) {
+                bool did = false;
+                if (ip < iq) {
+                    const long long j = ip;
                     const int pb = (int)(j & 1);
                     const bool first_pv = (j == 0) || (itp.t == 0);
-                    if (!wait_bar(&bs.p_full[pb], (uint32_t)((j >> 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (first_pv && piece_pv > 0 &&
-                        !wait_bar(bs.o_free, (uint32_t)((piece_pv - 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (first_pv) ++piece_pv;
-                    tc_fence_after();
+                    bool ready = mbar_test(&bs.p_full[pb], (uint32_t)((j >> 1) & 1));
+                    if (ready && first_pv && piece_pv > 0)
+                        ready = mbar_test(bs.o_free, (uint32_t)((piece_pv - 1) & 1));
 #pragma unroll
                     for (int db = 0; db < KCH; ++db) {
                         const long long idx = j * 2 * KCH + KCH + db;
-                        const int slot = (int)(idx % NCH);
-                        if (!wait_bar(&bs.chunk_full[slot], (uint32_t)((idx / NCH) & 1), abort_flag)) {
-                            ok = false;
-                            break;
+                        if (ready)
+                            ready = mbar_test(&bs.chunk_full[idx % NCH], (uint32_t)((idx / NCH) & 1));
+                    }
+                    if (ready) {
+                        if (first_pv) ++piece_pv;
+                        tc_fence_after();
+#pragma unroll
+                        for (int db = 0; db < KCH; ++db) {
+                            const long long idx = j * 2 * KCH + KCH + db;
+                            const int slot = (int)(idx % NCH);
+                            const uint32_t v0 = ring_s + slot * kChunk;
+                            const uint32_t d_o = tmem + 2 * NP + db * NP;
+                            // P = P_hi + P_lo (two bf16 parts): both products go into O
+#pragma unroll
+                            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                                for (int kk = 0; kk < 8; ++kk) {
+                                    // V^T: M = head dims (64-column boxes 16 KB apart), K = positions
+                                    const uint64_t ad = smem_desc(v0 + kk * 2048, 16384, 1024, 2);
+                                    // P^T: core matrices of 8 positions x 8 heads, 128 B each;
+                                    // position groups 128 B apart, head groups 2048 B apart
+                                    const uint64_t bd = smem_desc(
+                                        pbuf_s + (2 * (int)(j % C::PST) + part) * C::PB + kk * 256,
+                                        128, (kT / 8) * 128, 0);
+                                    umma_bf16(d_o, ad, bd, C::IDESC_PV,
+                                              !(first_pv && part == 0 && kk == 0));
+                                }
+                            }
+                            umma_commit(&bs.chunk_empty[slot]);
+                        }
+                        umma_commit(&bs.pv_done[pb]);
+                        if (j < ntiles - 1) itp.next();
+                        ++ip;
+                        did = true;
+                    }
+                }
+                if (iq < ntiles) {
+                    const long long i = iq;
+                    const int sb = (int)(i & 1);
+                    const bool first_q = (i == 0) || (itq.t == 0);
+                    bool ready = true;
+                    if (first_q) ready = mbar_test(&bs.q_full[piece_q & 1], (uint32_t)((piece_q >> 1) & 1));
+                    if (ready && i >= 2)
+                        ready = mbar_test(&bs.s_empty[sb], (uint32_t)(((i >> 1) - 1) & 1));
+#pragma unroll
+                    for (int c = 0; c < KCH; ++c) {
+                        const long long idx = i * 2 * KCH + c;
+                        if (ready)
+                            ready = mbar_test(&bs.chunk_full[idx % NCH], (uint32_t)((idx / NCH) & 1));
+                    }
+                    if (ready) {
+                        if (first_q) {
+                            qcur = piece_q & 1;
+                            ++piece_q;
                         }
                         tc_fence_after();
-                        const uint32_t v0 = ring_s + slot * kChunk;
-                        const uint32_t d_o = tmem + 2 * NP + db * NP;
-                        // P = P_hi + P_lo (two bf16 parts): both products go into O
+                        const uint32_t d_s = tmem + sb * NP;
 #pragma unroll
-                        for (int part = 0; part < 2; ++part) {
+                        for (int c = 0; c < KCH; ++c) {
+                            const long long idx = i * 2 * KCH + c;
+                            const int slot = (int)(idx % NCH);
+                            const uint32_t a0 = ring_s + slot * kChunk;
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
-                                // V^T: M = head dims (64-column boxes 16 KB apart), K = positions
-                                const uint64_t ad = smem_desc(v0 + kk * 2048, 16384, 1024, 2);
-                                // P^T: core matrices of 8 positions x 8 heads, 128 B each;
-                                // position groups 128 B apart, head groups 2048 B apart
+                                const int kq = c * 8 + kk;
+                                const uint64_t ad =
+                                    smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
                                 const uint64_t bd = smem_desc(
-                                    pbuf_s + (2 * (int)(j % C::PST) + part) * C::PB + kk * 256,
-                                    128, (kT / 8) * 128, 0);
-                                umma_bf16(d_o, ad, bd, C::IDESC_PV,
-                                          !(first_pv && part == 0 && kk == 0));
+                                    qbuf_s + qcur * C::QB + (kq >> 2) * (NP * 128) + (kq & 3) * 32,
+                                    16, 1024, 2);
+                                umma_bf16(d_s, ad, bd, C::IDESC_QK, kq != 0);
                             }
+                            umma_commit(&bs.chunk_empty[slot]);
                         }
-                        umma_commit(&bs.chunk_empty[slot]);
+                        umma_commit(&bs.s_full[sb]);
+                        if (itq.last_tile_of_segment() || i == ntiles - 1) umma_commit(&bs.q_empty[qcur]);
+                        if (i < ntiles - 1) itq.next();
+                        ++iq;
+                        did = true;
                     }
-                    if (!ok) break;
-                    umma_commit(&bs.pv_done[pb]);
-                    if (j < ntiles - 1) itp.next();
                 }
+                if (did) {
+                    idle = 0;
+                    continue;
+                }
+                ++idle;
+                if ((idle & 255u) == 0 && *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (idle >= kMmaIdleLimit) {
+                    ok = false;
+                    *abort_flag = 1;
+                    break;
+                }
+                if (idle > 16) __nanosleep(64);
             }
             if (!ok) {
                 set_error(p.err, DEV_ERR_TIMEOUT);
@@ -609,8 +635,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int NP>
 cudaError_t launch_t(const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmq,
                      const DecodeParams &p, int num_ctas, cudaStream_t stream) {
-    decode_tc_kernel<D, NP><<<num_ctas, kThreads, TcCfg<D, NP>::alloc, stream>>>(tmk, tmv, tmq, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = TcCfg<D, NP>::alloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NP>, tmk, tmv, tmq, p);
 }
 
 template <int D, int NP>

@@ -30,6 +30,7 @@ struct DecodeParams {
     float *ws_o;              // [2*num_ctas, heads_per_seg, D]  partial o (unnormalised)
     float *ws_ml;             // [2*num_ctas, heads_per_seg, 2]  partial (m, l), m in log2 units
     unsigned int *err;        // sticky device error word
+    int *split;               // [grid, 4] per-CTA combine record (b, seg, first slot, pieces)
     int B, Hq, Hkv, D, Lmax;
     int G;                    // Hq / Hkv
     int heads_per_seg;        // query heads one segment serves

@@ -13,6 +13,9 @@ __global__ void __launch_bounds__(128)
                      const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                      const int32_t *__restrict__ seq_lens, int B, int Hkv, int D, int Lmax,
                      unsigned int *err) {
+    // the attention kernel that follows may start its prologue now; it
+    // waits for these writes with griddepcontrol.wait before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (b, kvh) pair
     const int lane = threadIdx.x & 31;
     if (row >= B * Hkv) return;

@@ -91,8 +91,8 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
         if ((rc = noalloc_setup(dev, &nd))) return rc;
         num_ctas = nd->num_sms;
     }
-    // partial (o, m, l) for up to two pieces per CTA
-    const size_t need = size_t(2) * num_ctas * hps * (D + 2) * sizeof(float);
+    // partial (o, m, l) for up to two pieces per CTA, and one combine record per CTA
+    const size_t need = size_t(2) * num_ctas * hps * (D + 2) * sizeof(float) + size_t(16) * num_ctas;
     if (need > kNoallocScratchBytes) {
         char msg[192];
         snprintf(msg, sizeof msg,
@@ -116,6 +116,7 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
     p.out = out;
     p.ws_o = static_cast<float *>(nd->scratch);
     p.ws_ml = p.ws_o + size_t(2) * num_ctas * hps * D;
+    p.split = reinterpret_cast<int *>(p.ws_ml + size_t(2) * num_ctas * hps * 2);
     p.err = nd->err;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.Lmax = Lmax;
     p.G = G;

@@ -118,6 +118,29 @@ __device__ inline void sched_locate(const int32_t *__restrict__ lens, int B, int
     __syncthreads();
 }
 
+// The combine record of CTA c: when c's range starts strictly inside a
+// segment and c-1's range starts at or before that segment's start, c owns
+// the merge of the segment's pieces -- the last piece of CTA c-1 (or its
+// first, if c-1 started exactly at the segment start) and the first pieces
+// of CTAs c .. c_last.  Written as {b, seg, first_slot, pieces}, or b = -1.
+__device__ inline void sched_split_record(const int32_t *__restrict__ lens, int Lmax, int tile,
+                                          int c, const SchedStart &st, int *rec) {
+    int r0 = -1, r1 = 0, r2 = 0, r3 = 0;
+    if (st.found && c > 0 && st.t > 0 && c < st.ctas_eff) {
+        const long long S0 = st.g_begin - st.t;
+        const long long g_prev = (long long)(c - 1) * st.total / st.ctas_eff;
+        if (g_prev <= S0) {
+            const long long S1 = S0 + seq_ntiles(lens[st.b], Lmax, tile);
+            const int c_last = (int)((S1 * st.ctas_eff - 1) / st.total);
+            r0 = st.b;
+            r1 = st.seg;
+            r2 = (g_prev == S0) ? 2 * (c - 1) : 2 * (c - 1) + 1;
+            r3 = 1 + (c_last - c + 1);
+        }
+    }
+    reinterpret_cast<int4 *>(rec)[c] = make_int4(r0, r1, r2, r3);
+}
+
 // Walks the tile list in the same order in every thread that uses it.
 struct TileIter {
     const int32_t *lens;
