@@ -82,10 +82,12 @@ struct TcCfg {
     static constexpr int bytes = off_sched + (int)sizeof(SchedScratch);
     static constexpr int alloc = bytes + 1024;
 
-    static constexpr int TMEM_NEED = 2 * NP + KCH * NP;  // S0, S1, O blocks
+    // TMEM columns: S0, S1 (NP each), then per 128-row head-dim block an O
+    // accumulator of 2*NP columns: the V.P_hi products and the V.P_lo products
+    static constexpr int TMEM_NEED = 2 * NP + KCH * 2 * NP;
     static constexpr int TMEM_COLS = pow2_at_least(TMEM_NEED);
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, NP, false, false);
-    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, NP, true, true);
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 2 * NP, true, true);
 };
 
 struct Bars {
@@ -141,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar_base = reinterpret_cast<uint64_t *>(smem + C::off_bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::off_misc + 16);
-    SchedScratch *sched = reinterpret_cast<SchedScratch *>(smem + C::off_sched);
 
     Bars bs;
     bs.chunk_full = bar_base;
@@ -182,22 +183,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmv);
         prefetch_tmap(&tmq);
     }
-    pdl_launch_dependents();
-    pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
-    sched_locate(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, blockIdx.x, gridDim.x, sched);
-    const SchedStart st = sched->res;
-    if (tid == 0) sched_split_record(p.seq_lens, p.Lmax, kT, blockIdx.x, st, p.split);
-    if (!st.found || st.g_begin >= st.g_end) return;
-    const long long ntiles = st.g_end - st.g_begin;
-
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
+    // everything above overlaps the previous kernel's tail
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
+    // each warp locates the CTA's tile range by itself: no block barrier
+    // stands between reading the lengths and the first TMA load
+    const SchedStart st =
+        warp_locate(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, blockIdx.x, gridDim.x);
+    if (tid == 0) sched_split_record(p.seq_lens, p.Lmax, kT, blockIdx.x, st, p.split);
+    if (!st.found || st.g_begin >= st.g_end) {
+        if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+        return;
+    }
+    const long long ntiles = st.g_end - st.g_begin;
     const uint32_t ring_s = smem_u32(ring);
     const uint32_t qbuf_s = smem_u32(qbuf);
     const uint32_t pbuf_s = smem_u32(pbuf);
@@ -268,17 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ================================================================== MMA
-    // One thread issues both streams -- QK of tile iq and PV of tile ip --
-    // whichever has its inputs ready (non-blocking tests), PV first because
-    // it releases ring chunks.  Issuing PV only after the next tile's QK
-    // would keep each V chunk in the ring until the next K chunk arrived
-    // from HBM, i.e. one memory latency per tile.
+    // One thread issues both streams -- QK of tile iq (chunk by chunk, as
+    // each K chunk lands) and PV of tile ip -- whichever has its inputs ready
+    // (non-blocking tests), PV first because it releases ring chunks.  PV
+    // multiplies V^T by [P_hi^T | P_lo^T] (N = 2*NP) in one instruction per
+    // 16 positions; the two halves of the accumulator are summed at the end.
     if (warp == 1) {
         if (lane == 0) {
             TileIter itq, itp;
             itq.init(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, st);
             itp.init(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, st);
             long long iq = 0, ip = 0;
+            int qc = 0;  // next K chunk of tile iq
             int piece_q = 0, piece_pv = 0, qcur = 0;
             uint32_t idle = 0;
             bool ok = true;
@@ -300,27 +307,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ready) {
                         if (first_pv) ++piece_pv;
                         tc_fence_after();
+                        const uint32_t pstage = pbuf_s + 2 * (int)(j % C::PST) * C::PB;
 #pragma unroll
                         for (int db = 0; db < KCH; ++db) {
                             const long long idx = j * 2 * KCH + KCH + db;
                             const int slot = (int)(idx % NCH);
                             const uint32_t v0 = ring_s + slot * kChunk;
-                            const uint32_t d_o = tmem + 2 * NP + db * NP;
-                            // P = P_hi + P_lo (two bf16 parts): both products go into O
+                            const uint32_t d_o = tmem + 2 * NP + db * 2 * NP;
 #pragma unroll
-                            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                                for (int kk = 0; kk < 8; ++kk) {
-                                    // V^T: M = head dims (64-column boxes 16 KB apart), K = positions
-                                    const uint64_t ad = smem_desc(v0 + kk * 2048, 16384, 1024, 2);
-                                    // P^T: core matrices of 8 positions x 8 heads, 128 B each;
-                                    // position groups 128 B apart, head groups 2048 B apart
-                                    const uint64_t bd = smem_desc(
-                                        pbuf_s + (2 * (int)(j % C::PST) + part) * C::PB + kk * 256,
-                                        128, (kT / 8) * 128, 0);
-                                    umma_bf16(d_o, ad, bd, C::IDESC_PV,
-                                              !(first_pv && part == 0 && kk == 0));
-                                }
+                            for (int kk = 0; kk < 8; ++kk) {
+                                // V^T: M = head dims (64-column boxes 16 KB apart), K = positions
+                                const uint64_t ad = smem_desc(v0 + kk * 2048, 16384, 1024, 2);
+                                // [P_hi^T | P_lo^T]: core matrices of 8 positions x 8 heads,
+                                // 128 B each; position groups 128 B apart, head groups 2 KB
+                                const uint64_t bd =
+                                    smem_desc(pstage + kk * 256, 128, (kT / 8) * 128, 0);
+                                umma_bf16(d_o, ad, bd, C::IDESC_PV, !(first_pv && kk == 0));
                             }
                             umma_commit(&bs.chunk_empty[slot]);
                         }
@@ -335,43 +337,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int sb = (int)(i & 1);
                     const bool first_q = (i == 0) || (itq.t == 0);
                     bool ready = true;
-                    if (first_q) ready = mbar_test(&bs.q_full[piece_q & 1], (uint32_t)((piece_q >> 1) & 1));
-                    if (ready && i >= 2)
-                        ready = mbar_test(&bs.s_empty[sb], (uint32_t)(((i >> 1) - 1) & 1));
-#pragma unroll
-                    for (int c = 0; c < KCH; ++c) {
-                        const long long idx = i * 2 * KCH + c;
-                        if (ready)
-                            ready = mbar_test(&bs.chunk_full[idx % NCH], (uint32_t)((idx / NCH) & 1));
+                    if (qc == 0) {
+                        if (first_q)
+                            ready = mbar_test(&bs.q_full[piece_q & 1], (uint32_t)((piece_q >> 1) & 1));
+                        if (ready && i >= 2)
+                            ready = mbar_test(&bs.s_empty[sb], (uint32_t)(((i >> 1) - 1) & 1));
                     }
+                    const long long idx = i * 2 * KCH + qc;
+                    const int slot = (int)(idx % NCH);
+                    // A parity test is only meaningful once the slot's previous
+                    // occupant (chunk idx - NCH) has landed; the QK stream runs
+                    // ahead of PV, so that occupant may be a V chunk whose PV has
+                    // not been issued yet -- then the slot is simply not ready.
+                    if (ready && idx >= NCH) {
+                        const long long prev = idx - NCH;
+                        if (prev % (2 * KCH) >= KCH && prev / (2 * KCH) >= ip) ready = false;
+                    }
+                    if (ready) ready = mbar_test(&bs.chunk_full[slot], (uint32_t)((idx / NCH) & 1));
                     if (ready) {
-                        if (first_q) {
+                        if (qc == 0 && first_q) {
                             qcur = piece_q & 1;
                             ++piece_q;
                         }
                         tc_fence_after();
                         const uint32_t d_s = tmem + sb * NP;
+                        const uint32_t a0 = ring_s + slot * kChunk;
 #pragma unroll
-                        for (int c = 0; c < KCH; ++c) {
-                            const long long idx = i * 2 * KCH + c;
-                            const int slot = (int)(idx % NCH);
-                            const uint32_t a0 = ring_s + slot * kChunk;
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const int kq = c * 8 + kk;
-                                const uint64_t ad =
-                                    smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
-                                const uint64_t bd = smem_desc(
-                                    qbuf_s + qcur * C::QB + (kq >> 2) * (NP * 128) + (kq & 3) * 32,
-                                    16, 1024, 2);
-                                umma_bf16(d_s, ad, bd, C::IDESC_QK, kq != 0);
-                            }
-                            umma_commit(&bs.chunk_empty[slot]);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const int kq = qc * 8 + kk;
+                            const uint64_t ad =
+                                smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
+                            const uint64_t bd = smem_desc(
+                                qbuf_s + qcur * C::QB + (kq >> 2) * (NP * 128) + (kq & 3) * 32, 16,
+                                1024, 2);
+                            umma_bf16(d_s, ad, bd, C::IDESC_QK, kq != 0);
                         }
-                        umma_commit(&bs.s_full[sb]);
-                        if (itq.last_tile_of_segment() || i == ntiles - 1) umma_commit(&bs.q_empty[qcur]);
-                        if (i < ntiles - 1) itq.next();
-                        ++iq;
+                        umma_commit(&bs.chunk_empty[slot]);
+                        if (++qc == KCH) {
+                            qc = 0;
+                            umma_commit(&bs.s_full[sb]);
+                            if (itq.last_tile_of_segment() || i == ntiles - 1)
+                                umma_commit(&bs.q_empty[qcur]);
+                            if (i < ntiles - 1) itq.next();
+                            ++iq;
+                        }
                         did = true;
                     }
                 }
@@ -417,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long i = 0;
     bool first_piece = true;
     bool aborted = false;
+    bool carry_fail = false;  // a failed wait late in a tile is voted on at the next barrier
     float l[NP];
 
     while (i < ntiles && !aborted) {
@@ -437,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         while (true) {
             const int sb = (int)(i & 1);
-            bool fail = !wait_bar(&bs.s_full[sb], (uint32_t)((i >> 1) & 1), abort_flag);
+            bool fail = carry_fail || !wait_bar(&bs.s_full[sb], (uint32_t)((i >> 1) & 1), abort_flag);
             tc_fence_after();
             float s[NP];
 #pragma unroll
@@ -495,13 +505,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int db = 0; db < KCH; ++db) {
 #pragma unroll
-                        for (int c = 0; c < NP / 16; ++c) {
+                        for (int c = 0; c < 2 * NP / 16; ++c) {  // hi half, then lo half
                             float v[16];
-                            const uint32_t a = lane_base + 2 * NP + db * NP + c * 16;
+                            const uint32_t a = lane_base + 2 * NP + db * 2 * NP + c * 16;
                             tmem_ld16(a, v);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int k = 0; k < 16; ++k) v[k] *= alpha_s[c * 16 + k];
+                            for (int k = 0; k < 16; ++k) v[k] *= alpha_s[(c * 16 + k) % NP];
                             tmem_st16(a, v);
                         }
                     }
@@ -541,7 +551,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (nvalid < kT && row >= nvalid) {
                 // rows past the length take part in P.V with p = 0; clear their
-                // V rows so that non-finite padding cannot turn 0 * v into NaN
+                // V rows so that non-finite padding cannot turn 0 * v into NaN.
+                // First make sure the slots' previous occupants have been
+                // consumed (PV of tile i-1 done), so the parity waits below
+                // refer to this tile's V chunks.
+                if (i >= 1) {
+                    const long long j = i - 1;
+                    if (!wait_bar(&bs.pv_done[j & 1], (uint32_t)((j >> 1) & 1), abort_flag))
+                        fail = true;
+                }
 #pragma unroll
                 for (int db = 0; db < KCH; ++db) {
                     const long long idx = i * 2 * KCH + KCH + db;
@@ -560,11 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bs.p_full[sb]);
-            if (named_bar_sync_or(kBarSoftmax, 128, fail)) {
-                *abort_flag = 1;
-                aborted = true;
-                break;
-            }
+            carry_fail = fail;
 
             ++i;
             if (it.last_tile_of_segment() || i == ntiles) break;
@@ -574,7 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- piece end: O^T is complete once the last PV has finished
         const long long e = i - 1;
-        bool fail = !wait_bar(&bs.pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag);
+        bool fail = carry_fail || !wait_bar(&bs.pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag);
+        carry_fail = false;
         tc_fence_after();
 #pragma unroll
         for (int g = 0; g < NP; ++g) {
@@ -591,12 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             float o[NP];
 #pragma unroll
             for (int c = 0; c < NP / 16; ++c) {
-                float v[16];
-                tmem_ld16(lane_base + 2 * NP + db * NP + c * 16, v);
+                float v[16], w[16];
+                tmem_ld16(lane_base + 2 * NP + db * 2 * NP + c * 16, v);       // V.P_hi
+                tmem_ld16(lane_base + 2 * NP + db * 2 * NP + NP + c * 16, w);  // V.P_lo
+                tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) o[c * 16 + k] = v[k];
+                for (int k = 0; k < 16; ++k) o[c * 16 + k] = v[k] + w[k];
             }
-            tmem_ld_wait();
             const int d = db * 128 + row;
             if (complete) {
 #pragma unroll

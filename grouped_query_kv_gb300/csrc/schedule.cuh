@@ -118,6 +118,48 @@ __device__ inline void sched_locate(const int32_t *__restrict__ lens, int B, int
     __syncthreads();
 }
 
+// Warp-level variant of sched_locate: every warp of a CTA can locate the
+// CTA's range on its own, without block barriers, so the TMA producer can
+// start as soon as the lengths have been read.  Same result as sched_locate.
+__device__ inline SchedStart warp_locate(const int32_t *__restrict__ lens, int B, int Lmax,
+                                         int tile, int segs_per_b, int c, int grid) {
+    const int lane = threadIdx.x & 31;
+    long long mine = 0;
+    for (int b = lane; b < B; b += 32) mine += seq_ntiles(lens[b], Lmax, tile);
+    const long long tot = warp_sum_ll(mine) * segs_per_b;
+    SchedStart r;
+    r.total = tot;
+    r.ctas_eff = (int)(tot < (long long)grid ? tot : (long long)grid);
+    r.found = 0;
+    r.b = r.seg = r.t = 0;
+    r.g_begin = r.g_end = tot;
+    if (c >= r.ctas_eff) return r;
+    r.g_begin = (long long)c * tot / r.ctas_eff;
+    r.g_end = (long long)(c + 1) * tot / r.ctas_eff;
+    long long carry = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int b = base + lane;
+        const int nt = (b < B) ? seq_ntiles(lens[b], Lmax, tile) : 0;
+        const long long v = (long long)nt * segs_per_b;
+        const long long incl = warp_incl_scan_ll(v);
+        const long long excl = carry + incl - v;
+        const bool hit = (b < B) && excl <= r.g_begin && r.g_begin < excl + v;
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            const long long rem = __shfl_sync(0xffffffffu, r.g_begin - excl, src);
+            const int ntb = __shfl_sync(0xffffffffu, nt, src);
+            r.b = base + src;
+            r.seg = (int)(rem / ntb);
+            r.t = (int)(rem % ntb);
+            r.found = 1;
+            break;
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return r;
+}
+
 // The combine record of CTA c: when c's range starts strictly inside a
 // segment and c-1's range starts at or before that segment's start, c owns
 // the merge of the segment's pieces -- the last piece of CTA c-1 (or its

@@ -191,3 +191,24 @@ def test_tensor_core_split_pieces(ctas):
         run_step(w, seed=ctas + 1)
     finally:
         g.set_tuning(0, 0)
+
+
+@pytest.mark.parametrize("name,calls", [("palm8b_mqa", 400), ("palm540b_long_mqa", 150),
+                                        ("llama70b_gqa_ragged", 150)])
+def test_many_back_to_back_calls_are_stable(name, calls):
+    # hundreds of launches with no host synchronisation in between: a race in
+    # the pipeline's barrier phases shows up as a changed result or a device
+    # error word (the kernel's waits are bounded)
+    w = wl.WORKLOADS[name]
+    dev = torch.device("cuda")
+    x = wl.make_inputs(w, seed=21, device=dev)
+    lens = x["attn_lens"]
+    first = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], lens, w.scale)
+    outs = [torch.empty_like(first) for _ in range(4)]
+    for i in range(calls):
+        g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], lens, w.scale, out=outs[i % 4])
+        if i % 4 == 3:
+            torch.cuda.synchronize()
+            for o in outs:
+                assert torch.equal(o, first), "result changed between identical calls"
+    g.check_device_error()
