@@ -1,4 +1,5 @@
-"""Decode-attention benchmark: one step = kv_append + gqa_decode_attn over a
+"""Decode-attention benchmark: one step = kv_append + gqa_decode_attn (fused:
+gqa_decode_step) over a
 seeded synthetic batch shaped like the PaLM-8B multi-query decode
 (B=64, Hq=16, Hkv=1, D=256, 2048 cached positions) unless --workload says
 otherwise.  Prints ONE JSON line (rank 0).
@@ -10,9 +11,10 @@ Metric: KV-cache bytes the attention reads per second (only positions below
 each sequence's length count), with decode sequence-steps per second beside
 it.  Timing: W untimed steps, then exactly K steps between CUDA events on the
 launching stream, each step reading a different copy of the cache (copies
-together >= 4x L2) so reads come from HBM.  Steps are replayed as CUDA graphs
-(one for the append, one for the attention call), with an event pair around
-every attention launch for the per-launch duration used by the roofline.
+together >= 4x L2) so reads come from HBM.  A step is one gqa_decode_step call
+(the append fused into the attention kernel, plus the combine kernel),
+replayed as a CUDA graph, with an event pair around every launch for the
+per-launch duration used by the roofline.
 Under torchrun every rank runs its own batch (weak scaling, no collective in
 the data path); the barrier and the max over ranks stay.
 """
@@ -258,41 +260,32 @@ def gpu_arm(a, w):
     stream = torch.cuda.Stream(device=dev)
     sp = ctypes_void(stream.cuda_stream)
     P = lambda t: ctypes_void(t.data_ptr())  # noqa: E731
-    q_p, kn_p, vn_p, l_p, pos_p, out_p = map(P, (x["q"], x["k_new"], x["v_new"], lens, pos, out))
+    q_p, kn_p, vn_p, pos_p, out_p = map(P, (x["q"], x["k_new"], x["v_new"], pos, out))
 
-    def call_append(r):
-        rc = lib.kv_append(P(caches[r][0]), P(caches[r][1]), kn_p, vn_p, pos_p,
-                           w.B, w.Hkv, w.D, w.Lmax, sp)
-        assert rc == 0, lib.kvattn_last_error()
-
-    def call_attn(r):
-        rc = lib.gqa_decode_attn(q_p, P(caches[r][0]), P(caches[r][1]), l_p, out_p,
-                                 w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+    def call_step(r):
+        # one decode step: append this token's K/V and attend (fused kernel)
+        rc = lib.gqa_decode_step(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]), pos_p,
+                                 out_p, w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
         assert rc == 0, lib.kvattn_last_error()
 
     with torch.cuda.stream(stream):
         for r in range(ncopies):           # first calls allocate the workspace
-            call_append(r)
-            call_attn(r)
+            call_step(r)
     stream.synchronize()
     g.check_device_error(stream)
 
-    graphs_a, graphs_b = [], []
+    graphs = []
     for r in range(ncopies):
-        ga, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga, stream=stream):
-            call_append(r)
-        with torch.cuda.graph(gb, stream=stream):
-            call_attn(r)
-        graphs_a.append(ga)
-        graphs_b.append(gb)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            call_step(r)
+        graphs.append(gr)
     torch.cuda.synchronize(dev)
 
     # ---- warm-up, then exactly K timed steps
     with torch.cuda.stream(stream):
         for i in range(a.warmup):
-            graphs_a[i % ncopies].replay()
-            graphs_b[i % ncopies].replay()
+            graphs[i % ncopies].replay()
     stream.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(a.steps)]
@@ -305,10 +298,8 @@ def gpu_arm(a, w):
     with torch.cuda.stream(stream):
         t0.record(stream)
         for i in range(a.steps):
-            r = i % ncopies
-            graphs_a[r].replay()
             ev[i][0].record(stream)
-            graphs_b[r].replay()
+            graphs[i % ncopies].replay()
             ev[i][1].record(stream)
         t1.record(stream)
     torch.cuda.synchronize(dev)
@@ -317,27 +308,28 @@ def gpu_arm(a, w):
     clk = clocks.stop()
     g.check_device_error(stream)
     ms_total = t0.elapsed_time(t1)
-    attn_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     if world > 1:
         tt = torch.tensor([ms_total], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_total = float(tt.item())
     ms_step = ms_total / a.steps
     value = world * kv_bytes * a.steps / (ms_total / 1e3) / 1e9
-    attn_mean = statistics.mean(attn_ms)
-    achieved = kv_bytes / (attn_mean / 1e3) / 1e9
+    launch_mean = statistics.mean(step_ms)
+    achieved = kv_bytes / (launch_mean / 1e3) / 1e9
 
     # ---- end to end through the public Python API with host buffers
-    io = accounting.step_io_bytes(w.B, w.Hq, w.Hkv, w.D)
     hq = x["q"].cpu().pin_memory()
     hkn = x["k_new"].cpu().pin_memory()
     hvn = x["v_new"].cpu().pin_memory()
     hpos = pos.cpu().pin_memory()
-    hlens = lens.cpu().pin_memory()
     hout = torch.empty_like(out, device="cpu").pin_memory()
     dq, dkn, dvn = torch.empty_like(x["q"]), torch.empty_like(x["k_new"]), torch.empty_like(x["v_new"])
-    dpos, dlens = torch.empty_like(pos), torch.empty_like(lens)
+    dpos = torch.empty_like(pos)
     n_e2e = max(1, a.e2e_steps)
+    # bytes each e2e step moves, counted from the tensors it copies
+    io = {"h2d": sum(t.numel() * t.element_size() for t in (hq, hkn, hvn, hpos)),
+          "d2h": hout.numel() * hout.element_size()}
 
     def e2e_step(i):
         r = i % ncopies
@@ -345,9 +337,8 @@ def gpu_arm(a, w):
         dkn.copy_(hkn, non_blocking=True)
         dvn.copy_(hvn, non_blocking=True)
         dpos.copy_(hpos, non_blocking=True)
-        dlens.copy_(hlens, non_blocking=True)
-        g.kv_append(caches[r][0], caches[r][1], dkn, dvn, dpos, stream=stream)
-        g.gqa_decode_attn(dq, caches[r][0], caches[r][1], dlens, w.scale, out=out, stream=stream)
+        g.gqa_decode_step(dq, dkn, dvn, caches[r][0], caches[r][1], dpos, w.scale, out=out,
+                          stream=stream)
         hout.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -375,21 +366,22 @@ def gpu_arm(a, w):
                    "kv_bytes_per_step": kv_bytes,
                    "l2": "inputs larger than L2: %d rotating cache copies, %.0f MB (%.1fx L2)"
                          % (ncopies, ncopies * cache_bytes / 1e6, ncopies * cache_bytes / l2),
-                   "step": "kv_append + gqa_decode_attn, CUDA-graph replays",
+                   "step": "gqa_decode_step (kv_append fused into the attention kernel), "
+                           "one CUDA-graph replay per step",
                    "numerics": "bf16 in, fp32 accumulate and out",
                    "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
         "seq_steps_per_s": world * w.B * a.steps / (ms_total / 1e3),
-        "us_per_attn_call": 1e3 * attn_mean,
+        "us_per_step_launch": 1e3 * launch_mean,
         "hbm_fraction": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "gqa_decode_attn call (split-KV kernel + combine)",
+                     "kernel": "gqa_decode_step launch (fused append + split-KV kernel + combine)",
                      "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind
                      if peak_kind == "measured" else "fallback 6800 GB/s"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
                 "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms,
-                "api": "grouped_query_kv_gb300.kv_append + gqa_decode_attn (eager)"},
-        "gpu_launches": 3 * a.steps,
+                "api": "grouped_query_kv_gb300.gqa_decode_step (eager)"},
+        "gpu_launches": 2 * a.steps,
         "clocks": clk,
     }
     if rank == 0 and not a.no_cpu_baseline:

@@ -15,7 +15,7 @@ import os
 import threading
 
 __all__ = [
-    "kv_append", "gqa_decode_attn", "check_device_error", "get_plan",
+    "kv_append", "gqa_decode_attn", "gqa_decode_step", "check_device_error", "get_plan",
     "set_tuning", "release", "KvAttnError", "library_path", "lib",
     "KVATTN_OK", "KVATTN_ERR_INVALID_ARG", "KVATTN_ERR_UNSUPPORTED",
     "KVATTN_ERR_CUDA", "KVATTN_ERR_OOM", "KVATTN_ERR_DEVICE_BOUNDS",
@@ -56,6 +56,8 @@ _I = ctypes.c_int
 _SIGS = {
     "kv_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "gqa_decode_attn": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
+                             ctypes.c_float, _VP]),
+    "gqa_decode_step": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                              ctypes.c_float, _VP]),
     "gqa_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                      ctypes.c_float, _VP]),
@@ -172,6 +174,37 @@ def gqa_decode_attn(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None)
     _check(lib().gqa_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
                                  _ptr(out), B, Hq, Hkv, D, Lmax, float(scale),
                                  _stream_ptr(stream)))
+    return out
+
+
+def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out=None,
+                    stream=None):
+    """One fused decode step: write k_new/v_new into row seq_lens[b] of the
+    caches, then attend over positions [0, seq_lens[b] + 1).
+
+    q: bf16 [B, Hq, D]; k_new, v_new: bf16 [B, Hkv, D]; caches: bf16
+    [B, Hkv, Lmax, D] (modified in place); seq_lens: int32 [B], tokens cached
+    before this step (not modified); out: optional fp32 [B, Hq, D].
+    """
+    import torch
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    B, Hq, D = q.shape
+    _need(k_cache, "k_cache", torch.bfloat16)
+    if k_cache.dim() != 4 or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError("k_cache must be [B, Hkv, Lmax, D] matching q")
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lmax, D))
+    _need(k_new, "k_new", torch.bfloat16, (B, Hkv, D))
+    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, (B, Hq, D))
+    _check(lib().gqa_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                 _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D,
+                                 Lmax, float(scale), _stream_ptr(stream)))
     return out
 
 

@@ -37,11 +37,3 @@ def attn_flops(attn_lens, Hq: int, D: int) -> int:
     head and position."""
     total = int(sum(int(x) for x in attn_lens))
     return 4 * Hq * D * total
-
-
-def step_io_bytes(B: int, Hq: int, Hkv: int, D: int) -> dict:
-    """Per-step host<->device bytes of the end-to-end call: q, k_new, v_new
-    and the two int32 length vectors in; the fp32 output back."""
-    h2d = B * Hq * D * 2 + 2 * B * Hkv * D * 2 + 2 * B * 4
-    d2h = B * Hq * D * 4
-    return {"h2d": h2d, "d2h": d2h}

@@ -324,17 +324,25 @@ int kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new
     return KVATTN_OK;
 }
 
-int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
-                    const int32_t *seq_lens, float *out, int B, int Hq, int Hkv, int D, int Lmax,
-                    float scale, kvattn_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of gqa_decode_attn and gqa_decode_step (k_new != nullptr:
+// append this step's rows first; seq_lens then count tokens cached before).
+int run_decode(const void *q, const void *k_cache, const void *v_cache, const void *k_new,
+               const void *v_new, const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
+               int D, int Lmax, float scale, kvattn_stream_t stream_, const char *who) {
     t_last_error[0] = 0;
-    if (!q || !k_cache || !v_cache || !seq_lens || !out)
-        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_attn: null pointer");
+    const bool fused = k_new != nullptr || v_new != nullptr;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out || (fused && (!k_new || !v_new)))
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: null pointer", who);
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (fused && (!aligned16(k_new) || !aligned16(v_new))) ||
         (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_attn: pointers must be 16-byte aligned");
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", who);
     if (!std::isfinite(scale))
-        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_attn: scale must be finite");
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: scale must be finite", who);
     int rc = check_sizes(B, Hq, Hkv, D, Lmax);
     if (rc) return rc;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -360,6 +368,12 @@ int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     DecodeParams p;
     p.q = static_cast<const uint16_t *>(q);
     p.seq_lens = seq_lens;
+    p.len_add = fused ? 1 : 0;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    // written only by the fused append
+    p.k_cache = const_cast<uint16_t *>(static_cast<const uint16_t *>(k_cache));
+    p.v_cache = const_cast<uint16_t *>(static_cast<const uint16_t *>(v_cache));
     p.out = out;
     p.ws_o = static_cast<float *>(ws);
     p.ws_ml = p.ws_o + (size_t)2 * P.num_ctas * pl.heads_per_seg * D;
@@ -388,6 +402,28 @@ int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     e = launch_combine(p, P.num_ctas, stream);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     return KVATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *seq_lens, float *out, int B, int Hq, int Hkv, int D, int Lmax,
+                    float scale, kvattn_stream_t stream) {
+    return run_decode(q, k_cache, v_cache, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, Lmax,
+                      scale, stream, "gqa_decode_attn");
+}
+
+int gqa_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                    void *v_cache, const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
+                    int D, int Lmax, float scale, kvattn_stream_t stream) {
+    if (!k_new || !v_new) {
+        t_last_error[0] = 0;
+        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_step: null pointer");
+    }
+    return run_decode(q, k_cache, v_cache, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, Lmax,
+                      scale, stream, "gqa_decode_step");
 }
 
 int kvattn_check_device_error(kvattn_stream_t stream) {

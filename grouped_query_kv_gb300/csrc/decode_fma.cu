@@ -115,40 +115,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     pdl_launch_dependents();
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
-    sched_locate(p.seq_lens, p.B, p.Lmax, T, segs_per_b, blockIdx.x, gridDim.x, sched);
+    const LenView lens{p.seq_lens, p.len_add};
+    sched_locate(lens, p.B, p.Lmax, T, segs_per_b, blockIdx.x, gridDim.x, sched);
     const SchedStart st = sched->res;
-    if (tid == 0) sched_split_record(p.seq_lens, p.Lmax, T, blockIdx.x, st, p.split);
+    if (tid == 0) sched_split_record(lens, p.Lmax, T, blockIdx.x, st, p.split);
     if (!st.found || st.g_begin >= st.g_end) return;
     const long long ntiles = st.g_end - st.g_begin;
 
     // ------------------------------------------------------------ producer
+    // The whole warp walks the tile list (all lanes copy the fused append's
+    // row); lane 0 alone waits on stages and issues the copies.
     if (warp == 4) {
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            TileIter it;
-            it.init(p.seq_lens, p.B, p.Lmax, T, segs_per_b, st);
-            for (long long i = 0; i < ntiles; ++i) {
-                const int s = (int)(i % C::STAGES);
-                if (i >= C::STAGES) {
-                    const uint32_t par = (uint32_t)((i / C::STAGES - 1) & 1);
-                    if (!mbar_wait(&empty[s], par)) {
-                        set_error(p.err, DEV_ERR_TIMEOUT);
-                        break;
-                    }
-                }
+        const uint64_t pol = l2_policy_evict_first();
+        TileIter it;
+        it.init(lens, p.B, p.Lmax, T, segs_per_b, st);
+        for (long long i = 0; i < ntiles; ++i) {
+            const int s = (int)(i % C::STAGES);
+            bool w = true;
+            if (lane == 0 && i >= C::STAGES)
+                w = mbar_wait(&empty[s], (uint32_t)((i / C::STAGES - 1) & 1));
+            if (!__shfl_sync(0xffffffffu, w, 0)) {
+                if (lane == 0) set_error(p.err, DEV_ERR_TIMEOUT);
+                break;
+            }
+            const int kvh = it.seg / p.head_groups;
+            const int z = it.b * p.Hkv + kvh;
+            const int y = it.t * T;
+            // fused append: this tile holds the new token's row
+            if (p.len_add && it.last_tile_of_segment() && it.len >= 1 && it.len <= p.Lmax)
+                append_row_warp(p, z, it.len - 1, D, lane);
+            if (lane == 0) {
                 uint8_t *kdst = smem + s * S::stage_bytes;
                 uint8_t *vdst = kdst + C::TILE_BYTES;
                 mbar_arrive_expect_tx(&full[s], 2 * C::TILE_BYTES);
-                const int kvh = it.seg / p.head_groups;
-                const int z = it.b * p.Hkv + kvh;
-                const int y = it.t * T;
 #pragma unroll
                 for (int sl = 0; sl < C::NSLAB; ++sl) {
                     tma_load_3d(kdst + sl * T * 128, &tmk, &full[s], sl * 64, y, z, pol);
                     tma_load_3d(vdst + sl * T * 128, &tmv, &full[s], sl * 64, y, z, pol);
                 }
-                it.next();
             }
+            it.next();
         }
         return;
     }
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dcol = lane * C::DL;   // first value column of this lane (phase 4)
 
     TileIter it;
-    it.init(p.seq_lens, p.B, p.Lmax, T, segs_per_b, st);
+    it.init(lens, p.B, p.Lmax, T, segs_per_b, st);
     long long i = 0;
     bool first_piece = true;
     bool aborted = false;

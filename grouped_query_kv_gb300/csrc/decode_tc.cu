@@ -12,9 +12,9 @@
 //
 // Warp roles (192 threads, one persistent CTA per SM):
 //   warp 0    TMA producer: per segment piece the group's q rows (2-D map,
-//             128-byte swizzle, double-buffered), then the K and V tiles of
+//             128-byte swizzle, double-buffered), and the K and V tiles of
 //             T = 128 positions as 32 KB chunks (two 64-column boxes) into a
-//             ring of NCH chunks.
+//             ring of NCH chunks, each V tile one K tile behind its K tile.
 //   warp 1    allocates tensor memory; one thread issues every tcgen05.mma
 //             (QK of tile i, then PV of tile i-1) and the commits that release
 //             ring chunks, score buffers and probability buffers.
@@ -121,6 +121,32 @@ __device__ __forceinline__ float warp_sumf(float v) {
     return v;
 }
 
+// Ring order of the K/V chunks of a CTA's n tiles (KCH chunks per tile each):
+//     K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}
+// V_i goes in behind K_{i+1}: it is needed only after tile i's scores and
+// probabilities exist, so issuing it one K tile later shortens the time it
+// sits in the ring, and the ring keeps more bytes in flight.
+template <int KCH>
+__device__ __forceinline__ long long k_chunk(long long i, int c) {
+    return (i == 0 ? 0 : (2 * i - 1) * KCH) + c;
+}
+template <int KCH>
+__device__ __forceinline__ long long v_chunk(long long j, int c, long long n) {
+    return (j == n - 1 ? (2 * n - 1) * KCH : (2 * j + 2) * KCH) + c;
+}
+// Whether ring chunk m is a V chunk; if so *tile receives its tile.
+template <int KCH>
+__device__ __forceinline__ bool chunk_is_v(long long m, long long n, long long *tile) {
+    if (m < KCH) return false;
+    const long long r = (m - KCH) / (2 * KCH) + 1;
+    const long long w = (m - KCH) % (2 * KCH);
+    if (r == n || w >= KCH) {
+        *tile = r - 1;
+        return true;
+    }
+    return false;
+}
+
 template <int D, int NP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -196,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
     // each warp locates the CTA's tile range by itself: no block barrier
     // stands between reading the lengths and the first TMA load
-    const SchedStart st =
-        warp_locate(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, blockIdx.x, gridDim.x);
-    if (tid == 0) sched_split_record(p.seq_lens, p.Lmax, kT, blockIdx.x, st, p.split);
+    const LenView lens{p.seq_lens, p.len_add};
+    const SchedStart st = warp_locate(lens, p.B, p.Lmax, kT, segs_per_b, blockIdx.x, gridDim.x);
+    if (tid == 0) sched_split_record(lens, p.Lmax, kT, blockIdx.x, st, p.split);
     if (!st.found || st.g_begin >= st.g_end) {
         if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
         return;
@@ -209,65 +235,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t pbuf_s = smem_u32(pbuf);
 
     // ================================================================ producer
+    // The whole warp walks the tile list (it needs all lanes for the fused
+    // append); lane 0 alone waits on ring slots and issues the copies.
     if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            TileIter it;
-            it.init(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, st);
-            long long n = 0;
-            int piece = 0;
-            bool ok = true;
-            for (long long i = 0; i < ntiles && ok; ++i) {
-                const int kvh = it.seg / p.head_groups;
-                const int hg = it.seg % p.head_groups;
-                if (i == 0 || it.t == 0) {
+        const uint64_t pol = l2_policy_evict_first();
+        TileIter itk, itv;  // tile of the next K chunks / of the next V chunks
+        itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+        itv.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+        long long n = 0;
+        int piece = 0;
+        bool ok = true;
+        // one ring chunk: two 64-column boxes of 128 positions
+        auto issue = [&](const void *tm, int c, int y, int z) -> bool {
+            const int slot = (int)(n % NCH);
+            bool w = true;
+            if (lane == 0 && n >= NCH)
+                w = wait_bar(&bs.chunk_empty[slot], (uint32_t)(((n / NCH) - 1) & 1), abort_flag);
+            if (!__shfl_sync(0xffffffffu, w, 0)) return false;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bs.chunk_full[slot], kChunk);
+                uint8_t *dst = ring + slot * kChunk;
+                tma_load_3d(dst, tm, &bs.chunk_full[slot], (2 * c) * 64, y, z, pol);
+                tma_load_3d(dst + 16384, tm, &bs.chunk_full[slot], (2 * c + 1) * 64, y, z, pol);
+            }
+            ++n;
+            return true;
+        };
+        for (long long r = 0; r <= ntiles && ok; ++r) {
+            if (r < ntiles) {  // K of tile r (and the group's q at a piece start)
+                const int kvh = itk.seg / p.head_groups;
+                const int hg = itk.seg % p.head_groups;
+                if (r == 0 || itk.t == 0) {
                     const int qs = piece & 1;
-                    if (piece >= 2 && !wait_bar(&bs.q_empty[qs], ((piece >> 1) - 1) & 1, abort_flag)) {
+                    bool w = true;
+                    if (lane == 0 && piece >= 2)
+                        w = wait_bar(&bs.q_empty[qs], ((piece >> 1) - 1) & 1, abort_flag);
+                    if (!__shfl_sync(0xffffffffu, w, 0)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bs.q_full[qs], C::QB);
-                    const int row = it.b * p.Hq + kvh * p.G + hg * p.heads_per_seg;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bs.q_full[qs], C::QB);
+                        const int row = itk.b * p.Hq + kvh * p.G + hg * p.heads_per_seg;
 #pragma unroll
-                    for (int sl = 0; sl < D / 64; ++sl)
-                        tma_load_2d(qbuf + qs * C::QB + sl * NP * 128, &tmq, &bs.q_full[qs],
-                                    sl * 64, row);
+                        for (int sl = 0; sl < D / 64; ++sl)
+                            tma_load_2d(qbuf + qs * C::QB + sl * NP * 128, &tmq, &bs.q_full[qs],
+                                        sl * 64, row);
+                    }
                     ++piece;
                 }
-                const int z = it.b * p.Hkv + kvh;
-                const int y = it.t * kT;
+                const int z = itk.b * p.Hkv + kvh;
+                // fused append: this tile holds the new token's row
+                if (p.len_add && itk.last_tile_of_segment() && itk.len >= 1 && itk.len <= p.Lmax)
+                    append_row_warp(p, z, itk.len - 1, D, lane);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const void *tm = half ? (const void *)&tmv : (const void *)&tmk;
-#pragma unroll
-                    for (int c = 0; c < KCH; ++c) {
-                        const int slot = (int)(n % NCH);
-                        if (n >= NCH &&
-                            !wait_bar(&bs.chunk_empty[slot], (uint32_t)(((n / NCH) - 1) & 1),
-                                      abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&bs.chunk_full[slot], kChunk);
-                        uint8_t *dst = ring + slot * kChunk;
-                        tma_load_3d(dst, tm, &bs.chunk_full[slot], (2 * c) * 64, y, z, pol);
-                        tma_load_3d(dst + 16384, tm, &bs.chunk_full[slot], (2 * c + 1) * 64, y, z,
-                                    pol);
-                        ++n;
-                    }
-                    if (!ok) break;
-                }
-                it.next();
+                for (int c = 0; c < KCH && ok; ++c) ok = issue(&tmk, c, itk.t * kT, z);
+                itk.next();
             }
-            if (!ok) {
-                set_error(p.err, DEV_ERR_TIMEOUT);
-                *abort_flag = 1;
-                // let copies already issued land before the CTA can exit
-                const long long first = n > NCH ? n - NCH : 0;
-                for (long long k = first; k < n; ++k) {
-                    volatile int never = 0;
-                    wait_bar(&bs.chunk_full[k % NCH], (uint32_t)((k / NCH) & 1), &never);
-                }
+            if (r >= 1 && ok) {  // V of tile r-1
+                const int z = itv.b * p.Hkv + itv.seg / p.head_groups;
+#pragma unroll
+                for (int c = 0; c < KCH && ok; ++c) ok = issue(&tmv, c, itv.t * kT, z);
+                itv.next();
+            }
+        }
+        if (!ok && lane == 0) {
+            set_error(p.err, DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+            // let copies already issued land before the CTA can exit
+            const long long first = n > NCH ? n - NCH : 0;
+            for (long long k = first; k < n; ++k) {
+                volatile int never = 0;
+                wait_bar(&bs.chunk_full[k % NCH], (uint32_t)((k / NCH) & 1), &never);
             }
         }
         return;
@@ -282,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         if (lane == 0) {
             TileIter itq, itp;
-            itq.init(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, st);
-            itp.init(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, st);
+            itq.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+            itp.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
             long long iq = 0, ip = 0;
             int qc = 0;  // next K chunk of tile iq
             int piece_q = 0, piece_pv = 0, qcur = 0;
@@ -300,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ready = mbar_test(bs.o_free, (uint32_t)((piece_pv - 1) & 1));
 #pragma unroll
                     for (int db = 0; db < KCH; ++db) {
-                        const long long idx = j * 2 * KCH + KCH + db;
+                        const long long idx = v_chunk<KCH>(j, db, ntiles);
                         if (ready)
                             ready = mbar_test(&bs.chunk_full[idx % NCH], (uint32_t)((idx / NCH) & 1));
                     }
@@ -310,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t pstage = pbuf_s + 2 * (int)(j % C::PST) * C::PB;
 #pragma unroll
                         for (int db = 0; db < KCH; ++db) {
-                            const long long idx = j * 2 * KCH + KCH + db;
+                            const long long idx = v_chunk<KCH>(j, db, ntiles);
                             const int slot = (int)(idx % NCH);
                             const uint32_t v0 = ring_s + slot * kChunk;
                             const uint32_t d_o = tmem + 2 * NP + db * 2 * NP;
@@ -343,15 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ready && i >= 2)
                             ready = mbar_test(&bs.s_empty[sb], (uint32_t)(((i >> 1) - 1) & 1));
                     }
-                    const long long idx = i * 2 * KCH + qc;
+                    const long long idx = k_chunk<KCH>(i, qc);
                     const int slot = (int)(idx % NCH);
                     // A parity test is only meaningful once the slot's previous
                     // occupant (chunk idx - NCH) has landed; the QK stream runs
                     // ahead of PV, so that occupant may be a V chunk whose PV has
                     // not been issued yet -- then the slot is simply not ready.
                     if (ready && idx >= NCH) {
-                        const long long prev = idx - NCH;
-                        if (prev % (2 * KCH) >= KCH && prev / (2 * KCH) >= ip) ready = false;
+                        long long vt;
+                        if (chunk_is_v<KCH>(idx - NCH, ntiles, &vt) && vt >= ip) ready = false;
                     }
                     if (ready) ready = mbar_test(&bs.chunk_full[slot], (uint32_t)((idx / NCH) & 1));
                     if (ready) {
@@ -422,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
 
     TileIter it;
-    it.init(p.seq_lens, p.B, p.Lmax, kT, segs_per_b, st);
+    it.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
     long long i = 0;
     bool first_piece = true;
     bool aborted = false;
@@ -467,9 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = row < nvalid;
             bool over = false;
 #pragma unroll
-            for (int g = 0; g < NP; ++g) {
+            for (int g = 0; g < NP; g += 4) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g);
                 s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
-                over |= s[g] > mref_s[g] + kTau;
+                s[g + 1] = valid ? s[g + 1] * p.scale_log2 : -INFINITY;
+                s[g + 2] = valid ? s[g + 2] * p.scale_log2 : -INFINITY;
+                s[g + 3] = valid ? s[g + 3] * p.scale_log2 : -INFINITY;
+                over |= (s[g] > m4.x + kTau) | (s[g + 1] > m4.y + kTau) |
+                        (s[g + 2] > m4.z + kTau) | (s[g + 3] > m4.w + kTau);
             }
             if (named_bar_sync_or(kBarSoftmax, 128, over || fail)) {
                 if (named_bar_sync_or(kBarSoftmax, 128, fail || *abort_flag != 0)) {
@@ -524,16 +568,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // carry ~16 significant bits of p instead of 8
             uint32_t pk[NP / 2], pl[NP / 2];
 #pragma unroll
-            for (int g = 0; g < NP; g += 2) {
-                const float p0 = (s[g] == -INFINITY) ? 0.f : fast_exp2(s[g] - mref_s[g]);
-                const float p1 = (s[g + 1] == -INFINITY) ? 0.f : fast_exp2(s[g + 1] - mref_s[g + 1]);
-                l[g] += p0;
-                l[g + 1] += p1;
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                const __nv_bfloat162 r2 =
-                    __floats2bfloat162_rn(p0 - __low2float(h2), p1 - __high2float(h2));
-                pk[g / 2] = *reinterpret_cast<const uint32_t *>(&h2);
-                pl[g / 2] = *reinterpret_cast<const uint32_t *>(&r2);
+            for (int g4 = 0; g4 < NP; g4 += 4) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g4);
+                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int h = 0; h < 4; h += 2) {
+                    const int g = g4 + h;
+                    const float p0 = (s[g] == -INFINITY) ? 0.f : fast_exp2(s[g] - mm[h]);
+                    const float p1 = (s[g + 1] == -INFINITY) ? 0.f : fast_exp2(s[g + 1] - mm[h + 1]);
+                    l[g] += p0;
+                    l[g + 1] += p1;
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                    const __nv_bfloat162 r2 =
+                        __floats2bfloat162_rn(p0 - __low2float(h2), p1 - __high2float(h2));
+                    pk[g / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+                    pl[g / 2] = *reinterpret_cast<const uint32_t *>(&r2);
+                }
             }
             // the P stage written now was last read by PV of tile i - PST
             if (i >= C::PST) {
@@ -562,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int db = 0; db < KCH; ++db) {
-                    const long long idx = i * 2 * KCH + KCH + db;
+                    const long long idx = v_chunk<KCH>(i, db, ntiles);
                     const int slot = (int)(idx % NCH);
                     if (!wait_bar(&bs.chunk_full[slot], (uint32_t)((idx / NCH) & 1), abort_flag))
                         fail = true;

@@ -26,6 +26,11 @@ enum : unsigned int { DEV_ERR_BOUNDS = 5u, DEV_ERR_TIMEOUT = 6u };
 struct DecodeParams {
     const uint16_t *q;        // bf16 [B, Hq, D]
     const int32_t *seq_lens;  // [B]
+    int len_add;              // 1: fused append -- seq_lens count tokens cached before this step
+    const uint16_t *k_new;    // fused append only: bf16 [B, Hkv, D] rows written at seq_lens[b]
+    const uint16_t *v_new;
+    uint16_t *k_cache;        // fused append only: the caches the rows go into
+    uint16_t *v_cache;
     float *out;               // [B, Hq, D]
     float *ws_o;              // [2*num_ctas, heads_per_seg, D]  partial o (unnormalised)
     float *ws_ml;             // [2*num_ctas, heads_per_seg, 2]  partial (m, l), m in log2 units

@@ -113,6 +113,9 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
     DecodeParams p;
     p.q = static_cast<const uint16_t *>(q);
     p.seq_lens = seq_lens;
+    p.len_add = 0;
+    p.k_new = p.v_new = nullptr;
+    p.k_cache = p.v_cache = nullptr;
     p.out = out;
     p.ws_o = static_cast<float *>(nd->scratch);
     p.ws_ml = p.ws_o + size_t(2) * num_ctas * hps * D;

@@ -13,6 +13,18 @@
 
 namespace kvattn {
 
+// Lengths as the kernels see them.  For the fused append-then-attend step the
+// array holds the number of tokens cached BEFORE this step's token, and the
+// attention covers one more position; a negative entry stays invalid.
+struct LenView {
+    const int32_t *p;
+    int add;  // 0: attention lengths as given; 1: cached-before counts (+1)
+    __device__ __forceinline__ int operator[](int b) const {
+        const int r = p[b];
+        return add ? (r < 0 ? -1 : r + 1) : r;
+    }
+};
+
 // A sequence whose length is outside [1, Lmax] still owns one tile, with no
 // valid positions (zero output row; out-of-range lengths also raise the
 // device error word).
@@ -56,7 +68,7 @@ __device__ __forceinline__ long long warp_incl_scan_ll(long long v) {
 
 // Locate CTA `c`'s tile range.  Every thread of the block must call it
 // (blockDim.x a multiple of 32, at most 1024); the result is left in sh->res.
-__device__ inline void sched_locate(const int32_t *__restrict__ lens, int B, int Lmax, int tile,
+__device__ inline void sched_locate(LenView lens, int B, int Lmax, int tile,
                              int segs_per_b, int c, int grid, SchedScratch *sh) {
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
@@ -121,7 +133,7 @@ __device__ inline void sched_locate(const int32_t *__restrict__ lens, int B, int
 // Warp-level variant of sched_locate: every warp of a CTA can locate the
 // CTA's range on its own, without block barriers, so the TMA producer can
 // start as soon as the lengths have been read.  Same result as sched_locate.
-__device__ inline SchedStart warp_locate(const int32_t *__restrict__ lens, int B, int Lmax,
+__device__ inline SchedStart warp_locate(LenView lens, int B, int Lmax,
                                          int tile, int segs_per_b, int c, int grid) {
     const int lane = threadIdx.x & 31;
     long long mine = 0;
@@ -165,7 +177,7 @@ __device__ inline SchedStart warp_locate(const int32_t *__restrict__ lens, int B
 // the merge of the segment's pieces -- the last piece of CTA c-1 (or its
 // first, if c-1 started exactly at the segment start) and the first pieces
 // of CTAs c .. c_last.  Written as {b, seg, first_slot, pieces}, or b = -1.
-__device__ inline void sched_split_record(const int32_t *__restrict__ lens, int Lmax, int tile,
+__device__ inline void sched_split_record(LenView lens, int Lmax, int tile,
                                           int c, const SchedStart &st, int *rec) {
     int r0 = -1, r1 = 0, r2 = 0, r3 = 0;
     if (st.found && c > 0 && st.t > 0 && c < st.ctas_eff) {
@@ -183,13 +195,34 @@ __device__ inline void sched_split_record(const int32_t *__restrict__ lens, int 
     reinterpret_cast<int4 *>(rec)[c] = make_int4(r0, r1, r2, r3);
 }
 
+// Fused append, called by all 32 lanes of the producer warp before any TMA
+// copy of the tile that holds row `pos`: write this step's K and V rows of
+// (b, kvh) = z into that row of the caches, and make the writes visible to
+// the tensor-copy (async) proxy.  Every CTA that loads the tile writes the
+// row itself (head groups of one K/V head write identical bytes), so no
+// reader depends on another CTA's write.
+__device__ __forceinline__ void append_row_warp(const DecodeParams &p, int z, int pos, int D,
+                                                int lane) {
+    const int vecs = D / 8;  // 16-byte vectors per row
+    const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new) + (size_t)z * vecs;
+    const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new) + (size_t)z * vecs;
+    uint4 *kd = reinterpret_cast<uint4 *>(p.k_cache) + ((size_t)z * p.Lmax + pos) * vecs;
+    uint4 *vd = reinterpret_cast<uint4 *>(p.v_cache) + ((size_t)z * p.Lmax + pos) * vecs;
+    for (int i = lane; i < vecs; i += 32) {
+        kd[i] = ks[i];
+        vd[i] = vs[i];
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+}
+
 // Walks the tile list in the same order in every thread that uses it.
 struct TileIter {
-    const int32_t *lens;
+    LenView lens;
     int B, Lmax, tile, segs_per_b;
     int b, seg, t, nt, len;
 
-    __device__ __forceinline__ void init(const int32_t *lens_, int B_, int Lmax_, int tile_,
+    __device__ __forceinline__ void init(LenView lens_, int B_, int Lmax_, int tile_,
                                          int segs_per_b_, const SchedStart &s) {
         lens = lens_; B = B_; Lmax = Lmax_; tile = tile_; segs_per_b = segs_per_b_;
         b = s.b; seg = s.seg; t = s.t;

@@ -121,6 +121,32 @@ KVATTN_API int gqa_decode_attn(const void *q, const void *k_cache, const void *v
                     kvattn_stream_t stream);
 
 /*
+ * gqa_decode_step -- one whole decode step in one call: kv_append followed
+ * by gqa_decode_attn, fused into the attention kernel.
+ *
+ * Follows the same passages as the two calls it fuses: the new token's key
+ * and value are written into the cache, then its query attends over every
+ * cached position including its own ("The Basics of Transformer
+ * Inference", the KV-cache paragraph).
+ *
+ *   q                : bf16 [B, Hq, D]
+ *   k_new, v_new     : bf16 [B, Hkv, D], this step's key/value rows
+ *   k_cache, v_cache : bf16 [B, Hkv, Lmax, D]; row seq_lens[b] is written
+ *   seq_lens         : int32 [B] (device), tokens cached BEFORE this step
+ *                      (0 <= seq_lens[b] < Lmax); not modified -- the
+ *                      attention covers positions [0, seq_lens[b] + 1)
+ *   out              : fp32 [B, Hq, D]
+ *
+ * Results are identical to kv_append then gqa_decode_attn with lengths
+ * seq_lens + 1.  A sequence with seq_lens[b] outside [0, Lmax) is neither
+ * appended nor attended (zero output row) and sets KVATTN_ERR_DEVICE_BOUNDS.
+ */
+KVATTN_API int gqa_decode_step(const void *q, const void *k_new, const void *v_new,
+                               void *k_cache, void *v_cache, const int32_t *seq_lens,
+                               float *out, int B, int Hq, int Hkv, int D, int Lmax,
+                               float scale, kvattn_stream_t stream);
+
+/*
  * gqa_decode_attn_noalloc -- the same computation as gqa_decode_attn, for
  * callers that must not have the library allocate device memory (for
  * example a server that gives all free GPU memory to its own pool at

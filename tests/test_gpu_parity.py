@@ -212,3 +212,79 @@ def test_many_back_to_back_calls_are_stable(name, calls):
             for o in outs:
                 assert torch.equal(o, first), "result changed between identical calls"
     g.check_device_error()
+
+
+def run_fused_step(w, seed=0, lens=None, sample_b=None):
+    """gqa_decode_step (append fused into the attention kernel) vs the oracle's
+    append followed by its attention over one more position."""
+    dev = torch.device("cuda")
+    x = wl.make_inputs(w, seed=seed, device=dev, lens=lens)
+    bsel = list(range(w.B)) if sample_b is None else sorted(int(b) for b in sample_b)
+    idx = torch.tensor(bsel, device=dev)
+    k_ref = bits(x["k_cache"].index_select(0, idx))
+    v_ref = bits(x["v_cache"].index_select(0, idx))
+    pos = x["append_pos"].cpu().numpy()[bsel]
+    oracle.kv_append(k_ref, v_ref, bits(x["k_new"])[bsel], bits(x["v_new"])[bsel], pos)
+    out = g.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                            x["append_pos"], w.scale)
+    g.check_device_error()
+    assert np.array_equal(bits(x["k_cache"].index_select(0, idx)), k_ref), "fused append: K differs"
+    assert np.array_equal(bits(x["v_cache"].index_select(0, idx)), v_ref), "fused append: V differs"
+    lens_np = x["attn_lens"].cpu().numpy()[bsel]
+    ref = oracle.gqa_decode(bits(x["q"])[bsel], k_ref, v_ref, lens_np, w.scale,
+                            nthreads=oracle_threads())
+    return assert_close(out.index_select(0, idx), ref, v_ref, lens_np)
+
+
+@pytest.mark.parametrize("name", ["tiny_mqa", "palm8b_mqa", "llama70b_gqa_ragged",
+                                  "palm540b_long_mqa", "sweep_hkv8_b64", "sweep_hkv32_b8"])
+def test_fused_step_on_the_configs(name):
+    run_fused_step(wl.WORKLOADS[name])
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 16, 2), (256, 48, 1), (64, 4, 1), (128, 96, 1)])
+def test_fused_step_edges_and_paths(path, D, Hq, Hkv):
+    if path == 2 and D == 64:
+        pytest.skip("tensor-core path needs D in {128, 256}")
+    # lengths after the append: 1 (append into an empty cache), tile edges, Lmax
+    lens = (1, 127, 128, 129, 300, 64, 65, 2)
+    w = wl.Workload("fused", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, Lmax=300,
+                    scale=1.0 / np.sqrt(D), lens=lens)
+    g.set_tuning(path, 0)
+    try:
+        run_fused_step(w, seed=3 * path + D)
+    finally:
+        g.set_tuning(0, 0)
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 152, 400])
+def test_fused_step_with_split_pieces(ctas):
+    w = wl.Workload("fsplit", B=4, Hq=32, Hkv=4, D=128, Lmax=3000, scale=0.088,
+                    lens=(3000, 1, 1700, 250))
+    g.set_tuning(0, ctas)
+    try:
+        run_fused_step(w, seed=ctas)
+    finally:
+        g.set_tuning(0, 0)
+
+
+def test_fused_step_flags_rows_outside_the_cache():
+    dev = torch.device("cuda")
+    w = wl.Workload("fbad", B=3, Hq=16, Hkv=2, D=128, Lmax=64, scale=0.1, lens=(5, 5, 5))
+    x = wl.make_inputs(w, seed=9, device=dev)
+    before = bits(x["k_cache"])
+    pos = torch.tensor([64, 3, -1], dtype=torch.int32, device=dev)
+    out = g.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], pos,
+                            w.scale)
+    with pytest.raises(g.KvAttnError) as ei:
+        g.check_device_error()
+    assert ei.value.status == g.KVATTN_ERR_DEVICE_BOUNDS
+    after = bits(x["k_cache"])
+    assert np.array_equal(after[0], before[0]) and np.array_equal(after[2], before[2])
+    assert np.array_equal(after[1, :, 3], bits(x["k_new"])[1])
+    o = out.cpu()
+    assert torch.all(o[0] == 0) and torch.all(o[2] == 0)
+    ref = oracle.gqa_decode(bits(x["q"])[1:2], after[1:2], bits(x["v_cache"])[1:2],
+                            np.array([4], np.int32), w.scale)
+    assert_close(out[1:2], ref, bits(x["v_cache"])[1:2], [4])
