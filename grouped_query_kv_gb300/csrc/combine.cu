@@ -35,6 +35,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
     __shared__ int s_owner;
     __shared__ float s_w[kMaxHeadsPerBlock][kMaxPieces];
     __shared__ float s_m[kMaxHeadsPerBlock], s_den[kMaxHeadsPerBlock], s_scale[kMaxHeadsPerBlock];
+    // the next kernel in the stream may start its prologue while this one
+    // runs; it waits for these writes with its own griddepcontrol.wait
+    pdl_launch_dependents();
     pdl_wait_prior();  // partials and records come from the split-KV kernel just before
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int4 *recs = reinterpret_cast<const int4 *>(p.split);

@@ -113,13 +113,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
     }
-    pdl_launch_dependents();
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
     const LenView lens{p.seq_lens, p.len_add};
     sched_locate(lens, p.B, p.Lmax, T, segs_per_b, blockIdx.x, gridDim.x, sched);
     const SchedStart st = sched->res;
     if (tid == 0) sched_split_record(lens, p.Lmax, T, blockIdx.x, st, p.split);
-    if (!st.found || st.g_begin >= st.g_end) return;
+    if (!st.found || st.g_begin >= st.g_end) {
+        pdl_launch_dependents();
+        return;
+    }
     const long long ntiles = st.g_end - st.g_begin;
 
     // ------------------------------------------------------------ producer
@@ -156,6 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             it.next();
         }
+        // every load is issued: let the combine kernel be scheduled
+        pdl_launch_dependents();
         return;
     }
 

@@ -218,7 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_launch_dependents();
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
     // each warp locates the CTA's tile range by itself: no block barrier
     // stands between reading the lengths and the first TMA load
@@ -227,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) sched_split_record(lens, p.Lmax, kT, blockIdx.x, st, p.split);
     if (!st.found || st.g_begin >= st.g_end) {
         if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+        pdl_launch_dependents();
         return;
     }
     const long long ntiles = st.g_end - st.g_begin;
@@ -309,6 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_bar(&bs.chunk_full[k % NCH], (uint32_t)((k / NCH) & 1), &never);
             }
         }
+        // every load of this CTA is issued: the next kernel (the combine) may
+        // be scheduled now -- late enough that its waiting blocks do not sit
+        // beside this kernel for long, early enough to hide its launch
+        pdl_launch_dependents();
         return;
     }
 
