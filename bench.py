@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
 
@@ -78,6 +78,46 @@ def cpu_model():
     except Exception:
         pass
     return "unknown"
+
+
+# ------------------------------------------------- DRAM traffic (from ncu)
+
+def sources_digest():
+    """sha256 over the CUDA sources and the C header (sorted by name): ties a
+    stored ncu traffic figure to the exact kernels it was measured on."""
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    csrc = os.path.join(root, "grouped_query_kv_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)
+                   if f.endswith((".cu", ".cuh", ".h")))
+    files.append(os.path.join(root, "include", "kvattn.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload):
+    """DRAM bytes (read + write) per launch of each kernel of one step, from
+    the table in profiles/dram_traffic.md, when it was taken on the current
+    sources; None otherwise."""
+    root = os.path.dirname(os.path.abspath(__file__))
+    path = os.path.join(root, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    digest = sources_digest()
+    kernels = {}
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) != 5 or cells[0] != workload or cells[4] != digest:
+            continue
+        try:
+            kernels[cells[1]] = int(cells[2]) + int(cells[3])
+        except ValueError:
+            continue
+    return kernels or None
 
 
 # ------------------------------------------------------------ clocks sampler
@@ -137,8 +177,10 @@ class Clocks:
 # --------------------------------------------------------------- CPU oracle
 
 def oracle_sample(w, seed, target_s, max_seqs=None):
-    """Time the oracle (all host cores) on whole sequences of the workload.
-    Returns (seconds, sequences, kv_bytes, threads)."""
+    """Time the oracle (all host cores) on whole sequences of the workload:
+    as many sequences as fit in target_s (at most the whole batch), repeated
+    until target_s of CPU work has run.  Returns (seconds, sequences,
+    kv_bytes, threads, repetitions)."""
     import dataclasses
 
     import oracle
@@ -148,24 +190,29 @@ def oracle_sample(w, seed, target_s, max_seqs=None):
     threads = os.cpu_count() or 1
     lens_all = wl.attn_lens(w, seed)
 
-    def run(nb):
+    def inputs(nb):
         sub = dataclasses.replace(w, B=nb, lens=None, ragged=False)
         x = wl.make_inputs(sub, seed=seed, device="cpu", lens=lens_all[:nb])
         q, k, v = (wl.bf16_bits(x[n]) for n in ("q", "k_cache", "v_cache"))
         lens = x["attn_lens"].numpy()
+        return q, k, v, lens, accounting.kv_bytes_read(lens, w.Hkv, w.D)
+
+    def once(x):
+        q, k, v, lens, _ = x
         t = time.perf_counter()
         oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads)
-        dt = time.perf_counter() - t
-        return dt, accounting.kv_bytes_read(lens, w.Hkv, w.D)
+        return time.perf_counter() - t
 
-    dt1, by1 = run(1)
+    x1 = inputs(1)
+    dt1 = once(x1)
     nb = max(1, min(w.B if max_seqs is None else max_seqs,
                     int(math.ceil(target_s / max(dt1, 1e-6)))))
-    if nb > 1:
-        dt, by = run(nb)
-    else:
-        dt, by = dt1, by1
-    return dt, nb, by, threads
+    x = inputs(nb) if nb > 1 else x1
+    total, reps = 0.0, 0
+    while total < target_s or reps == 0:
+        total += once(x)
+        reps += 1
+    return total, nb, x[4] * reps, threads, reps
 
 
 def reference_arm(a, w):
@@ -176,7 +223,7 @@ def reference_arm(a, w):
     if rank != 0:
         return 0
     per_step = min(3.0, 120.0 / max(1, a.steps + a.warmup))
-    _, nb, _, threads = oracle_sample(w, a.seed, per_step)
+    _, nb, _, threads, _ = oracle_sample(w, a.seed, per_step)
     times, by = [], 0
     for i in range(a.warmup + a.steps):
         dt, _, by, _ = _oracle_fixed(w, a.seed, nb, threads)
@@ -363,6 +410,7 @@ def gpu_arm(a, w):
     e2e_val = world * kv_bytes / (e2e_ms / 1e3) / 1e9
     g.check_device_error(stream)
 
+    traffic = stored_traffic(w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_step,
@@ -381,7 +429,9 @@ def gpu_arm(a, w):
         "us_per_step": 1e3 * ms_step,
         "hbm_fraction": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": sum(traffic.values()) if traffic else None,
+                     "traffic_by_kernel": traffic,
                      "kernel": "gqa_decode_step (fused append + split-KV kernel + combine), "
                                "average over the timed steps",
                      "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind
@@ -393,11 +443,11 @@ def gpu_arm(a, w):
         "clocks": clk,
     }
     if rank == 0 and not a.no_cpu_baseline:
-        dt, nb, by, threads = oracle_sample(w, a.seed, a.cpu_seconds)
+        dt, nb, by, threads, reps = oracle_sample(w, a.seed, a.cpu_seconds)
         line["cpu_baseline"] = {
             "value": by / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": "%d of %d sequences (all heads), %.1f s, double precision; %s"
-                      % (nb, w.B, dt, cpu_model())}
+            "sample": "%d of %d sequences (all heads) x %d repetitions, %.1f s, "
+                      "double precision; %s" % (nb, w.B, reps, dt, cpu_model())}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
