@@ -57,7 +57,7 @@ struct TcCfg {
     static constexpr int KCH = D / 128;               // ring chunks per K (or V) tile
     static constexpr int QB = (D / 64) * NP * 128;    // one q buffer (swizzled, K-major)
     static constexpr int PB = NP * kT * 2;            // one P^T operand (bf16); hi and lo per stage
-    static constexpr int NBAR_FIXED = 13;
+    static constexpr int NBAR_FIXED = 14;
     static constexpr int FIXED = 2 * QB + 4 * 64 * 4 + 3 * 64 * 4 + 64 +
                                  (int)sizeof(SchedScratch) + 1024 + (2 * 5 + NBAR_FIXED) * 8;
     // P^T stages (each holding the hi and lo parts): two when the ring still
@@ -289,13 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.len_add && itk.last_tile_of_segment() && itk.len >= 1 && itk.len <= p.Lmax)
                     append_row_warp(p, z, itk.len - 1, D, lane);
 #pragma unroll
-                for (int c = 0; c < KCH && ok; ++c) ok = issue(&tmk, c, itk.t * kT, z);
+                for (int c = 0; c < KCH && ok; ++c) ok = issue(&tmk, c, itk.row0(), z);
                 itk.next();
             }
             if (r >= 1 && ok) {  // V of tile r-1
                 const int z = itv.b * p.Hkv + itv.seg / p.head_groups;
 #pragma unroll
-                for (int c = 0; c < KCH && ok; ++c) ok = issue(&tmv, c, itv.t * kT, z);
+                for (int c = 0; c < KCH && ok; ++c) ok = issue(&tmv, c, itv.row0(), z);
                 itv.next();
             }
         }
@@ -505,9 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bs.s_empty[sb]);
 
-            const int pos0 = it.t * kT;
-            const int nvalid = max(0, min(kT, len - pos0));
-            const bool valid = row < nvalid;
+            // rows of the box before this tile's first new position repeat
+            // positions already attended (or are zeros before row 0)
+            const int r0 = it.row0();
+            const bool valid = row >= it.t * kT - r0 && r0 + row < len;
             bool over = false;
 #pragma unroll
             for (int g = 0; g < NP; g += 4) {
@@ -602,31 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 *reinterpret_cast<uint4 *>(pdst + C::PB + c * (kT / 8) * 128) =
                     make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
-            }
-            if (nvalid < kT && row >= nvalid) {
-                // rows past the length take part in P.V with p = 0; clear their
-                // V rows so that non-finite padding cannot turn 0 * v into NaN.
-                // First make sure the slots' previous occupants have been
-                // consumed (PV of tile i-1 done), so the parity waits below
-                // refer to this tile's V chunks.
-                if (i >= 1) {
-                    const long long j = i - 1;
-                    if (!wait_bar(&bs.pv_done[j & 1], (uint32_t)((j >> 1) & 1), abort_flag))
-                        fail = true;
-                }
-#pragma unroll
-                for (int db = 0; db < KCH; ++db) {
-                    const long long idx = v_chunk<KCH>(i, db, ntiles);
-                    const int slot = (int)(idx % NCH);
-                    if (!wait_bar(&bs.chunk_full[slot], (uint32_t)((idx / NCH) & 1), abort_flag))
-                        fail = true;
-                    uint8_t *vrow = ring + slot * kChunk + row * 128;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        *reinterpret_cast<uint4 *>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(vrow + 16384 + k * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                }
             }
             fence_proxy_async_smem();
             tc_fence_before();

@@ -230,6 +230,12 @@ struct TileIter {
         nt = seq_ntiles(len, Lmax, tile);
     }
     __device__ __forceinline__ bool last_tile_of_segment() const { return t == nt - 1; }
+    // First cache row of the tile's box.  A segment's last tile is moved back
+    // to end exactly at the length (rows before 0 read as zeros), so no tile
+    // ever covers rows past the length: padding is never loaded.
+    __device__ __forceinline__ int row0() const {
+        return (t == nt - 1) ? seq_valid_len(len, Lmax) - tile : t * tile;
+    }
     __device__ __forceinline__ void next() {
         if (++t < nt) return;
         t = 0;

@@ -193,6 +193,34 @@ def test_tensor_core_split_pieces(ctas):
         g.set_tuning(0, 0)
 
 
+@pytest.mark.parametrize("ctas", [1, 2, 5, 152])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 2), (256, 96, 2)])
+def test_tensor_core_many_short_pieces_with_padding(ctas, D, Hq, Hkv):
+    # runs of one- to three-tile segments, most ending in a partial tile, with
+    # non-finite padding: consecutive pieces alternate between the two output
+    # buffers, and a partial tile's padded V rows are cleared while the next
+    # tile is already in flight (D = 256 with 48 heads per pass has a single
+    # probability stage and clears them at once)
+    dev = torch.device("cuda")
+    lens = (1, 129, 300, 128, 2, 257, 5, 383, 64, 256, 1, 200, 130, 17, 384, 255)
+    w = wl.Workload("short", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, Lmax=384,
+                    scale=1.0 / np.sqrt(D), lens=lens)
+    x = wl.make_inputs(w, seed=ctas + D, device=dev)
+    for b, n in enumerate(lens):
+        x["k_cache"][b, :, n:] = float("nan")
+        x["v_cache"][b, :, n:] = float("inf")
+    g.set_tuning(2, ctas)
+    try:
+        out = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale)
+        g.check_device_error()
+    finally:
+        g.set_tuning(0, 0)
+    lens_np = x["attn_lens"].cpu().numpy()
+    ref = oracle.gqa_decode(bits(x["q"]), bits(x["k_cache"]), bits(x["v_cache"]), lens_np,
+                            w.scale, nthreads=oracle_threads())
+    assert_close(out, ref, bits(x["v_cache"]), lens_np)
+
+
 @pytest.mark.parametrize("name,calls", [("palm8b_mqa", 400), ("palm540b_long_mqa", 150),
                                         ("llama70b_gqa_ragged", 150)])
 def test_many_back_to_back_calls_are_stable(name, calls):
