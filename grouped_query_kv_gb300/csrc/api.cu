@@ -116,9 +116,11 @@ struct Plan {
     int np;  // tensor-core path: heads per pass rounded up to 16
 };
 
-// Path choice: the tensor-core kernel when a K/V head serves G >= 8 query
-// heads (every position then meets a dense G x D block of work) and D is 128
-// or 256; the CUDA-core kernel otherwise.
+// Path choice: the tensor-core kernel whenever D is 128 or 256, for every
+// group size G (heads are padded to a multiple of 16 MMA columns, which the
+// tensor pipe absorbs: measured on GB300 it streams at copy bandwidth even
+// at G = 1, where the CUDA-core kernel is instruction-bound); the CUDA-core
+// kernel for D = 64.
 int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
     (void)Lmax;
     (void)B;
@@ -126,7 +128,7 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
     kvattn_plan &p = pl->pub;
     memset(&p, 0, sizeof p);
     const bool tc_ok = (D == 128 || D == 256);
-    int path = (G >= 8 && tc_ok) ? 2 : 1;
+    int path = tc_ok ? 2 : 1;
     if (g_force_path == 1) path = 1;
     if (g_force_path == 2) {
         if (!tc_ok)

@@ -1,13 +1,14 @@
-// decode_fma.cu -- split-KV decode attention on the CUDA cores (FMA), for
-// small query groups (G < 8) and as the general path for any (D, G).
+// decode_fma.cu -- split-KV decode attention on the CUDA cores (FMA): the
+// path for D = 64, and a general path for any (D, G) that tests force.
 //
 // One persistent CTA per SM: warp 4 streams K/V tiles of `T` cached
 // positions from HBM into a ring of shared-memory stages with TMA
 // (cp.async.bulk.tensor, 128-byte swizzle, one tile = D/64 boxes of
 // 64 elements x T rows for K and the same for V); warps 0-3 consume them.
 // Each K/V tile is read from HBM once and used by every query head of the
-// segment ("grouped multi-query attention ... share [K/V heads] with many Q
-// heads", "The Basics of Transformer Inference").
+// segment: in grouped-query attention several query heads share one K/V
+// head ("The Basics of Transformer Inference", item "Grouped multi-query
+// attention").
 //
 // Per tile, in the consumers:
 //   1. scores  s[g][j] = (scale*log2e*q_g) . k_j     one thread per position

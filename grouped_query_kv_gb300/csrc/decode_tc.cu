@@ -1,5 +1,6 @@
 // decode_tc.cu -- split-KV decode attention on the 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory), for query groups G >= 8.
+// cores (tcgen05, accumulators in tensor memory), for any query group size
+// G when D is 128 or 256.
 //
 // Grouped-query attention shares each K/V head among G query heads ("The
 // Basics of Transformer Inference", item "Grouped multi-query attention";

@@ -161,8 +161,9 @@ def test_each_path_on_each_head_shape(path, D, Hq, Hkv):
 
 @pytest.mark.parametrize("path", [1, 2])
 def test_non_finite_padding_is_never_used(path):
-    # rows at and past each length hold NaN keys and infinite values; the
-    # pages' "only read the non-padding part" means none of it may leak
+    # rows at and past each length hold NaN keys and infinite values; padding
+    # is not part of the attention ("The Basics of Transformer Inference",
+    # item "Using ragged HBM reads and Paged Attention"), so none of it may leak
     dev = torch.device("cuda")
     w = wl.Workload("nanpad", B=4, Hq=16, Hkv=2, D=128, Lmax=600, scale=0.088,
                     lens=(600, 5, 130, 257))
