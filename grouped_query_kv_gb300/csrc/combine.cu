@@ -5,14 +5,15 @@
 // The split-KV kernel leaves one record per CTA; CTA c's record names a
 // segment when c is the first cut inside it.  Block (x, y) merges the
 // segment of the x-th such record (found with a block-wide ballot over the
-// records), y picks a slice of kThreads of the segment's heads x D outputs
-// (one output per thread).  For each head in the slice one warp weighs the
-// pieces once -- w_s = 2^(m_s - m*), and the denominator -- into shared
-// memory; every thread then only streams its o_s values, independent loads
-// that can all be in flight.  The grid has at most min(CTAs, segments) rows.
-// Launched
-// with programmatic serialisation: it waits on the split-KV kernel with
-// griddepcontrol.wait instead of a full launch gap.
+// records), y picks a slice of 4 x kThreads of the segment's heads x D
+// outputs (four consecutive d per thread, as float4).  Each thread loads its
+// head's (m_s, l_s) and its own o_s for a batch of pieces at once -- all
+// independent loads, one round trip -- and forms the weights itself (the
+// (m, l) loads of a warp hit one or two addresses).  Batches after the first
+// fold in with an online rescale.  The grid has at most min(CTAs, segments)
+// rows, and few blocks: a large grid takes microseconds just to be placed.  Launched with programmatic
+// serialisation: it waits on the split-KV kernel with griddepcontrol.wait
+// instead of a full launch gap.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -20,9 +21,8 @@ namespace kvattn {
 
 namespace {
 
-constexpr int kThreads = 256;       // one output (head, d) per thread
-constexpr int kMaxPieces = 64;      // pieces weighed per batch (per head, in shared memory)
-constexpr int kMaxHeadsPerBlock = kThreads / 64;  // D >= 64
+constexpr int kThreads = 256;  // four outputs (head, d..d+3) per thread
+constexpr int kBatch = 8;      // pieces whose loads are in flight together
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -33,8 +33,6 @@ __device__ __forceinline__ float ex2(float x) {
 __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p, int num_ctas) {
     __shared__ int s_wcount[kThreads / 32];
     __shared__ int s_owner;
-    __shared__ float s_w[kMaxHeadsPerBlock][kMaxPieces];
-    __shared__ float s_m[kMaxHeadsPerBlock], s_den[kMaxHeadsPerBlock], s_scale[kMaxHeadsPerBlock];
     // the next kernel in the stream may start its prologue while this one
     // runs; it waits for these writes with its own griddepcontrol.wait
     pdl_launch_dependents();
@@ -71,77 +69,57 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
     const int h0 = kvh * p.G + hg * p.heads_per_seg;
     const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
     const int D = p.D;
-    // this block's heads: kThreads consecutive (head, d) outputs
-    const int x0 = blockIdx.y * kThreads;
-    const int g_lo = x0 / D;
-    const int g_hi = min(gvalid - 1, (x0 + kThreads - 1) / D);
-    if (g_lo >= gvalid) return;
-
-    // warp w (< heads in the block) forms its head's weights: lane k takes
-    // pieces k, k+32, ...; the max is a warp reduction
-    const int x = x0 + tid;
+    const int x = (blockIdx.y * kThreads + tid) * 4;
     const int g = x / D, d = x % D;
-    float num = 0.f;
-    for (int k0 = 0; k0 < npieces; k0 += kMaxPieces) {
-        const int nk = min(kMaxPieces, npieces - k0);
-        if (warp <= g_hi - g_lo) {
-            const int gw = g_lo + warp;
-            float mk[kMaxPieces / 32], lk[kMaxPieces / 32];
-            float mx = -INFINITY;
+    if (g >= gvalid) return;
+
+    // piece k's workspace slot: the first piece is the last piece of CTA
+    // c-1 (or its first), piece k >= 1 is the first piece of CTA c + k - 1
+    float mrun = -INFINITY, den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < npieces; k0 += kBatch) {
+        const int nk = min(kBatch, npieces - k0);
+        float mk[kBatch], lk[kBatch];
+        float4 ok[kBatch];
 #pragma unroll
-            for (int u = 0; u < kMaxPieces / 32; ++u) {
-                const int k = u * 32 + lane;
-                mk[u] = -INFINITY;
-                lk[u] = 0.f;
-                if (k < nk) {
-                    const int kk = k0 + k;
-                    const size_t slot = (kk == 0) ? first_slot : 2 * (c + kk - 1);
-                    const size_t ml = (slot * p.heads_per_seg + gw) * 2;
-                    mk[u] = p.ws_ml[ml];
-                    lk[u] = p.ws_ml[ml + 1];
-                }
-                mx = fmaxf(mx, mk[u]);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            // fold the previous batches into this batch's reference
-            const float m_prev = (k0 == 0) ? -INFINITY : s_m[warp];
-            const float m_new = fmaxf(m_prev, mx);
-            float dsum = 0.f;
-#pragma unroll
-            for (int u = 0; u < kMaxPieces / 32; ++u) {
-                const int k = u * 32 + lane;
-                const float w = (m_new == -INFINITY || mk[u] == -INFINITY) ? 0.f : ex2(mk[u] - m_new);
-                if (k < nk) s_w[warp][k] = w;
-                dsum = fmaf(w, lk[u], dsum);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-            if (lane == 0) {
-                const float a = (m_prev == -INFINITY || m_new == -INFINITY) ? 0.f : ex2(m_prev - m_new);
-                s_scale[warp] = a;
-                s_den[warp] = ((k0 == 0) ? 0.f : s_den[warp] * a) + dsum;
-                s_m[warp] = m_new;
-            }
-        }
-        __syncthreads();
-        if (g < gvalid) {
-            const int wi = g - g_lo;
-            float acc = num * s_scale[wi];
-#pragma unroll 8
-            for (int k = 0; k < nk; ++k) {
+        for (int k = 0; k < kBatch; ++k) {
+            mk[k] = -INFINITY;
+            lk[k] = 0.f;
+            ok[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < nk) {
                 const int kk = k0 + k;
-                const size_t slot = (kk == 0) ? first_slot : 2 * (c + kk - 1);
-                acc = fmaf(s_w[wi][k], p.ws_o[(slot * p.heads_per_seg + g) * D + d], acc);
+                const size_t slot = (kk == 0) ? first_slot : 2 * (size_t)(c + kk - 1);
+                const size_t hs = slot * p.heads_per_seg + g;
+                const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + hs * 2);
+                mk[k] = ml.x;
+                lk[k] = ml.y;
+                ok[k] = *reinterpret_cast<const float4 *>(p.ws_o + hs * D + d);
             }
-            num = acc;
         }
-        __syncthreads();
+        float mx = mrun;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) mx = fmaxf(mx, mk[k]);
+        if (mx == -INFINITY) continue;  // nothing but empty pieces so far
+        const float a = (mrun == -INFINITY) ? 0.f : ex2(mrun - mx);
+        num.x *= a;
+        num.y *= a;
+        num.z *= a;
+        num.w *= a;
+        den *= a;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float w = (mk[k] == -INFINITY) ? 0.f : ex2(mk[k] - mx);
+            num.x = fmaf(w, ok[k].x, num.x);
+            num.y = fmaf(w, ok[k].y, num.y);
+            num.z = fmaf(w, ok[k].z, num.z);
+            num.w = fmaf(w, ok[k].w, num.w);
+            den = fmaf(w, lk[k], den);
+        }
+        mrun = mx;
     }
-    if (g < gvalid) {
-        const float den = s_den[g - g_lo];
-        p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (den > 0.f) ? num / den : 0.f;
-    }
+    const float inv = (den > 0.f) ? 1.f / den : 0.f;
+    *reinterpret_cast<float4 *>(p.out + ((size_t)b * p.Hq + h0 + g) * D + d) =
+        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
 }
 
 }  // namespace
@@ -151,7 +129,7 @@ cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t str
     const long long segs = (long long)p.B * p.Hkv * p.head_groups;
     const int rows = (int)(segs < num_ctas ? segs : num_ctas);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows, (p.heads_per_seg * p.D + kThreads - 1) / kThreads);
+    cfg.gridDim = dim3(rows, (p.heads_per_seg * p.D / 4 + kThreads - 1) / kThreads);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

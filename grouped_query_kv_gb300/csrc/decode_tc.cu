@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stands between reading the lengths and the first TMA load
     const LenView lens{p.seq_lens, p.len_add};
     const SchedStart st = warp_locate(lens, p.B, p.Lmax, kT, segs_per_b, blockIdx.x, gridDim.x);
-    if (tid == 0) sched_split_record(lens, p.Lmax, kT, blockIdx.x, st, p.split);
+    // (a softmax thread: the producer goes straight to its first loads)
+    if (tid == 64) sched_split_record(lens, p.Lmax, kT, blockIdx.x, st, p.split);
     if (!st.found || st.g_begin >= st.g_end) {
         if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
         pdl_launch_dependents();
