@@ -222,6 +222,34 @@ def test_tensor_core_many_short_pieces_with_padding(ctas, D, Hq, Hkv):
     assert_close(out, ref, bits(x["v_cache"]), lens_np)
 
 
+def test_split_merges_across_changing_shapes():
+    # calls of different shapes and split structures, queued on one stream
+    # with no synchronisation in between, twice over: no state that one call
+    # leaves on the device (workspace, split records) may leak into the next
+    dev = torch.device("cuda")
+    shapes = [
+        wl.Workload("m16", B=3, Hq=16, Hkv=1, D=128, Lmax=3000, scale=0.088,
+                    lens=(3000, 700, 129)),
+        wl.Workload("m48", B=2, Hq=96, Hkv=2, D=256, Lmax=2500, scale=1 / 16,
+                    lens=(2500, 1300), k_scale=0.5),
+        wl.Workload("m8", B=6, Hq=32, Hkv=4, D=128, Lmax=1500, scale=0.088,
+                    lens=(1500, 1, 640, 1499, 300, 1024)),
+    ]
+    inputs = [wl.make_inputs(w, seed=40 + i, device=dev) for i, w in enumerate(shapes)]
+    outs = []
+    for _ in range(2):
+        for w, x in zip(shapes, inputs):
+            outs.append(g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"],
+                                          w.scale))
+    g.check_device_error()
+    for r in range(2):
+        for i, (w, x) in enumerate(zip(shapes, inputs)):
+            lens_np = x["attn_lens"].cpu().numpy()
+            ref = oracle.gqa_decode(bits(x["q"]), bits(x["k_cache"]), bits(x["v_cache"]), lens_np,
+                                    w.scale, nthreads=oracle_threads())
+            assert_close(outs[r * len(shapes) + i], ref, bits(x["v_cache"]), lens_np)
+
+
 @pytest.mark.parametrize("name,calls", [("palm8b_mqa", 400), ("palm540b_long_mqa", 150),
                                         ("llama70b_gqa_ragged", 150)])
 def test_many_back_to_back_calls_are_stable(name, calls):
