@@ -114,6 +114,7 @@ struct Plan {
     kvattn_plan pub;
     int heads_per_seg;
     int np;  // tensor-core path: heads per pass rounded up to 16
+    int cost_piece;  // schedule weight of a piece (a tile weighs 32)
 };
 
 // Path choice: the tensor-core kernel whenever D is 128 or 256, for every
@@ -153,6 +154,12 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
     }
     p.heads_per_cta = pl->heads_per_seg;
     p.head_groups = (G + pl->heads_per_seg - 1) / pl->heads_per_seg;
+    // CTA ranges balance cost: a tile costs W and a piece (q load, the first
+    // tile's exact max, the output's read-out and stores) costs P more.
+    // Measured on GB300 with the tensor-core kernel, a piece takes about
+    // (0.6 + 0.05 NP) tiles' time at D = 128 and half as many D = 256 tiles
+    // (twice the bytes each).
+    pl->cost_piece = path == 2 ? (int)lround(32.0 * (0.6 + 0.05 * pl->np) * 128.0 / D) : 16;
     const int ctas = g_force_ctas > 0 ? g_force_ctas : num_sms;
     p.num_ctas = ctas;
     p.workspace_bytes = (int64_t)2 * ctas * pl->heads_per_seg * (D + 2) * (int64_t)sizeof(float) +
@@ -185,6 +192,9 @@ int check_sizes(int B, int Hq, int Hkv, int D, int Lmax) {
     if (B > 65535 || Hkv > 4096 || Hq > 8192 || Lmax > (1 << 24))
         return fail(KVATTN_ERR_UNSUPPORTED,
                     "sizes beyond limits (B<=65535, Hkv<=4096, Hq<=8192, Lmax<=2^24)");
+    // the kernels count one segment's tiles of all sequences in 32 bits
+    if ((long long)B * ((Lmax + 63) / 64) > (1LL << 30))
+        return fail(KVATTN_ERR_UNSUPPORTED, "B * ceil(Lmax / 64) beyond 2^30 (B=%d Lmax=%d)", B, Lmax);
     return KVATTN_OK;
 }
 
@@ -386,6 +396,7 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     p.heads_per_seg = pl.heads_per_seg;
     p.head_groups = P.head_groups;
     p.tile = P.tile_positions;
+    p.cost_piece = pl.cost_piece;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaError_t e;

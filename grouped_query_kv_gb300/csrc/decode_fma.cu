@@ -53,8 +53,7 @@ struct FmaSmem {
     static constexpr int off_redm = off_o + GC * D * 4;
     static constexpr int off_redl = off_redm + 4 * GC * 4;
     static constexpr int off_bar = (off_redl + 4 * GC * 4 + 7) & ~7;
-    static constexpr int off_sched = off_bar + 2 * C::STAGES * 8;
-    static constexpr int bytes = off_sched + (int)sizeof(SchedScratch);
+    static constexpr int bytes = off_bar + 2 * C::STAGES * 8;
     static constexpr int alloc = bytes + 1024;  // slack to align the base to 1024 B
 };
 
@@ -97,7 +96,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *red_l = reinterpret_cast<float *>(smem + S::off_redl);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::off_bar);
     uint64_t *empty = full + C::STAGES;
-    SchedScratch *sched = reinterpret_cast<SchedScratch *>(smem + S::off_sched);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -116,9 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
     const LenView lens{p.seq_lens, p.len_add};
-    sched_locate(lens, p.B, p.Lmax, T, segs_per_b, blockIdx.x, gridDim.x, sched);
-    const SchedStart st = sched->res;
-    if (tid == 0) sched_split_record(lens, p.Lmax, T, blockIdx.x, st, p.split);
+    const SchedCost wcost{p.cost_piece};
+    const SchedStart st = warp_locate(lens, p.B, p.Lmax, T, segs_per_b, wcost, blockIdx.x, gridDim.x);
+    if (warp == 0) sched_split_record(lens, p.B, p.Lmax, T, segs_per_b, wcost, blockIdx.x, st, p.split);
     if (!st.found || st.g_begin >= st.g_end) {
         pdl_launch_dependents();
         return;

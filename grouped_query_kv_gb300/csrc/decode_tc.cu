@@ -60,7 +60,7 @@ struct TcCfg {
     static constexpr int PB = NP * kT * 2;            // one P^T operand (bf16); hi and lo per stage
     static constexpr int NBAR_FIXED = 14;
     static constexpr int FIXED = 2 * QB + 4 * 64 * 4 + 3 * 64 * 4 + 64 +
-                                 (int)sizeof(SchedScratch) + 1024 + (2 * 5 + NBAR_FIXED) * 8;
+                                 1024 + (2 * 5 + NBAR_FIXED) * 8;
     // P^T stages (each holding the hi and lo parts): two when the ring still
     // fits one K and one V tile, else one (then tile i's P waits for PV of i-1)
     static constexpr int NCH_2P = (kSmemLimit - FIXED - 2 * 2 * PB) / kChunk;
@@ -79,8 +79,7 @@ struct TcCfg {
     static constexpr int off_bar = off_alpha + 64 * 4;
     static constexpr int nbar = 2 * NCH + NBAR_FIXED;
     static constexpr int off_misc = off_bar + nbar * 8;  // tmem base, abort flag
-    static constexpr int off_sched = (off_misc + 64 + 15) & ~15;
-    static constexpr int bytes = off_sched + (int)sizeof(SchedScratch);
+    static constexpr int bytes = off_misc + 64;
     static constexpr int alloc = bytes + 1024;
 
     // TMEM columns: S0, S1 (NP each), then per 128-row head-dim block an O
@@ -223,10 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // each warp locates the CTA's tile range by itself: no block barrier
     // stands between reading the lengths and the first TMA load
     const LenView lens{p.seq_lens, p.len_add};
-    const SchedStart st = warp_locate(lens, p.B, p.Lmax, kT, segs_per_b, blockIdx.x, gridDim.x);
-    // (a softmax thread: the producer goes straight to its first loads)
-    if (tid == 64) sched_split_record(lens, p.Lmax, kT, blockIdx.x, st, p.split);
-    if (!st.found || st.g_begin >= st.g_end) {
+    const SchedCost wcost{p.cost_piece};
+    const SchedStart st = warp_locate(lens, p.B, p.Lmax, kT, segs_per_b, wcost, blockIdx.x, gridDim.x);
+    // (a softmax warp writes the record: the producer goes straight to its loads)
+    if (warp == 2) sched_split_record(lens, p.B, p.Lmax, kT, segs_per_b, wcost, blockIdx.x, st, p.split);
+    if (!st.found) {  // (a range that has a start is never empty)
         if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
         pdl_launch_dependents();
         return;

@@ -1,11 +1,19 @@
 // schedule.cuh -- the persistent grid's split of the flat tile list.
 //
 // Every segment (b, kvh, hg) owns ntiles(len_b) tiles; the list of all tiles
-// in (b, kvh, hg, t) order is cut into ctas_eff = min(gridDim.x, total)
-// contiguous ranges [c*total/ctas_eff, (c+1)*total/ctas_eff).  Because
-// ctas_eff <= total, every range is non-empty.  Lengths live on the device,
-// so each CTA locates its own start with a block-wide scan over seq_lens (no
-// host synchronisation; ragged batches balance to within one tile per CTA).
+// in (b, kvh, hg, t) order is cut into contiguous CTA ranges of equal COST.
+// A segment of nt tiles costs nt * W + P: W per tile, and P for the fixed
+// work of starting and finishing a piece (its q load, the first tile's exact
+// max, reading out and storing the output), charged at its first tile.  So
+// tile t of a segment whose cost starts at B0 starts at cost B0 for t = 0 and
+// at B0 + P + W t for t >= 1, and with TC the total cost and C the CTAs,
+//     CTA c owns the tiles whose start cost s has  T(c) <= s < T(c + 1),
+//     T(c) = ceil(c TC / C).
+// C = min(gridDim.x, tiles, TC / (W + P)): every share is then at least as
+// long as the costliest tile, and consecutive start costs are at most W + P
+// apart, so no range is empty.  With P = 0 this is the plain equal split.
+// Lengths live on the device, so each CTA locates its own range with a
+// warp-level scan over seq_lens (no host synchronisation).
 #pragma once
 
 #include <cstdint>
@@ -29,25 +37,31 @@ struct LenView {
 // valid positions (zero output row; out-of-range lengths also raise the
 // device error word).
 __device__ __forceinline__ int seq_ntiles(int len, int Lmax, int tile) {
-    return (len <= 0 || len > Lmax) ? 1 : (len + tile - 1) / tile;
+    // tiles are a power of two positions (64 or 128): a shift, not a division
+    return (len <= 0 || len > Lmax) ? 1 : (len + tile - 1) >> (__ffs(tile) - 1);
 }
 
 __device__ __forceinline__ int seq_valid_len(int len, int Lmax) {
     return (len < 0 || len > Lmax) ? 0 : len;
 }
 
+// The cost model's weights: W = kCostTile per tile (a power of two, so the
+// kernels divide by shifting) and P = DecodeParams::cost_piece per segment.
+constexpr int kCostTile = 32;
+constexpr int kCostTileShift = 5;
+struct SchedCost {
+    int P;
+};
+
 struct SchedStart {
     long long total;    // tiles in the whole call
+    long long cost;     // total cost TC
     long long g_begin;  // this CTA's first tile
     long long g_end;    // one past its last tile
+    long long cost0;    // start cost of the segment that holds g_begin
     int ctas_eff;
     int found;          // 1 if this CTA has work
     int b, seg, t;      // coordinates of g_begin: sequence, segment within b, tile
-};
-
-struct SchedScratch {
-    long long part[32];
-    SchedStart res;
 };
 
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
@@ -56,143 +70,190 @@ __device__ __forceinline__ long long warp_sum_ll(long long v) {
     return v;
 }
 
-__device__ __forceinline__ long long warp_incl_scan_ll(long long v) {
+__device__ __forceinline__ int warp_incl_scan(int v) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        long long n = __shfl_up_sync(0xffffffffu, v, o);
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += n;
     }
     return v;
 }
 
-// Locate CTA `c`'s tile range.  Every thread of the block must call it
-// (blockDim.x a multiple of 32, at most 1024); the result is left in sh->res.
-__device__ inline void sched_locate(LenView lens, int B, int Lmax, int tile,
-                             int segs_per_b, int c, int grid, SchedScratch *sh) {
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+// A tile found by its start cost.
+struct SchedHit {
+    long long g;      // tile index (the total if the cost is past the end)
+    long long cost0;  // start cost of its segment
+    int b, seg, t;
+};
 
-    long long mine = 0;
-    for (int b = tid; b < B; b += nthr) mine += seq_ntiles(lens[b], Lmax, tile);
-    mine = warp_sum_ll(mine);
-    if (lane == 0) sh->part[warp] = mine;
-    __syncthreads();
-    if (tid == 0) {
-        long long tot = 0;
-        for (int w = 0; w < nwarps; ++w) tot += sh->part[w];
-        tot *= segs_per_b;
-        SchedStart r;
-        r.total = tot;
-        r.ctas_eff = (int)(tot < (long long)grid ? tot : (long long)grid);
-        r.found = 0;
-        r.b = r.seg = r.t = 0;
-        if (c < r.ctas_eff) {
-            r.g_begin = (long long)c * tot / r.ctas_eff;
-            r.g_end = (long long)(c + 1) * tot / r.ctas_eff;
-        } else {
-            r.g_begin = r.g_end = tot;
+// Where cost T falls in a sequence whose cost starts at ec (segments of segc,
+// nt tiles each): the tile, its segment's start cost and coordinates.
+__device__ __forceinline__ SchedHit sched_hit_in(long long T, long long ec, int segc, int nt,
+                                                 long long tiles_before, int b, int segs_per_b,
+                                                 int P) {
+    const unsigned long long rb = (unsigned long long)(T - ec);
+    int seg = (int)(rb <= 0xffffffffull ? (unsigned)rb / (unsigned)segc
+                                        : rb / (unsigned long long)segc);
+    const int rem = (int)(rb - (unsigned long long)seg * segc);
+    int t = rem == 0 ? 0 : max(1, (rem - P + kCostTile - 1) >> kCostTileShift);
+    SchedHit h;
+    h.g = tiles_before + (long long)seg * nt + t;
+    h.cost0 = ec + (long long)seg * segc;
+    h.b = b;
+    if (t >= nt) {  // the next segment's first tile
+        t = 0;
+        h.cost0 += segc;
+        if (++seg == segs_per_b) {
+            seg = 0;
+            ++h.b;
         }
-        sh->res = r;
     }
-    __syncthreads();
-    const long long g_begin = sh->res.g_begin;
-    const bool active = c < sh->res.ctas_eff;
-    __syncthreads();
-    if (!active) return;
-
-    long long carry = 0;
-    for (int base = 0; base < B; base += nthr) {
-        const int b = base + tid;
-        const int nt = (b < B) ? seq_ntiles(lens[b], Lmax, tile) : 0;
-        const long long v = (long long)nt * segs_per_b;
-        const long long incl = warp_incl_scan_ll(v);
-        if (lane == 31) sh->part[warp] = incl;
-        __syncthreads();
-        long long woff = 0, chunk = 0;
-        for (int w = 0; w < nwarps; ++w) {
-            const long long pw = sh->part[w];
-            if (w < warp) woff += pw;
-            chunk += pw;
-        }
-        const long long excl = carry + woff + incl - v;
-        if (b < B && excl <= g_begin && g_begin < excl + v) {
-            const long long rem = g_begin - excl;
-            sh->res.b = b;
-            sh->res.seg = (int)(rem / nt);
-            sh->res.t = (int)(rem % nt);
-            sh->res.found = 1;
-        }
-        __syncthreads();
-        carry += chunk;
-        if (carry > g_begin) break;  // uniform: carry is the same in every thread
-    }
-    __syncthreads();
+    h.seg = seg;
+    h.t = t;
+    return h;
 }
 
-// Warp-level variant of sched_locate: every warp of a CTA can locate the
-// CTA's range on its own, without block barriers, so the TMA producer can
-// start as soon as the lengths have been read.  Same result as sched_locate.
-__device__ inline SchedStart warp_locate(LenView lens, int B, int Lmax,
-                                         int tile, int segs_per_b, int c, int grid) {
+__device__ __forceinline__ void sched_take(SchedHit *h, const SchedHit &mine, int src) {
+    h->g = __shfl_sync(0xffffffffu, mine.g, src);
+    h->cost0 = __shfl_sync(0xffffffffu, mine.cost0, src);
+    h->b = __shfl_sync(0xffffffffu, mine.b, src);
+    h->seg = __shfl_sync(0xffffffffu, mine.seg, src);
+    h->t = __shfl_sync(0xffffffffu, mine.t, src);
+}
+
+// Called by a whole warp: the first tiles whose start costs are >= T0 and
+// (NT = 2) >= T1, T0 <= T1.  The cost before sequence b is
+// segs_per_b * (W * (tiles of the sequences before b) + P * b).  Every lane
+// evaluates its own sequence for both bounds at once; a ballot picks the
+// lane that holds each.
+template <int NT>
+__device__ inline void sched_find(LenView lens, int B, int Lmax, int tile, int segs_per_b,
+                                  SchedCost w, long long T0, long long T1, long long total,
+                                  SchedHit *h0, SchedHit *h1) {
     const int lane = threadIdx.x & 31;
-    long long mine = 0;
-    for (int b = lane; b < B; b += 32) mine += seq_ntiles(lens[b], Lmax, tile);
-    const long long tot = warp_sum_ll(mine) * segs_per_b;
-    SchedStart r;
-    r.total = tot;
-    r.ctas_eff = (int)(tot < (long long)grid ? tot : (long long)grid);
-    r.found = 0;
-    r.b = r.seg = r.t = 0;
-    r.g_begin = r.g_end = tot;
-    if (c >= r.ctas_eff) return r;
-    r.g_begin = (long long)c * tot / r.ctas_eff;
-    r.g_end = (long long)(c + 1) * tot / r.ctas_eff;
-    long long carry = 0;
-    for (int base = 0; base < B; base += 32) {
+    h0->g = h1->g = total;
+    h0->cost0 = h1->cost0 = 0;
+    h0->b = h0->seg = h0->t = h1->b = h1->seg = h1->t = 0;
+    bool got0 = false, got1 = NT < 2;
+    int tcarry = 0;  // tiles of one segment of every sequence so far
+    for (int base = 0; base < B && !(got0 && got1); base += 32) {
         const int b = base + lane;
         const int nt = (b < B) ? seq_ntiles(lens[b], Lmax, tile) : 0;
-        const long long v = (long long)nt * segs_per_b;
-        const long long incl = warp_incl_scan_ll(v);
-        const long long excl = carry + incl - v;
-        const bool hit = (b < B) && excl <= r.g_begin && r.g_begin < excl + v;
-        const unsigned m = __ballot_sync(0xffffffffu, hit);
-        if (m) {
-            const int src = __ffs(m) - 1;
-            const long long rem = __shfl_sync(0xffffffffu, r.g_begin - excl, src);
-            const int ntb = __shfl_sync(0xffffffffu, nt, src);
-            r.b = base + src;
-            r.seg = (int)(rem / ntb);
-            r.t = (int)(rem % ntb);
-            r.found = 1;
-            break;
+        const int incl = warp_incl_scan(nt);
+        const int before = tcarry + incl - nt;
+        const int segc = nt * kCostTile + w.P;  // one segment of sequence b
+        const long long ec = (long long)segs_per_b * ((long long)before * kCostTile + (long long)w.P * b);
+        const long long vc = (b < B) ? (long long)segs_per_b * segc : 0;
+        const long long tb = (long long)before * segs_per_b;
+        const bool in0 = (b < B) && ec <= T0 && T0 < ec + vc;
+        const bool in1 = NT > 1 && (b < B) && ec <= T1 && T1 < ec + vc;
+        const SchedHit m0 = sched_hit_in(in0 ? T0 : ec, ec, segc > 0 ? segc : 1, nt, tb, b,
+                                         segs_per_b, w.P);
+        SchedHit m1 = m0;
+        if (NT > 1) m1 = sched_hit_in(in1 ? T1 : ec, ec, segc > 0 ? segc : 1, nt, tb, b, segs_per_b, w.P);
+        const unsigned b0 = __ballot_sync(0xffffffffu, in0);
+        const unsigned b1 = __ballot_sync(0xffffffffu, in1);
+        if (b0 && !got0) {
+            sched_take(h0, m0, __ffs(b0) - 1);
+            got0 = true;
         }
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+        if (NT > 1 && b1 && !got1) {
+            sched_take(h1, m1, __ffs(b1) - 1);
+            got1 = true;
+        }
+        tcarry += __shfl_sync(0xffffffffu, incl, 31);
     }
+}
+
+// Called by a whole warp: totals (tiles, cost) and the CTA count that the
+// split uses.
+__device__ inline void sched_totals(LenView lens, int B, int Lmax, int tile, int segs_per_b,
+                                    SchedCost w, int grid, long long *total, long long *cost,
+                                    int *ctas_eff) {
+    const int lane = threadIdx.x & 31;
+    int nt_lane = 0;
+    for (int b = lane; b < B; b += 32) nt_lane += seq_ntiles(lens[b], Lmax, tile);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nt_lane += __shfl_xor_sync(0xffffffffu, nt_lane, o);
+    const long long nt_sum = nt_lane;  // tiles of one segment of every sequence
+    *total = nt_sum * segs_per_b;
+    *cost = (long long)segs_per_b * (nt_sum * kCostTile + (long long)w.P * B);
+    long long ce = *total < (long long)grid ? *total : (long long)grid;
+    if (*cost < (long long)(kCostTile + w.P) * ce) ce = *cost / (kCostTile + w.P);
+    *ctas_eff = (int)(ce < 1 ? 1 : ce);
+}
+
+// Owner of a tile with start cost s.
+__device__ __forceinline__ int sched_owner(long long s, long long cost, int ctas_eff) {
+    const long long c = s * ctas_eff / cost;
+    return (int)(c < ctas_eff - 1 ? c : ctas_eff - 1);
+}
+
+// T(c) = ceil(c TC / C) = c q + ceil(c rem / C) with TC = q C + rem (the
+// last part in 32 bits: C <= 65535).
+__device__ __forceinline__ long long sched_bound(long long cost, int ctas_eff, int c) {
+    const long long q = cost / ctas_eff;
+    const unsigned rem = (unsigned)(cost - q * ctas_eff);
+    const unsigned C = (unsigned)ctas_eff;
+    return (long long)c * q + ((unsigned)c * rem + C - 1) / C;
+}
+
+// Locate CTA `c`'s tile range; called by a whole warp (every warp of a CTA
+// can do it on its own, so the TMA producer starts as soon as the lengths
+// have been read).
+__device__ inline SchedStart warp_locate(LenView lens, int B, int Lmax, int tile,
+                                         int segs_per_b, SchedCost w, int c, int grid) {
+    SchedStart r;
+    sched_totals(lens, B, Lmax, tile, segs_per_b, w, grid, &r.total, &r.cost, &r.ctas_eff);
+    r.found = 0;
+    r.b = r.seg = r.t = 0;
+    r.g_begin = r.g_end = r.total;
+    r.cost0 = 0;
+    if (c >= r.ctas_eff) return r;
+    const long long T0 = sched_bound(r.cost, r.ctas_eff, c);
+    const long long T1 = sched_bound(r.cost, r.ctas_eff, c + 1);
+    SchedHit h0, h1;
+    sched_find<2>(lens, B, Lmax, tile, segs_per_b, w, T0, T1, r.total, &h0, &h1);
+    r.g_end = h1.g;
+    r.g_begin = h0.g;
+    r.cost0 = h0.cost0;
+    r.b = h0.b;
+    r.seg = h0.seg;
+    r.t = h0.t;
+    r.found = h0.g < r.total ? 1 : 0;
     return r;
 }
 
-// The combine record of CTA c: when c's range starts strictly inside a
-// segment and c-1's range starts at or before that segment's start, c owns
-// the merge of the segment's pieces -- the last piece of CTA c-1 (or its
-// first, if c-1 started exactly at the segment start) and the first pieces
-// of CTAs c .. c_last.  Written as {b, seg, first_slot, pieces}, or b = -1.
-__device__ inline void sched_split_record(LenView lens, int Lmax, int tile,
-                                          int c, const SchedStart &st, int *rec) {
+// The combine record of CTA c, written by lane 0 of a whole calling warp:
+// when c's range starts strictly inside a segment and c-1's range starts at
+// or before that segment's start, c owns the merge of the segment's pieces
+// -- the last piece of CTA c-1 (or its first, if c-1 started exactly at the
+// segment start) and the first pieces of CTAs c .. c_last.  Written as
+// {b, seg, first_slot, pieces}, or b = -1.
+__device__ inline void sched_split_record(LenView lens, int B, int Lmax, int tile,
+                                          int segs_per_b, SchedCost w, int c,
+                                          const SchedStart &st, int *rec) {
+    const int lane = threadIdx.x & 31;
     int r0 = -1, r1 = 0, r2 = 0, r3 = 0;
     if (st.found && c > 0 && st.t > 0 && c < st.ctas_eff) {
-        const long long S0 = st.g_begin - st.t;
-        const long long g_prev = (long long)(c - 1) * st.total / st.ctas_eff;
-        if (g_prev <= S0) {
-            const long long S1 = S0 + seq_ntiles(lens[st.b], Lmax, tile);
-            const int c_last = (int)((S1 * st.ctas_eff - 1) / st.total);
+        const long long S0 = st.g_begin - st.t;  // the segment's first tile
+        // CTA c-1 holds the segment's start iff that start's cost is not
+        // below T(c-1)
+        const long long Tp = sched_bound(st.cost, st.ctas_eff, c - 1);
+        if (st.cost0 >= Tp) {
+            SchedHit hp, unused;
+            sched_find<1>(lens, B, Lmax, tile, segs_per_b, w, Tp, Tp, st.total, &hp, &unused);
+            const int nt = seq_ntiles(lens[st.b], Lmax, tile);
+            const long long last_cost = st.cost0 + (nt == 1 ? 0 : w.P + (long long)kCostTile * (nt - 1));
+            const int c_last = sched_owner(last_cost, st.cost, st.ctas_eff);
             r0 = st.b;
             r1 = st.seg;
-            r2 = (g_prev == S0) ? 2 * (c - 1) : 2 * (c - 1) + 1;
+            r2 = (hp.g == S0) ? 2 * (c - 1) : 2 * (c - 1) + 1;
             r3 = 1 + (c_last - c + 1);
         }
     }
-    reinterpret_cast<int4 *>(rec)[c] = make_int4(r0, r1, r2, r3);
+    if (lane == 0) reinterpret_cast<int4 *>(rec)[c] = make_int4(r0, r1, r2, r3);
 }
 
 // Fused append, called by all 32 lanes of the producer warp before any TMA
