@@ -57,6 +57,10 @@ def _bind(path):
     lib.oracle_gqa_decode.argtypes = [u16p, u16p, u16p, i32p, f64p,
                                       i64, i64, i64, i64, i64,
                                       ctypes.c_double, ctypes.c_int]
+    lib.oracle_gqa_decode_window.restype = ctypes.c_int
+    lib.oracle_gqa_decode_window.argtypes = [u16p, u16p, u16p, i32p, f64p,
+                                             i64, i64, i64, i64, i64,
+                                             ctypes.c_double, i64, ctypes.c_int]
     lib.oracle_gqa_decode_pairs.restype = ctypes.c_int
     lib.oracle_gqa_decode_pairs.argtypes = [u16p, u16p, u16p, i32p, f64p,
                                             i64, i64, i64, i64, i64,
@@ -136,7 +140,7 @@ class Oracle:
             raise ValueError("oracle_kv_append: seq_lens out of [0, Lmax)")
 
     def gqa_decode(self, q, k_cache, v_cache, seq_lens, scale, nthreads=1,
-                   pairs=None):
+                   pairs=None, window=None):
         """softmax(scale * q . K^T) . V per query head, in double.
 
         q:        uint16 [B, Hq, D] (bf16 bits)
@@ -144,6 +148,8 @@ class Oracle:
         seq_lens: int32 [B], positions [0, seq_lens[b]) take part
         pairs:    optional int64 [n, 2] list of (b, h) rows to compute; the
                   other rows of the returned array are left at zero.
+        window:   optional W >= 1: only positions [max(0, len - W), len)
+                  take part (a local attention layer); not with pairs.
         Returns float64 [B, Hq, D].
         """
         qa, q_p = _u16(q)
@@ -156,7 +162,13 @@ class Oracle:
             raise ValueError("shape mismatch")
         out = np.zeros((B, Hq, D), dtype=np.float64)
         out_p = out.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
-        if pairs is None:
+        if window is not None:
+            if pairs is not None:
+                raise ValueError("window and pairs together are not supported")
+            rc = self.lib.oracle_gqa_decode_window(q_p, k_p, v_p, sl_p, out_p, B, Hq,
+                                                   Hkv, D, Lmax, float(scale),
+                                                   int(window), int(nthreads))
+        elif pairs is None:
             rc = self.lib.oracle_gqa_decode(q_p, k_p, v_p, sl_p, out_p, B, Hq,
                                             Hkv, D, Lmax, float(scale),
                                             int(nthreads))

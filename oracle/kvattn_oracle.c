@@ -42,6 +42,14 @@
  *
  *   KV append: the new token's K and V rows are copied, element by element,
  *   into row seq_lens[b] of the cache (the number of tokens cached before it).
+ *
+ *   Local (sliding-window) layers: "The Basics of Transformer Inference", the
+ *   item on mixing in local attention layers -- a local layer caps how far
+ *   back a token attends (a diagonal strip of the attention matrix instead
+ *   of a triangle).  For a decode query at position len_b - 1 and a window
+ *   of W positions (the token itself included; a reading, the pages give no
+ *   formula) the sums above run over j = max(0, len_b - W) .. len_b - 1.
+ *   W >= len_b is the full attention.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -86,12 +94,13 @@ int oracle_kv_append(uint16_t *k_cache, uint16_t *v_cache,
 static void oracle_one_head(const uint16_t *q, const uint16_t *k_cache,
                             const uint16_t *v_cache, const int32_t *seq_lens,
                             double *out, int64_t Hq, int64_t Hkv, int64_t D,
-                            int64_t Lmax, double scale, int64_t b, int64_t h,
-                            double *s_buf)
+                            int64_t Lmax, double scale, int64_t window,
+                            int64_t b, int64_t h, double *s_buf)
 {
     const int64_t G = Hq / Hkv;
     const int64_t kvh = h / G;
     const int64_t len = seq_lens[b];
+    const int64_t j0 = len > window ? len - window : 0; /* first attended position */
     double *o = out + (b * Hq + h) * D;
 
     for (int64_t d = 0; d < D; ++d)
@@ -103,27 +112,28 @@ static void oracle_one_head(const uint16_t *q, const uint16_t *k_cache,
     const uint16_t *K = k_cache + (b * Hkv + kvh) * Lmax * D;
     const uint16_t *V = v_cache + (b * Hkv + kvh) * Lmax * D;
 
-    /* scores */
-    for (int64_t j = 0; j < len; ++j) {
+    /* scores (s_buf[j - j0] holds s_j) */
+    for (int64_t j = j0; j < len; ++j) {
         double dot = 0.0;
         for (int64_t d = 0; d < D; ++d)
             dot += oracle_bf16_to_double(qh[d]) * oracle_bf16_to_double(K[j * D + d]);
-        s_buf[j] = scale * dot;
+        s_buf[j - j0] = scale * dot;
     }
+    const int64_t n = len - j0;
     /* max */
     double m = s_buf[0];
-    for (int64_t j = 1; j < len; ++j)
+    for (int64_t j = 1; j < n; ++j)
         if (s_buf[j] > m)
             m = s_buf[j];
     /* normaliser */
     double denom = 0.0;
-    for (int64_t j = 0; j < len; ++j)
+    for (int64_t j = 0; j < n; ++j)
         denom += exp(s_buf[j] - m);
     /* weighted sum of values */
-    for (int64_t j = 0; j < len; ++j) {
+    for (int64_t j = 0; j < n; ++j) {
         double p = exp(s_buf[j] - m) / denom;
         for (int64_t d = 0; d < D; ++d)
-            o[d] += p * oracle_bf16_to_double(V[j * D + d]);
+            o[d] += p * oracle_bf16_to_double(V[(j0 + j) * D + d]);
     }
 }
 
@@ -133,6 +143,7 @@ typedef struct {
     double *out;
     int64_t B, Hq, Hkv, D, Lmax;
     double scale;
+    int64_t window;
     const int64_t *pairs; /* NULL: all (b,h); else npairs (b,h) pairs */
     int64_t first, last;  /* range of work items (pairs or flat b*Hq+h) */
     int status;
@@ -156,7 +167,7 @@ static void *oracle_worker(void *arg)
             h = w % j->Hq;
         }
         oracle_one_head(j->q, j->k_cache, j->v_cache, j->seq_lens, j->out,
-                        j->Hq, j->Hkv, j->D, j->Lmax, j->scale, b, h, s_buf);
+                        j->Hq, j->Hkv, j->D, j->Lmax, j->scale, j->window, b, h, s_buf);
     }
     free(s_buf);
     j->status = 0;
@@ -166,10 +177,10 @@ static void *oracle_worker(void *arg)
 static int oracle_run(const uint16_t *q, const uint16_t *k_cache,
                       const uint16_t *v_cache, const int32_t *seq_lens,
                       double *out, int64_t B, int64_t Hq, int64_t Hkv,
-                      int64_t D, int64_t Lmax, double scale,
+                      int64_t D, int64_t Lmax, double scale, int64_t window,
                       const int64_t *pairs, int64_t nitems, int nthreads)
 {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax < 0 || Hq % Hkv != 0)
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax < 0 || Hq % Hkv != 0 || window < 1)
         return -1;
     for (int64_t b = 0; b < B; ++b)
         if (seq_lens[b] < 0 || seq_lens[b] > Lmax)
@@ -193,7 +204,7 @@ static int oracle_run(const uint16_t *q, const uint16_t *k_cache,
         j->q = q; j->k_cache = k_cache; j->v_cache = v_cache;
         j->seq_lens = seq_lens; j->out = out;
         j->B = B; j->Hq = Hq; j->Hkv = Hkv; j->D = D; j->Lmax = Lmax;
-        j->scale = scale; j->pairs = pairs;
+        j->scale = scale; j->window = window; j->pairs = pairs;
         j->first = nitems * t / nthreads;
         j->last = nitems * (t + 1) / nthreads;
         j->status = -3;
@@ -226,7 +237,19 @@ int oracle_gqa_decode(const uint16_t *q, const uint16_t *k_cache,
                       int64_t D, int64_t Lmax, double scale, int nthreads)
 {
     return oracle_run(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, D, Lmax,
-                      scale, NULL, B * Hq, nthreads);
+                      scale, Lmax > 0 ? Lmax : 1, NULL, B * Hq, nthreads);
+}
+
+/* As oracle_gqa_decode, attending only the last `window` positions of each
+ * sequence (window >= 1). */
+int oracle_gqa_decode_window(const uint16_t *q, const uint16_t *k_cache,
+                             const uint16_t *v_cache, const int32_t *seq_lens,
+                             double *out, int64_t B, int64_t Hq, int64_t Hkv,
+                             int64_t D, int64_t Lmax, double scale, int64_t window,
+                             int nthreads)
+{
+    return oracle_run(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, D, Lmax,
+                      scale, window, NULL, B * Hq, nthreads);
 }
 
 /* Only the listed (b, h) rows: pairs is [npairs, 2] int64; out is still the
@@ -238,5 +261,5 @@ int oracle_gqa_decode_pairs(const uint16_t *q, const uint16_t *k_cache,
                             const int64_t *pairs, int64_t npairs, int nthreads)
 {
     return oracle_run(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, D, Lmax,
-                      scale, pairs, npairs, nthreads);
+                      scale, Lmax > 0 ? Lmax : 1, pairs, npairs, nthreads);
 }

@@ -65,20 +65,39 @@ def pins_pass(orc) -> bool:
         orc.kv_append(kc, vc, kn, vn, pos)
     except ValueError:
         return False
-    return np.array_equal(kc, kr) and np.array_equal(vc, vr)
+    if not (np.array_equal(kc, kr) and np.array_equal(vc, vr)):
+        return False
+    # a window of W positions: the full attention over a cache that holds
+    # only those W rows (checked with torch's attention on the rows)
+    for W in (1, 5, 23):
+        try:
+            ow = orc.gqa_decode(q, k, v, lens, scale=scale, window=W)
+        except ValueError:
+            return False
+        for b in range(B):
+            n = int(lens[b])
+            j0 = max(0, n - W)
+            ref = F.scaled_dot_product_attention(
+                torch.from_numpy(_unbits(q[b:b + 1]))[:, :, None, :],
+                torch.from_numpy(_unbits(k[b:b + 1, :, j0:n])),
+                torch.from_numpy(_unbits(v[b:b + 1, :, j0:n])),
+                scale=scale, enable_gqa=True)[0, :, 0].numpy()
+            if not np.allclose(ow[b], ref, rtol=1e-12, atol=1e-13):
+                return False
+    return True
 
 
 MUTANTS = {
     "interleaved head mapping": ("const int64_t kvh = h / G;",
                                  "const int64_t kvh = h % Hkv;"),
-    "dropped scale": ("s_buf[j] = scale * dot;", "s_buf[j] = dot;"),
+    "dropped scale": ("s_buf[j - j0] = scale * dot;", "s_buf[j - j0] = dot;"),
     "normaliser without max shift": ("denom += exp(s_buf[j] - m);",
                                      "denom += exp(s_buf[j]);"),
     "flipped sign in weights": ("double p = exp(s_buf[j] - m) / denom;",
                                 "double p = exp(m - s_buf[j]) / denom;"),
     "keys and values swapped": (
-        "oracle_bf16_to_double(V[j * D + d]);",
-        "oracle_bf16_to_double(K[j * D + d]);"),
+        "oracle_bf16_to_double(V[(j0 + j) * D + d]);",
+        "oracle_bf16_to_double(K[(j0 + j) * D + d]);"),
     "wrong query row": ("const uint16_t *qh = q + (b * Hq + h) * D;",
                         "const uint16_t *qh = q + (b * Hq + kvh) * D;"),
     "reads one row past the length": (
@@ -88,6 +107,12 @@ MUTANTS = {
                             "int64_t pos = seq_lens[b] + (seq_lens[b] + 1 < Lmax);"),
     "append swaps k and v": ("v_cache[dst] = v_new[src];",
                              "v_cache[dst] = k_new[src];"),
+    "window one position short": ("const int64_t j0 = len > window ? len - window : 0;",
+                                  "const int64_t j0 = len > window ? len - window + 1 : 0;"),
+    "window one position long": ("const int64_t j0 = len > window ? len - window : 0;",
+                                 "const int64_t j0 = len > window ? len - window - 1 : 0;"),
+    "window values not shifted": ("oracle_bf16_to_double(V[(j0 + j) * D + d]);",
+                                  "oracle_bf16_to_double(V[j * D + d]);"),
 }
 
 

@@ -340,3 +340,62 @@ def test_kv_append_rejects_rows_outside_the_cache(bad):
     with pytest.raises(ValueError):
         oracle.kv_append(k, v, kn, kn, np.array([3, bad], np.int32))
     assert np.array_equal(k, before)
+
+
+# ------------------------------------------------------- local (window) layers
+# "The Basics of Transformer Inference", item on mixing in local attention
+# layers: a local layer attends only the last W positions.
+
+def test_window_covering_the_sequence_is_the_full_attention():
+    rng = np.random.default_rng(60)
+    q, k, v, lens = rand_case(rng, 3, 8, 2, 16, 40, lens=[40, 13, 1])
+    full = oracle.gqa_decode(q, k, v, lens, 0.25)
+    for W in (40, 41, 1000):
+        assert np.array_equal(oracle.gqa_decode(q, k, v, lens, 0.25, window=W), full)
+
+
+def test_window_of_one_returns_the_last_value_row_exactly():
+    rng = np.random.default_rng(61)
+    q, k, v, lens = rand_case(rng, 2, 4, 1, 8, 30, lens=[30, 7])
+    out = oracle.gqa_decode(q, k, v, lens, 0.5, window=1)
+    for b in range(2):
+        assert np.array_equal(out[b], unbits(v[b, 0, lens[b] - 1])[None].repeat(4, 0))
+
+
+@pytest.mark.parametrize("W", [2, 7, 16, 29])
+def test_window_equals_full_attention_on_the_window_rows(W):
+    # the same rows copied to the front of a fresh cache, attended in full
+    rng = np.random.default_rng(62 + W)
+    q, k, v, lens = rand_case(rng, 3, 6, 3, 8, 32, lens=[32, 20, 9])
+    out = oracle.gqa_decode(q, k, v, lens, 0.3, window=W)
+    for b in range(3):
+        n = int(lens[b]); j0 = max(0, n - W)
+        ks = np.zeros_like(k[b:b + 1]); vs = np.zeros_like(v[b:b + 1])
+        ks[:, :, :n - j0] = k[b:b + 1, :, j0:n]
+        vs[:, :, :n - j0] = v[b:b + 1, :, j0:n]
+        ref = oracle.gqa_decode(q[b:b + 1], ks, vs, np.array([n - j0], np.int32), 0.3)
+        assert np.array_equal(out[b:b + 1], ref)
+
+
+def test_window_matches_torch_sdpa_with_a_band_mask():
+    rng = np.random.default_rng(63)
+    B, Hq, Hkv, D, L, W = 2, 8, 2, 16, 48, 10
+    q, k, v, lens = rand_case(rng, B, Hq, Hkv, D, L, lens=[48, 25])
+    out = oracle.gqa_decode(q, k, v, lens, 0.2, window=W)
+    for b in range(B):
+        n = int(lens[b])
+        mask = torch.zeros(1, 1, 1, n, dtype=torch.bool)
+        mask[..., max(0, n - W):] = True
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(unbits(q[b:b + 1]))[:, :, None, :],
+            torch.from_numpy(unbits(k[b:b + 1, :, :n])),
+            torch.from_numpy(unbits(v[b:b + 1, :, :n])),
+            attn_mask=mask, scale=0.2, enable_gqa=True)[0, :, 0].numpy()
+        np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_window_must_be_positive():
+    rng = np.random.default_rng(64)
+    q, k, v, lens = rand_case(rng, 1, 2, 1, 8, 8, lens=[5])
+    with pytest.raises(ValueError):
+        oracle.gqa_decode(q, k, v, lens, 0.5, window=0)
