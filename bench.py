@@ -195,12 +195,12 @@ def oracle_sample(w, seed, target_s, max_seqs=None):
         x = wl.make_inputs(sub, seed=seed, device="cpu", lens=lens_all[:nb])
         q, k, v = (wl.bf16_bits(x[n]) for n in ("q", "k_cache", "v_cache"))
         lens = x["attn_lens"].numpy()
-        return q, k, v, lens, accounting.kv_bytes_read(lens, w.Hkv, w.D)
+        return q, k, v, lens, accounting.kv_bytes_read(lens, w.Hkv, w.D, window=w.window)
 
     def once(x):
         q, k, v, lens, _ = x
         t = time.perf_counter()
-        oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads)
+        oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
         return time.perf_counter() - t
 
     x1 = inputs(1)
@@ -237,7 +237,7 @@ def reference_arm(a, w):
         "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B_sampled": nb, "B": w.B, "Hq": w.Hq,
-                   "Hkv": w.Hkv, "D": w.D, "Lmax": w.Lmax},
+                   "Hkv": w.Hkv, "D": w.D, "Lmax": w.Lmax, "window": w.window},
         "seq_steps_per_s": nb * len(times) / tot,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": "%d of %d sequences (all heads) per step; %s" %
@@ -267,8 +267,9 @@ def _oracle_fixed(w, seed, nb, threads):
             (x["attn_lens"].numpy(),)
     q, k, v, lens = _FIXED_CACHE[key]
     t = time.perf_counter()
-    oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads)
-    return time.perf_counter() - t, nb, accounting.kv_bytes_read(lens, w.Hkv, w.D), threads
+    oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
+    return (time.perf_counter() - t, nb,
+            accounting.kv_bytes_read(lens, w.Hkv, w.D, window=w.window), threads)
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -289,11 +290,14 @@ def gpu_arm(a, w):
     lib = g.lib()
     peak, peak_kind = measured_peaks()
 
-    # ---- inputs: `ncopies` caches so consecutive steps never hit in L2
+    # ---- inputs: `ncopies` caches so consecutive steps never hit in L2 (the
+    # steps of one round read at least 4x L2 between them)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     cache_bytes = 2 * w.B * w.Hkv * w.Lmax * w.D * 2
-    ncopies = max(1, int(math.ceil(4 * l2 / cache_bytes)))
+    read_bytes = accounting.kv_bytes_read(wl.attn_lens(w, a.seed + 1000 * rank).tolist(),
+                                          w.Hkv, w.D, window=w.window)
+    ncopies = max(1, int(math.ceil(4 * l2 / read_bytes)))
     ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
     x = wl.make_inputs(w, seed=a.seed + 1000 * rank, device=dev)
     caches = [(x["k_cache"], x["v_cache"])]
@@ -302,7 +306,7 @@ def gpu_arm(a, w):
     lens = x["attn_lens"]
     pos = x["append_pos"]
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
-    kv_bytes = accounting.kv_bytes_read(lens.cpu().tolist(), w.Hkv, w.D)
+    kv_bytes = accounting.kv_bytes_read(lens.cpu().tolist(), w.Hkv, w.D, window=w.window)
 
     stream = torch.cuda.Stream(device=dev)
     sp = ctypes_void(stream.cuda_stream)
@@ -311,8 +315,13 @@ def gpu_arm(a, w):
 
     def call_step(r):
         # one decode step: append this token's K/V and attend (fused kernel)
-        rc = lib.gqa_decode_step(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]), pos_p,
-                                 out_p, w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+        if w.window is None:
+            rc = lib.gqa_decode_step(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]), pos_p,
+                                     out_p, w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+        else:
+            rc = lib.gqa_decode_step_window(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]),
+                                            pos_p, out_p, w.B, w.Hq, w.Hkv, w.D, w.Lmax,
+                                            float(w.scale), int(w.window), sp)
         assert rc == 0, lib.kvattn_last_error()
 
     with torch.cuda.stream(stream):
@@ -392,7 +401,7 @@ def gpu_arm(a, w):
         dvn.copy_(hvn, non_blocking=True)
         dpos.copy_(hpos, non_blocking=True)
         g.gqa_decode_step(dq, dkn, dvn, caches[r][0], caches[r][1], dpos, w.scale, out=out,
-                          stream=stream)
+                          stream=stream, window=w.window)
         hout.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -417,7 +426,7 @@ def gpu_arm(a, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                   "Lmax": w.Lmax, "seq_len": int(lens.max().item()),
+                   "Lmax": w.Lmax, "window": w.window, "seq_len": int(lens.max().item()),
                    "kv_bytes_per_step": kv_bytes,
                    "l2": "inputs larger than L2: %d rotating cache copies, %.0f MB (%.1fx L2)"
                          % (ncopies, ncopies * cache_bytes / 1e6, ncopies * cache_bytes / l2),

@@ -59,6 +59,10 @@ _SIGS = {
                              ctypes.c_float, _VP]),
     "gqa_decode_step": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                              ctypes.c_float, _VP]),
+    "gqa_decode_attn_window": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
+                                    ctypes.c_float, _I, _VP]),
+    "gqa_decode_step_window": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
+                                    ctypes.c_float, _I, _VP]),
     "gqa_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                      ctypes.c_float, _VP]),
     "kvattn_status_string": (ctypes.c_char_p, [_I]),
@@ -150,12 +154,15 @@ def kv_append(k_cache, v_cache, k_new, v_new, seq_lens, stream=None):
                            _ptr(seq_lens), B, Hkv, D, Lmax, _stream_ptr(stream)))
 
 
-def gqa_decode_attn(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None):
+def gqa_decode_attn(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None,
+                    window=None):
     """out[b,h] = softmax(scale * q[b,h] . K[b,h//G]^T) . V[b,h//G] over the
-    first seq_lens[b] cached positions.
+    first seq_lens[b] cached positions (only the last `window` of them for a
+    local attention layer).
 
     q: bf16 [B, Hq, D]; caches: bf16 [B, Hkv, Lmax, D]; seq_lens: int32 [B];
-    out: optional fp32 [B, Hq, D] (allocated if None).  Returns out.
+    out: optional fp32 [B, Hq, D] (allocated if None); window: None (all
+    positions) or an int >= 1.  Returns out.
     """
     import torch
     _need(q, "q", torch.bfloat16)
@@ -171,16 +178,22 @@ def gqa_decode_attn(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None)
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32, (B, Hq, D))
-    _check(lib().gqa_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
-                                 _ptr(out), B, Hq, Hkv, D, Lmax, float(scale),
-                                 _stream_ptr(stream)))
+    if window is None:
+        _check(lib().gqa_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                     _ptr(out), B, Hq, Hkv, D, Lmax, float(scale),
+                                     _stream_ptr(stream)))
+    else:
+        _check(lib().gqa_decode_attn_window(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, Lmax,
+                                            float(scale), int(window), _stream_ptr(stream)))
     return out
 
 
 def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out=None,
-                    stream=None):
+                    stream=None, window=None):
     """One fused decode step: write k_new/v_new into row seq_lens[b] of the
-    caches, then attend over positions [0, seq_lens[b] + 1).
+    caches, then attend over positions [0, seq_lens[b] + 1) (only the last
+    `window` of them for a local attention layer).
 
     q: bf16 [B, Hq, D]; k_new, v_new: bf16 [B, Hkv, D]; caches: bf16
     [B, Hkv, Lmax, D] (modified in place); seq_lens: int32 [B], tokens cached
@@ -202,9 +215,15 @@ def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out=None
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32, (B, Hq, D))
-    _check(lib().gqa_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
-                                 _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D,
-                                 Lmax, float(scale), _stream_ptr(stream)))
+    if window is None:
+        _check(lib().gqa_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D,
+                                     Lmax, float(scale), _stream_ptr(stream)))
+    else:
+        _check(lib().gqa_decode_step_window(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
+                                            Hkv, D, Lmax, float(scale), int(window),
+                                            _stream_ptr(stream)))
     return out
 
 

@@ -26,14 +26,21 @@ def kv_cache_bytes(layers: int, kv_heads: int, head_dim: int, elem_bytes: int,
     return kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes) * batch * tokens
 
 
-def kv_bytes_read(attn_lens, Hkv: int, D: int, elem_bytes: int = 2) -> int:
+def attended_positions(attn_lens, window=None) -> int:
+    """Positions attended over the batch: each sequence's length, capped at
+    the window for a local attention layer ("The Basics of Transformer
+    Inference", item on mixing in local attention layers)."""
+    if window is None:
+        return int(sum(int(x) for x in attn_lens))
+    return int(sum(min(int(x), int(window)) for x in attn_lens))
+
+
+def kv_bytes_read(attn_lens, Hkv: int, D: int, elem_bytes: int = 2, window=None) -> int:
     """Algorithmic K+V bytes one decode-attention call reads (one layer)."""
-    total = int(sum(int(x) for x in attn_lens))
-    return total * Hkv * D * 2 * elem_bytes
+    return attended_positions(attn_lens, window) * Hkv * D * 2 * elem_bytes
 
 
-def attn_flops(attn_lens, Hq: int, D: int) -> int:
+def attn_flops(attn_lens, Hq: int, D: int, window=None) -> int:
     """Algorithmic FLOPs of one call: 2*D for q.k plus 2*D for p*v per query
     head and position."""
-    total = int(sum(int(x) for x in attn_lens))
-    return 4 * Hq * D * total
+    return 4 * Hq * D * attended_positions(attn_lens, window)

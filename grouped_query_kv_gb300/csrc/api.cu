@@ -344,7 +344,8 @@ namespace {
 // append this step's rows first; seq_lens then count tokens cached before).
 int run_decode(const void *q, const void *k_cache, const void *v_cache, const void *k_new,
                const void *v_new, const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
-               int D, int Lmax, float scale, kvattn_stream_t stream_, const char *who) {
+               int D, int Lmax, float scale, int window, kvattn_stream_t stream_,
+               const char *who) {
     t_last_error[0] = 0;
     const bool fused = k_new != nullptr || v_new != nullptr;
     if (!q || !k_cache || !v_cache || !seq_lens || !out || (fused && (!k_new || !v_new)))
@@ -355,6 +356,8 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         return fail(KVATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", who);
     if (!std::isfinite(scale))
         return fail(KVATTN_ERR_INVALID_ARG, "%s: scale must be finite", who);
+    if (window < 1)
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: window must be >= 1 (got %d)", who, window);
     int rc = check_sizes(B, Hq, Hkv, D, Lmax);
     if (rc) return rc;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -397,6 +400,7 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     p.head_groups = P.head_groups;
     p.tile = P.tile_positions;
     p.cost_piece = pl.cost_piece;
+    p.window = window < Lmax ? window : Lmax;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaError_t e;
@@ -425,7 +429,14 @@ int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
                     const int32_t *seq_lens, float *out, int B, int Hq, int Hkv, int D, int Lmax,
                     float scale, kvattn_stream_t stream) {
     return run_decode(q, k_cache, v_cache, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, Lmax,
-                      scale, stream, "gqa_decode_attn");
+                      scale, Lmax, stream, "gqa_decode_attn");
+}
+
+int gqa_decode_attn_window(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *seq_lens, float *out, int B, int Hq, int Hkv, int D,
+                           int Lmax, float scale, int window, kvattn_stream_t stream) {
+    return run_decode(q, k_cache, v_cache, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, Lmax,
+                      scale, window, stream, "gqa_decode_attn_window");
 }
 
 int gqa_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
@@ -436,7 +447,19 @@ int gqa_decode_step(const void *q, const void *k_new, const void *v_new, void *k
         return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_step: null pointer");
     }
     return run_decode(q, k_cache, v_cache, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, Lmax,
-                      scale, stream, "gqa_decode_step");
+                      scale, Lmax, stream, "gqa_decode_step");
+}
+
+int gqa_decode_step_window(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                           void *v_cache, const int32_t *seq_lens, float *out, int B, int Hq,
+                           int Hkv, int D, int Lmax, float scale, int window,
+                           kvattn_stream_t stream) {
+    if (!k_new || !v_new) {
+        t_last_error[0] = 0;
+        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_step_window: null pointer");
+    }
+    return run_decode(q, k_cache, v_cache, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, Lmax,
+                      scale, window, stream, "gqa_decode_step_window");
 }
 
 int kvattn_check_device_error(kvattn_stream_t stream) {

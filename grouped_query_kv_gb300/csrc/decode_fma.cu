@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmv);
     }
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
-    const LenView lens{p.seq_lens, p.len_add};
+    const LenView lens{p.seq_lens, p.len_add, p.window};
     const SchedCost wcost{p.cost_piece};
     const SchedStart st = warp_locate(lens, p.B, p.Lmax, T, segs_per_b, wcost, blockIdx.x, gridDim.x);
     if (warp == 0) sched_split_record(lens, p.B, p.Lmax, T, segs_per_b, wcost, blockIdx.x, st, p.split);
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int kvh = it.seg / p.head_groups;
             const int z = it.b * p.Hkv + kvh;
-            const int y = it.t * T;
+            const int y = it.first_pos();
             // fused append: this tile holds the new token's row
             if (p.len_add && it.last_tile_of_segment() && it.len >= 1 && it.len <= p.Lmax)
                 append_row_warp(p, z, it.len - 1, D, lane);
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool timed_out = !mbar_wait(&full[s], par);
             const uint8_t *kt = smem + s * S::stage_bytes;
             const uint8_t *vt = kt + C::TILE_BYTES;
-            const int pos0 = it.t * T;
+            const int pos0 = it.first_pos();
             const int nvalid = max(0, min(T, len - pos0));
 
             // ---- 1. scores, one position per TPP threads

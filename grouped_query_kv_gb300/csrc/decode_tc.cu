@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
     // each warp locates the CTA's tile range by itself: no block barrier
     // stands between reading the lengths and the first TMA load
-    const LenView lens{p.seq_lens, p.len_add};
+    const LenView lens{p.seq_lens, p.len_add, p.window};
     const SchedCost wcost{p.cost_piece};
     const SchedStart st = warp_locate(lens, p.B, p.Lmax, kT, segs_per_b, wcost, blockIdx.x, gridDim.x);
     // (a softmax warp writes the record: the producer goes straight to its loads)
@@ -508,9 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bs.s_empty[sb]);
 
             // rows of the box before this tile's first new position repeat
-            // positions already attended (or are zeros before row 0)
+            // positions already attended, lie before a local layer's window,
+            // or are zeros before row 0
             const int r0 = it.row0();
-            const bool valid = row >= it.t * kT - r0 && r0 + row < len;
+            const bool valid = row >= it.first_pos() - r0 && r0 + row < len;
             bool over = false;
 #pragma unroll
             for (int g = 0; g < NP; g += 4) {

@@ -41,6 +41,7 @@ struct DecodeParams {
     int heads_per_seg;        // query heads one segment serves
     int head_groups;          // ceil(G / heads_per_seg)
     int tile;                 // positions per tile
+    int window;               // positions attended at most (>= Lmax: all)
     int cost_piece;           // schedule cost of starting and finishing a piece, in
                               // units where a tile costs 32
     float scale_log2;         // scale * log2(e)

@@ -23,10 +23,14 @@ namespace kvattn {
 
 // Lengths as the kernels see them.  For the fused append-then-attend step the
 // array holds the number of tokens cached BEFORE this step's token, and the
-// attention covers one more position; a negative entry stays invalid.
+// attention covers one more position; a negative entry stays invalid.  A
+// local (sliding-window) layer attends only the last `window` positions
+// ("The Basics of Transformer Inference", item on mixing in local attention
+// layers); window >= Lmax is the full attention.
 struct LenView {
     const int32_t *p;
-    int add;  // 0: attention lengths as given; 1: cached-before counts (+1)
+    int add;     // 0: attention lengths as given; 1: cached-before counts (+1)
+    int window;  // positions attended at most, >= 1
     __device__ __forceinline__ int operator[](int b) const {
         const int r = p[b];
         return add ? (r < 0 ? -1 : r + 1) : r;
@@ -35,14 +39,20 @@ struct LenView {
 
 // A sequence whose length is outside [1, Lmax] still owns one tile, with no
 // valid positions (zero output row; out-of-range lengths also raise the
-// device error word).
-__device__ __forceinline__ int seq_ntiles(int len, int Lmax, int tile) {
+// device error word).  Otherwise its tiles cover the min(len, window)
+// attended positions.
+__device__ __forceinline__ int seq_ntiles(int len, int Lmax, int tile, int window) {
     // tiles are a power of two positions (64 or 128): a shift, not a division
-    return (len <= 0 || len > Lmax) ? 1 : (len + tile - 1) >> (__ffs(tile) - 1);
+    return (len <= 0 || len > Lmax) ? 1 : ((len < window ? len : window) + tile - 1) >> (__ffs(tile) - 1);
 }
 
 __device__ __forceinline__ int seq_valid_len(int len, int Lmax) {
     return (len < 0 || len > Lmax) ? 0 : len;
+}
+
+// First attended position of a sequence of (valid) length len.
+__device__ __forceinline__ int seq_window_start(int len, int window) {
+    return len > window ? len - window : 0;
 }
 
 // The cost model's weights: W = kCostTile per tile (a power of two, so the
@@ -139,7 +149,7 @@ __device__ inline void sched_find(LenView lens, int B, int Lmax, int tile, int s
     int tcarry = 0;  // tiles of one segment of every sequence so far
     for (int base = 0; base < B && !(got0 && got1); base += 32) {
         const int b = base + lane;
-        const int nt = (b < B) ? seq_ntiles(lens[b], Lmax, tile) : 0;
+        const int nt = (b < B) ? seq_ntiles(lens[b], Lmax, tile, lens.window) : 0;
         const int incl = warp_incl_scan(nt);
         const int before = tcarry + incl - nt;
         const int segc = nt * kCostTile + w.P;  // one segment of sequence b
@@ -173,7 +183,7 @@ __device__ inline void sched_totals(LenView lens, int B, int Lmax, int tile, int
                                     int *ctas_eff) {
     const int lane = threadIdx.x & 31;
     int nt_lane = 0;
-    for (int b = lane; b < B; b += 32) nt_lane += seq_ntiles(lens[b], Lmax, tile);
+    for (int b = lane; b < B; b += 32) nt_lane += seq_ntiles(lens[b], Lmax, tile, lens.window);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nt_lane += __shfl_xor_sync(0xffffffffu, nt_lane, o);
     const long long nt_sum = nt_lane;  // tiles of one segment of every sequence
@@ -244,7 +254,7 @@ __device__ inline void sched_split_record(LenView lens, int B, int Lmax, int til
         if (st.cost0 >= Tp) {
             SchedHit hp, unused;
             sched_find<1>(lens, B, Lmax, tile, segs_per_b, w, Tp, Tp, st.total, &hp, &unused);
-            const int nt = seq_ntiles(lens[st.b], Lmax, tile);
+            const int nt = seq_ntiles(lens[st.b], Lmax, tile, lens.window);
             const long long last_cost = st.cost0 + (nt == 1 ? 0 : w.P + (long long)kCostTile * (nt - 1));
             const int c_last = sched_owner(last_cost, st.cost, st.ctas_eff);
             r0 = st.b;
@@ -288,14 +298,21 @@ struct TileIter {
         lens = lens_; B = B_; Lmax = Lmax_; tile = tile_; segs_per_b = segs_per_b_;
         b = s.b; seg = s.seg; t = s.t;
         len = lens[b];
-        nt = seq_ntiles(len, Lmax, tile);
+        nt = seq_ntiles(len, Lmax, tile, lens.window);
     }
     __device__ __forceinline__ bool last_tile_of_segment() const { return t == nt - 1; }
+    // First attended position of the current sequence, and the first
+    // position that tile t adds.
+    __device__ __forceinline__ int start() const {
+        return seq_window_start(seq_valid_len(len, Lmax), lens.window);
+    }
+    __device__ __forceinline__ int first_pos() const { return start() + t * tile; }
     // First cache row of the tile's box.  A segment's last tile is moved back
-    // to end exactly at the length (rows before 0 read as zeros), so no tile
-    // ever covers rows past the length: padding is never loaded.
+    // to end exactly at the length (rows before 0 read as zeros; rows before
+    // the tile's first new position are masked), so no tile ever covers rows
+    // past the length: padding is never loaded.
     __device__ __forceinline__ int row0() const {
-        return (t == nt - 1) ? seq_valid_len(len, Lmax) - tile : t * tile;
+        return (t == nt - 1) ? seq_valid_len(len, Lmax) - tile : first_pos();
     }
     __device__ __forceinline__ void next() {
         if (++t < nt) return;
@@ -304,7 +321,7 @@ struct TileIter {
         seg = 0;
         if (++b < B) {
             len = lens[b];
-            nt = seq_ntiles(len, Lmax, tile);
+            nt = seq_ntiles(len, Lmax, tile, lens.window);
         }
     }
 };

@@ -40,6 +40,9 @@ class Workload:
     lens: Optional[tuple] = None
     ragged: bool = False
     k_scale: float = 1.0
+    # a local (sliding-window) attention layer: attend the last `window`
+    # positions only; None is the full attention
+    window: Optional[int] = None
     note: str = ""
 
     @property
@@ -72,6 +75,10 @@ WORKLOADS = {w.name: w for w in [
     Workload("palm540b_long_mqa", B=8, Hq=48, Hkv=1, D=256, Lmax=32768,
              scale=1.0 / 16.0, lens=(32768,), k_scale=0.5,
              note="PaLM-540B-shaped long-context MQA decode, k scaled by 0.5"),
+    Workload("local_gqa_w4096", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
+             scale=1.0 / math.sqrt(128), lens=(8192,), window=4096,
+             note="Llama-70B-shaped GQA decode through a local attention layer: "
+                  "8192-token caches, the last 4096 positions attended"),
 ] + _sweep()}
 
 # the five configurations in the order the benchmark suite lists them

@@ -147,6 +147,30 @@ KVATTN_API int gqa_decode_step(const void *q, const void *k_new, const void *v_n
                                float scale, kvattn_stream_t stream);
 
 /*
+ * gqa_decode_attn_window, gqa_decode_step_window -- the same two calls for a
+ * local (sliding-window) attention layer: the query at position len_b - 1
+ * attends only positions [max(0, len_b - window), len_b), the token itself
+ * included ("The Basics of Transformer Inference", item on mixing in local
+ * attention layers: a local layer caps how far back a token attends).
+ *
+ * Arguments, layouts, ownership and errors are those of gqa_decode_attn and
+ * gqa_decode_step, plus
+ *   window : positions attended at most, >= 1 (KVATTN_ERR_INVALID_ARG
+ *            otherwise); window >= Lmax is the full attention.
+ * Only the attended rows are read from HBM.  Cache rows in [0, len_b) must
+ * hold finite values (the last tile may load rows just before the window,
+ * which are then masked); rows at and past len_b may hold anything.
+ */
+KVATTN_API int gqa_decode_attn_window(const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *seq_lens, float *out, int B, int Hq,
+                                      int Hkv, int D, int Lmax, float scale, int window,
+                                      kvattn_stream_t stream);
+KVATTN_API int gqa_decode_step_window(const void *q, const void *k_new, const void *v_new,
+                                      void *k_cache, void *v_cache, const int32_t *seq_lens,
+                                      float *out, int B, int Hq, int Hkv, int D, int Lmax,
+                                      float scale, int window, kvattn_stream_t stream);
+
+/*
  * gqa_decode_attn_noalloc -- the same computation as gqa_decode_attn, for
  * callers that must not have the library allocate device memory (for
  * example a server that gives all free GPU memory to its own pool at

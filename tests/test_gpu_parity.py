@@ -345,3 +345,88 @@ def test_fused_step_flags_rows_outside_the_cache():
     ref = oracle.gqa_decode(bits(x["q"])[1:2], after[1:2], bits(x["v_cache"])[1:2],
                             np.array([4], np.int32), w.scale)
     assert_close(out[1:2], ref, bits(x["v_cache"])[1:2], [4])
+
+
+# ------------------------------------------------------- local (window) layers
+# "The Basics of Transformer Inference", item on mixing in local attention
+# layers: the query attends only the last `window` positions.
+
+def _window_case(w, seed, window, nan_pad=True):
+    dev = torch.device("cuda")
+    x = wl.make_inputs(w, seed=seed, device=dev)
+    if nan_pad:
+        for b, n in enumerate(x["attn_lens"].tolist()):
+            x["k_cache"][b, :, n:] = float("nan")
+            x["v_cache"][b, :, n:] = float("inf")
+    out = g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale,
+                            window=window)
+    g.check_device_error()
+    lens_np = x["attn_lens"].cpu().numpy()
+    ref = oracle.gqa_decode(bits(x["q"]), bits(x["k_cache"]), bits(x["v_cache"]), lens_np,
+                            w.scale, nthreads=oracle_threads(), window=window)
+    assert_close(out, ref, bits(x["v_cache"]), lens_np)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 16, 2), (256, 48, 1), (128, 8, 8)])
+@pytest.mark.parametrize("window", [1, 5, 127, 128, 129, 300, 5000])
+def test_local_window_attention(path, D, Hq, Hkv, window):
+    lens = (700, 1, 129, 256, 1000, 383, 128, 4)
+    w = wl.Workload("win", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, Lmax=1000,
+                    scale=1.0 / np.sqrt(D), lens=lens)
+    g.set_tuning(path, 0)
+    try:
+        _window_case(w, seed=window + D + path, window=window)
+    finally:
+        g.set_tuning(0, 0)
+
+
+def test_local_window_on_the_cuda_core_path_at_d64():
+    w = wl.Workload("win64", B=4, Hq=8, Hkv=2, D=64, Lmax=600, scale=0.125,
+                    lens=(600, 77, 1, 300))
+    for window in (1, 63, 64, 65, 200):
+        _window_case(w, seed=window, window=window)
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 152, 400])
+def test_local_window_with_split_pieces(ctas):
+    w = wl.Workload("winsplit", B=3, Hq=48, Hkv=1, D=256, Lmax=5000, scale=1 / 16,
+                    lens=(5000, 130, 2047), k_scale=0.5)
+    g.set_tuning(2, ctas)
+    try:
+        _window_case(w, seed=ctas, window=1500)
+    finally:
+        g.set_tuning(0, 0)
+
+
+@pytest.mark.parametrize("window", [1, 100, 2000])
+def test_local_window_fused_step(window):
+    dev = torch.device("cuda")
+    w = wl.Workload("winstep", B=5, Hq=32, Hkv=4, D=128, Lmax=1500, scale=0.088,
+                    lens=(1500, 1, 640, 129, 1000))
+    x = wl.make_inputs(w, seed=window, device=dev)
+    k_ref, v_ref = bits(x["k_cache"]), bits(x["v_cache"])
+    oracle.kv_append(k_ref, v_ref, bits(x["k_new"]), bits(x["v_new"]),
+                     x["append_pos"].cpu().numpy())
+    out = g.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                            x["append_pos"], w.scale, window=window)
+    g.check_device_error()
+    assert np.array_equal(bits(x["k_cache"]), k_ref)
+    assert np.array_equal(bits(x["v_cache"]), v_ref)
+    lens_np = x["attn_lens"].cpu().numpy()
+    ref = oracle.gqa_decode(bits(x["q"]), k_ref, v_ref, lens_np, w.scale,
+                            nthreads=oracle_threads(), window=window)
+    assert_close(out, ref, v_ref, lens_np)
+
+
+def test_local_window_workload_every_output():
+    w = wl.WORKLOADS["local_gqa_w4096"]
+    _window_case(w, seed=0, window=w.window, nan_pad=False)
+
+
+def test_local_window_must_be_positive():
+    dev = torch.device("cuda")
+    w = wl.WORKLOADS["tiny_mqa"]
+    x = wl.make_inputs(w, seed=0, device=dev)
+    with pytest.raises(g.KvAttnError):
+        g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale, window=0)
