@@ -61,6 +61,10 @@ def _bind(path):
     lib.oracle_gqa_decode_window.argtypes = [u16p, u16p, u16p, i32p, f64p,
                                              i64, i64, i64, i64, i64,
                                              ctypes.c_double, i64, ctypes.c_int]
+    lib.oracle_gqa_decode_multi.restype = ctypes.c_int
+    lib.oracle_gqa_decode_multi.argtypes = [u16p, u16p, u16p, i32p, f64p,
+                                            i64, i64, i64, i64, i64, i64,
+                                            ctypes.c_double, ctypes.c_int]
     lib.oracle_gqa_decode_pairs.restype = ctypes.c_int
     lib.oracle_gqa_decode_pairs.argtypes = [u16p, u16p, u16p, i32p, f64p,
                                             i64, i64, i64, i64, i64,
@@ -183,10 +187,37 @@ class Oracle:
         return out
 
 
+    def gqa_decode_multi(self, q, k_cache, v_cache, seq_lens, scale, nthreads=1):
+        """T new tokens per sequence, causal among themselves.
+
+        q:        uint16 [B, T, Hq, D] (bf16 bits); token t of sequence b sits
+                  at position seq_lens[b] - T + t and attends positions
+                  [0, seq_lens[b] - T + 1 + t) (a zero row when that is empty)
+        k_cache:  uint16 [B, Hkv, Lmax, D];  v_cache the same shape
+        Returns float64 [B, T, Hq, D].
+        """
+        qa, q_p = _u16(q)
+        ka, k_p = _u16(k_cache)
+        va, v_p = _u16(v_cache)
+        sl, sl_p = _i32(seq_lens)
+        B, T, Hq, D = qa.shape
+        Bk, Hkv, Lmax, Dk = ka.shape
+        if Bk != B or Dk != D or va.shape != ka.shape or sl.shape != (B,):
+            raise ValueError("shape mismatch")
+        out = np.zeros((B, T, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_gqa_decode_multi(
+            q_p, k_p, v_p, sl_p, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            B, T, Hq, Hkv, D, Lmax, float(scale), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_gqa_decode_multi: bad arguments (rc=%d)" % rc)
+        return out
+
+
 _default = Oracle()
 bf16_to_double = _default.bf16_to_double
 kv_append = _default.kv_append
 gqa_decode = _default.gqa_decode
+gqa_decode_multi = _default.gqa_decode_multi
 
 
 def _u16(a):

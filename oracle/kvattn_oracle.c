@@ -50,6 +50,15 @@
  *   of W positions (the token itself included; a reading, the pages give no
  *   formula) the sums above run over j = max(0, len_b - W) .. len_b - 1.
  *   W >= len_b is the full attention.
+ *
+ *   Several new tokens per sequence (speculative sampling, "The Basics of
+ *   Transformer Inference": the big model scores a run of drafted tokens in
+ *   one pass, sharing the KV-cache loads among them): the T new tokens sit
+ *   at positions len_b - T .. len_b - 1 and token t (0-based) attends
+ *   positions 0 .. len_b - T + t, i.e. the cached prefix and the new tokens
+ *   up to itself (causal among the new tokens; a reading, the pages give no
+ *   formula).  A token with nothing to attend (len_b - T + t < 0) gets a zero
+ *   row.  q and out are [B, T, Hq, D].
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -93,22 +102,24 @@ int oracle_kv_append(uint16_t *k_cache, uint16_t *v_cache,
  * s_buf must hold len_b doubles. */
 static void oracle_one_head(const uint16_t *q, const uint16_t *k_cache,
                             const uint16_t *v_cache, const int32_t *seq_lens,
-                            double *out, int64_t Hq, int64_t Hkv, int64_t D,
+                            double *out, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
                             int64_t Lmax, double scale, int64_t window,
-                            int64_t b, int64_t h, double *s_buf)
+                            int64_t b, int64_t t, int64_t h, double *s_buf)
 {
     const int64_t G = Hq / Hkv;
     const int64_t kvh = h / G;
-    const int64_t len = seq_lens[b];
+    int64_t len = seq_lens[b] - (T - 1 - t); /* positions this query attends */
+    if (len < 0)
+        len = 0;
     const int64_t j0 = len > window ? len - window : 0; /* first attended position */
-    double *o = out + (b * Hq + h) * D;
+    double *o = out + ((b * T + t) * Hq + h) * D;
 
     for (int64_t d = 0; d < D; ++d)
         o[d] = 0.0;
     if (len == 0)
         return;
 
-    const uint16_t *qh = q + (b * Hq + h) * D;
+    const uint16_t *qh = q + ((b * T + t) * Hq + h) * D;
     const uint16_t *K = k_cache + (b * Hkv + kvh) * Lmax * D;
     const uint16_t *V = v_cache + (b * Hkv + kvh) * Lmax * D;
 
@@ -141,7 +152,7 @@ typedef struct {
     const uint16_t *q, *k_cache, *v_cache;
     const int32_t *seq_lens;
     double *out;
-    int64_t B, Hq, Hkv, D, Lmax;
+    int64_t B, T, Hq, Hkv, D, Lmax;
     double scale;
     int64_t window;
     const int64_t *pairs; /* NULL: all (b,h); else npairs (b,h) pairs */
@@ -158,16 +169,18 @@ static void *oracle_worker(void *arg)
         return NULL;
     }
     for (int64_t w = j->first; w < j->last; ++w) {
-        int64_t b, h;
+        int64_t b, t, h;
         if (j->pairs) {
             b = j->pairs[2 * w];
+            t = 0;
             h = j->pairs[2 * w + 1];
         } else {
-            b = w / j->Hq;
+            b = w / (j->T * j->Hq);
+            t = (w / j->Hq) % j->T;
             h = w % j->Hq;
         }
-        oracle_one_head(j->q, j->k_cache, j->v_cache, j->seq_lens, j->out,
-                        j->Hq, j->Hkv, j->D, j->Lmax, j->scale, j->window, b, h, s_buf);
+        oracle_one_head(j->q, j->k_cache, j->v_cache, j->seq_lens, j->out, j->T,
+                        j->Hq, j->Hkv, j->D, j->Lmax, j->scale, j->window, b, t, h, s_buf);
     }
     free(s_buf);
     j->status = 0;
@@ -176,11 +189,12 @@ static void *oracle_worker(void *arg)
 
 static int oracle_run(const uint16_t *q, const uint16_t *k_cache,
                       const uint16_t *v_cache, const int32_t *seq_lens,
-                      double *out, int64_t B, int64_t Hq, int64_t Hkv,
+                      double *out, int64_t B, int64_t T, int64_t Hq, int64_t Hkv,
                       int64_t D, int64_t Lmax, double scale, int64_t window,
                       const int64_t *pairs, int64_t nitems, int nthreads)
 {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax < 0 || Hq % Hkv != 0 || window < 1)
+    if (B < 0 || T < 1 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax < 0 || Hq % Hkv != 0 ||
+        window < 1 || (pairs && T != 1))
         return -1;
     for (int64_t b = 0; b < B; ++b)
         if (seq_lens[b] < 0 || seq_lens[b] > Lmax)
@@ -203,7 +217,7 @@ static int oracle_run(const uint16_t *q, const uint16_t *k_cache,
         oracle_job *j = &jobs[t];
         j->q = q; j->k_cache = k_cache; j->v_cache = v_cache;
         j->seq_lens = seq_lens; j->out = out;
-        j->B = B; j->Hq = Hq; j->Hkv = Hkv; j->D = D; j->Lmax = Lmax;
+        j->B = B; j->T = T; j->Hq = Hq; j->Hkv = Hkv; j->D = D; j->Lmax = Lmax;
         j->scale = scale; j->window = window; j->pairs = pairs;
         j->first = nitems * t / nthreads;
         j->last = nitems * (t + 1) / nthreads;
@@ -236,8 +250,19 @@ int oracle_gqa_decode(const uint16_t *q, const uint16_t *k_cache,
                       double *out, int64_t B, int64_t Hq, int64_t Hkv,
                       int64_t D, int64_t Lmax, double scale, int nthreads)
 {
-    return oracle_run(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, D, Lmax,
+    return oracle_run(q, k_cache, v_cache, seq_lens, out, B, 1, Hq, Hkv, D, Lmax,
                       scale, Lmax > 0 ? Lmax : 1, NULL, B * Hq, nthreads);
+}
+
+/* T new tokens per sequence: q and out are [B, T, Hq, D]; token t attends
+ * positions [0, seq_lens[b] - T + 1 + t). */
+int oracle_gqa_decode_multi(const uint16_t *q, const uint16_t *k_cache,
+                            const uint16_t *v_cache, const int32_t *seq_lens,
+                            double *out, int64_t B, int64_t T, int64_t Hq, int64_t Hkv,
+                            int64_t D, int64_t Lmax, double scale, int nthreads)
+{
+    return oracle_run(q, k_cache, v_cache, seq_lens, out, B, T, Hq, Hkv, D, Lmax,
+                      scale, Lmax > 0 ? Lmax : 1, NULL, B * T * Hq, nthreads);
 }
 
 /* As oracle_gqa_decode, attending only the last `window` positions of each
@@ -248,7 +273,7 @@ int oracle_gqa_decode_window(const uint16_t *q, const uint16_t *k_cache,
                              int64_t D, int64_t Lmax, double scale, int64_t window,
                              int nthreads)
 {
-    return oracle_run(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, D, Lmax,
+    return oracle_run(q, k_cache, v_cache, seq_lens, out, B, 1, Hq, Hkv, D, Lmax,
                       scale, window, NULL, B * Hq, nthreads);
 }
 
@@ -260,6 +285,6 @@ int oracle_gqa_decode_pairs(const uint16_t *q, const uint16_t *k_cache,
                             int64_t D, int64_t Lmax, double scale,
                             const int64_t *pairs, int64_t npairs, int nthreads)
 {
-    return oracle_run(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, D, Lmax,
+    return oracle_run(q, k_cache, v_cache, seq_lens, out, B, 1, Hq, Hkv, D, Lmax,
                       scale, Lmax > 0 ? Lmax : 1, pairs, npairs, nthreads);
 }

@@ -84,6 +84,25 @@ def pins_pass(orc) -> bool:
                 scale=scale, enable_gqa=True)[0, :, 0].numpy()
             if not np.allclose(ow[b], ref, rtol=1e-12, atol=1e-13):
                 return False
+    # T new tokens: token t is a single-token decode over len - T + 1 + t
+    # positions (torch's attention on those rows)
+    T = 3
+    qm = _bits(rng.standard_normal((B, T, Hq, D)))
+    lm = np.array([24, 7, 3], np.int32)
+    try:
+        om = orc.gqa_decode_multi(qm, k, v, lm, scale=scale)
+    except ValueError:
+        return False
+    for b in range(B):
+        for t in range(T):
+            n = int(lm[b]) - T + 1 + t
+            ref = F.scaled_dot_product_attention(
+                torch.from_numpy(_unbits(qm[b:b + 1, t]))[:, :, None, :],
+                torch.from_numpy(_unbits(k[b:b + 1, :, :n])),
+                torch.from_numpy(_unbits(v[b:b + 1, :, :n])),
+                scale=scale, enable_gqa=True)[0, :, 0].numpy()
+            if not np.allclose(om[b, t], ref, rtol=1e-12, atol=1e-13):
+                return False
     return True
 
 
@@ -98,11 +117,18 @@ MUTANTS = {
     "keys and values swapped": (
         "oracle_bf16_to_double(V[(j0 + j) * D + d]);",
         "oracle_bf16_to_double(K[(j0 + j) * D + d]);"),
-    "wrong query row": ("const uint16_t *qh = q + (b * Hq + h) * D;",
-                        "const uint16_t *qh = q + (b * Hq + kvh) * D;"),
+    "wrong query row": ("const uint16_t *qh = q + ((b * T + t) * Hq + h) * D;",
+                        "const uint16_t *qh = q + ((b * T + t) * Hq + kvh) * D;"),
     "reads one row past the length": (
-        "const int64_t len = seq_lens[b];",
-        "const int64_t len = seq_lens[b] + (seq_lens[b] < Lmax);"),
+        "int64_t len = seq_lens[b] - (T - 1 - t);",
+        "int64_t len = seq_lens[b] - (T - 1 - t) + (seq_lens[b] < Lmax);"),
+    "new tokens see one position too few": ("int64_t len = seq_lens[b] - (T - 1 - t);",
+                                            "int64_t len = seq_lens[b] - (T - t);"),
+    "new tokens see the whole run": ("int64_t len = seq_lens[b] - (T - 1 - t);",
+                                     "int64_t len = seq_lens[b] - 0 * t;"),
+    "new tokens' queries reversed": (
+        "const uint16_t *qh = q + ((b * T + t) * Hq + h) * D;",
+        "const uint16_t *qh = q + ((b * T + (T - 1 - t)) * Hq + h) * D;"),
     "append one row late": ("int64_t pos = seq_lens[b];",
                             "int64_t pos = seq_lens[b] + (seq_lens[b] + 1 < Lmax);"),
     "append swaps k and v": ("v_cache[dst] = v_new[src];",

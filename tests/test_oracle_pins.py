@@ -399,3 +399,59 @@ def test_window_must_be_positive():
     q, k, v, lens = rand_case(rng, 1, 2, 1, 8, 8, lens=[5])
     with pytest.raises(ValueError):
         oracle.gqa_decode(q, k, v, lens, 0.5, window=0)
+
+
+# ----------------------------------------------- several new tokens (speculative)
+# "The Basics of Transformer Inference", speculative sampling: the T drafted
+# tokens are scored in one pass; token t sits at position len - T + t and
+# attends the prefix and the new tokens up to itself.
+
+def test_one_new_token_is_the_single_token_decode():
+    rng = np.random.default_rng(70)
+    q, k, v, lens = rand_case(rng, 3, 8, 2, 16, 40, lens=[40, 13, 1])
+    out = oracle.gqa_decode_multi(q[:, None], k, v, lens, 0.25)
+    assert np.array_equal(out[:, 0], oracle.gqa_decode(q, k, v, lens, 0.25))
+
+
+@pytest.mark.parametrize("T", [2, 4, 8])
+def test_each_new_token_equals_a_single_decode_over_its_prefix(T):
+    rng = np.random.default_rng(71 + T)
+    B, Hq, Hkv, D, L = 3, 6, 3, 8, 32
+    q = bits(rng.standard_normal((B, T, Hq, D)))
+    _, k, v, _ = rand_case(rng, B, Hq, Hkv, D, L)
+    lens = np.array([32, 20, T], np.int32)
+    out = oracle.gqa_decode_multi(q, k, v, lens, 0.3)
+    for t in range(T):
+        ref = oracle.gqa_decode(np.ascontiguousarray(q[:, t]), k, v, lens - (T - 1 - t), 0.3)
+        assert np.array_equal(out[:, t], ref)
+
+
+def test_new_tokens_match_torch_sdpa_with_a_causal_block_mask():
+    rng = np.random.default_rng(72)
+    B, T, Hq, Hkv, D, L = 2, 4, 8, 2, 16, 30
+    q = bits(rng.standard_normal((B, T, Hq, D)))
+    _, k, v, _ = rand_case(rng, B, Hq, Hkv, D, L)
+    lens = np.array([30, 9], np.int32)
+    out = oracle.gqa_decode_multi(q, k, v, lens, 0.2)
+    for b in range(B):
+        n = int(lens[b])
+        # queries [Hq, T, D] against n positions; token t sees positions < n - T + 1 + t
+        mask = torch.zeros(1, 1, T, n, dtype=torch.bool)
+        for t in range(T):
+            mask[..., t, :n - T + 1 + t] = True
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(unbits(q[b:b + 1])).permute(0, 2, 1, 3),
+            torch.from_numpy(unbits(k[b:b + 1, :, :n])),
+            torch.from_numpy(unbits(v[b:b + 1, :, :n])),
+            attn_mask=mask, scale=0.2, enable_gqa=True)[0].permute(1, 0, 2).numpy()
+        np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_new_tokens_before_the_start_of_the_sequence_get_zero_rows():
+    rng = np.random.default_rng(73)
+    T = 5
+    q = bits(rng.standard_normal((1, T, 2, 8)))
+    _, k, v, _ = rand_case(rng, 1, 2, 1, 8, 10)
+    out = oracle.gqa_decode_multi(q, k, v, np.array([3], np.int32), 0.5)
+    assert np.all(out[0, :2] == 0.0)                 # len - T + 1 + t <= 0
+    assert np.array_equal(out[0, 2], unbits(v[0, 0, 0])[None].repeat(2, 0))  # sees one row
