@@ -200,7 +200,10 @@ def oracle_sample(w, seed, target_s, max_seqs=None):
     def once(x):
         q, k, v, lens, _ = x
         t = time.perf_counter()
-        oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
+        if w.T > 1:
+            oracle.gqa_decode_multi(q, k, v, lens, w.scale, nthreads=threads)
+        else:
+            oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
         return time.perf_counter() - t
 
     x1 = inputs(1)
@@ -267,7 +270,10 @@ def _oracle_fixed(w, seed, nb, threads):
             (x["attn_lens"].numpy(),)
     q, k, v, lens = _FIXED_CACHE[key]
     t = time.perf_counter()
-    oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
+    if w.T > 1:
+        oracle.gqa_decode_multi(q, k, v, lens, w.scale, nthreads=threads)
+    else:
+        oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
     return (time.perf_counter() - t, nb,
             accounting.kv_bytes_read(lens, w.Hkv, w.D, window=w.window), threads)
 
@@ -305,7 +311,7 @@ def gpu_arm(a, w):
         caches.append((x["k_cache"].clone(), x["v_cache"].clone()))
     lens = x["attn_lens"]
     pos = x["append_pos"]
-    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    out = torch.empty(tuple(x["q"].shape), dtype=torch.float32, device=dev)
     kv_bytes = accounting.kv_bytes_read(lens.cpu().tolist(), w.Hkv, w.D, window=w.window)
 
     stream = torch.cuda.Stream(device=dev)
@@ -313,9 +319,15 @@ def gpu_arm(a, w):
     P = lambda t: ctypes_void(t.data_ptr())  # noqa: E731
     q_p, kn_p, vn_p, pos_p, out_p = map(P, (x["q"], x["k_new"], x["v_new"], pos, out))
 
+    lens_p = P(lens)
+
     def call_step(r):
-        # one decode step: append this token's K/V and attend (fused kernel)
-        if w.window is None:
+        # one decode step: append this token's K/V and attend (fused kernel);
+        # for T drafted tokens, their scoring pass over the cache
+        if w.T > 1:
+            rc = lib.gqa_decode_attn_multi(q_p, P(caches[r][0]), P(caches[r][1]), lens_p, out_p,
+                                           w.B, w.T, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+        elif w.window is None:
             rc = lib.gqa_decode_step(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]), pos_p,
                                      out_p, w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
         else:
@@ -390,18 +402,26 @@ def gpu_arm(a, w):
     dq, dkn, dvn = torch.empty_like(x["q"]), torch.empty_like(x["k_new"]), torch.empty_like(x["v_new"])
     dpos = torch.empty_like(pos)
     n_e2e = max(1, a.e2e_steps)
+    hlens = lens.cpu().pin_memory()
+    dlens = torch.empty_like(lens)
     # bytes each e2e step moves, counted from the tensors it copies
-    io = {"h2d": sum(t.numel() * t.element_size() for t in (hq, hkn, hvn, hpos)),
+    inputs_h = (hq, hlens) if w.T > 1 else (hq, hkn, hvn, hpos)
+    io = {"h2d": sum(t.numel() * t.element_size() for t in inputs_h),
           "d2h": hout.numel() * hout.element_size()}
 
     def e2e_step(i):
         r = i % ncopies
         dq.copy_(hq, non_blocking=True)
-        dkn.copy_(hkn, non_blocking=True)
-        dvn.copy_(hvn, non_blocking=True)
-        dpos.copy_(hpos, non_blocking=True)
-        g.gqa_decode_step(dq, dkn, dvn, caches[r][0], caches[r][1], dpos, w.scale, out=out,
-                          stream=stream, window=w.window)
+        if w.T > 1:
+            dlens.copy_(hlens, non_blocking=True)
+            g.gqa_decode_attn_multi(dq, caches[r][0], caches[r][1], dlens, w.scale, out=out,
+                                    stream=stream)
+        else:
+            dkn.copy_(hkn, non_blocking=True)
+            dvn.copy_(hvn, non_blocking=True)
+            dpos.copy_(hpos, non_blocking=True)
+            g.gqa_decode_step(dq, dkn, dvn, caches[r][0], caches[r][1], dpos, w.scale, out=out,
+                              stream=stream, window=w.window)
         hout.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -430,24 +450,32 @@ def gpu_arm(a, w):
                    "kv_bytes_per_step": kv_bytes,
                    "l2": "inputs larger than L2: %d rotating cache copies, %.0f MB (%.1fx L2)"
                          % (ncopies, ncopies * cache_bytes / 1e6, ncopies * cache_bytes / l2),
-                   "step": "gqa_decode_step (kv_append fused into the attention kernel), "
-                           "steps chained in CUDA graphs",
+                   "T": w.T,
+                   "step": ("gqa_decode_attn_multi (T new tokens scored in one pass over the "
+                            "cache, which already holds their rows), steps chained in CUDA graphs"
+                            if w.T > 1 else
+                            "gqa_decode_step (kv_append fused into the attention kernel), "
+                            "steps chained in CUDA graphs"),
                    "numerics": "bf16 in, fp32 accumulate and out",
                    "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
         "seq_steps_per_s": world * w.B * a.steps / (ms_total / 1e3),
+        "tokens_scored_per_s": world * w.B * w.T * a.steps / (ms_total / 1e3),
         "us_per_step": 1e3 * ms_step,
         "hbm_fraction": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": sum(traffic.values()) if traffic else None,
                      "traffic_by_kernel": traffic,
-                     "kernel": "gqa_decode_step (fused append + split-KV kernel + combine), "
+                     "kernel": ("gqa_decode_attn_multi (split-KV kernel + combine), " if w.T > 1
+                                else "gqa_decode_step (fused append + split-KV kernel + combine), ")
+                               +
                                "average over the timed steps",
                      "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind
                      if peak_kind == "measured" else "fallback 6800 GB/s"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
                 "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms,
-                "api": "grouped_query_kv_gb300.gqa_decode_step (eager)"},
+                "api": "grouped_query_kv_gb300.%s (eager)"
+                       % ("gqa_decode_attn_multi" if w.T > 1 else "gqa_decode_step")},
         "gpu_launches": 2 * a.steps,
         "clocks": clk,
     }

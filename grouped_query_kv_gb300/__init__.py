@@ -59,6 +59,8 @@ _SIGS = {
                              ctypes.c_float, _VP]),
     "gqa_decode_step": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                              ctypes.c_float, _VP]),
+    "gqa_decode_attn_multi": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
+                                   ctypes.c_float, _VP]),
     "gqa_decode_attn_window": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                     ctypes.c_float, _I, _VP]),
     "gqa_decode_step_window": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
@@ -224,6 +226,34 @@ def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out=None
                                             _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
                                             Hkv, D, Lmax, float(scale), int(window),
                                             _stream_ptr(stream)))
+    return out
+
+
+def gqa_decode_attn_multi(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None):
+    """Attention for T new tokens per sequence, causal among themselves: token
+    t of sequence b attends positions [0, seq_lens[b] - T + 1 + t).
+
+    q: bf16 [B, T, Hq, D]; caches: bf16 [B, Hkv, Lmax, D] already holding the
+    new tokens' rows; seq_lens: int32 [B], tokens in the cache including the
+    new ones; out: optional fp32 [B, T, Hq, D].  Returns out.
+    """
+    import torch
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, Hq, D]")
+    B, T, Hq, D = q.shape
+    _need(k_cache, "k_cache", torch.bfloat16)
+    if k_cache.dim() != 4 or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError("k_cache must be [B, Hkv, Lmax, D] matching q")
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lmax, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, T, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, (B, T, Hq, D))
+    _check(lib().gqa_decode_attn_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                       _ptr(out), B, T, Hq, Hkv, D, Lmax, float(scale),
+                                       _stream_ptr(stream)))
     return out
 
 

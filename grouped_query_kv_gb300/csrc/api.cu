@@ -122,7 +122,7 @@ struct Plan {
 // tensor pipe absorbs: measured on GB300 it streams at copy bandwidth even
 // at G = 1, where the CUDA-core kernel is instruction-bound); the CUDA-core
 // kernel for D = 64.
-int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
+int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl, int T = 1) {
     (void)Lmax;
     (void)B;
     const int G = Hq / Hkv;
@@ -131,13 +131,27 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
     const bool tc_ok = (D == 128 || D == 256);
     int path = tc_ok ? 2 : 1;
     if (g_force_path == 1) path = 1;
-    if (g_force_path == 2) {
+    if (g_force_path == 2 || T > 1) {
         if (!tc_ok)
             return fail(KVATTN_ERR_UNSUPPORTED, "tensor-core path needs D in {128, 256} (D=%d)", D);
         path = 2;
     }
+    if (T > 1 && g_force_path == 1)
+        return fail(KVATTN_ERR_UNSUPPORTED, "several new tokens need the tensor-core path");
     p.path = path;
-    if (path == 2) {
+    if (T > 1) {
+        // one pass takes the group's heads of all T tokens
+        if (tc_heads_per_seg(G * T, D) != G * T)
+            return fail(KVATTN_ERR_UNSUPPORTED,
+                        "G * T = %d query rows per K/V head exceed one pass (%d at D=%d)", G * T,
+                        tc_heads_per_seg(1 << 20, D), D);
+        pl->heads_per_seg = G * T;
+        pl->np = tc_np(G * T, D);
+        p.tile_positions = tc_tile();
+        p.stages = tc_stages(D, pl->np);
+        p.threads = tc_threads();
+        p.smem_bytes = tc_smem_bytes(D, pl->np);
+    } else if (path == 2) {
         pl->heads_per_seg = tc_heads_per_seg(G, D);
         pl->np = tc_np(G, D);
         p.tile_positions = tc_tile();
@@ -153,7 +167,7 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
         p.smem_bytes = fma_smem_bytes(D, pl->heads_per_seg);
     }
     p.heads_per_cta = pl->heads_per_seg;
-    p.head_groups = (G + pl->heads_per_seg - 1) / pl->heads_per_seg;
+    p.head_groups = T > 1 ? 1 : (G + pl->heads_per_seg - 1) / pl->heads_per_seg;
     // CTA ranges balance cost: a tile costs W and a piece (q load, the first
     // tile's exact max, the output's read-out and stores) costs P more.
     // Measured on GB300 with the tensor-core kernel, a piece takes about
@@ -167,13 +181,16 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl) {
     return KVATTN_OK;
 }
 
-// 2-D map over q viewed as [B*Hq rows, D]: box (64, np), 128-byte swizzle.
-int encode_q_map(CUtensorMap *m, const void *base, int D, int rows, int np) {
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)np};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+// 3-D map over q, 128-byte swizzle.  One token per sequence: q viewed as
+// (D, B*Hq, 1) with box (64, np, 1).  T tokens: q [B, T, Hq, D] viewed as
+// (D, Hq, B*T) with box (64, G, T) -- the group's heads of every token.
+int encode_q_map(CUtensorMap *m, const void *base, int D, int B, int T, int Hq, int G, int np) {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(T == 1 ? B * Hq : Hq),
+                          (cuuint64_t)(T == 1 ? 1 : B * T)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)(T == 1 ? B * Hq : Hq) * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)(T == 1 ? np : G), (cuuint32_t)T};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -345,7 +362,7 @@ namespace {
 int run_decode(const void *q, const void *k_cache, const void *v_cache, const void *k_new,
                const void *v_new, const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
                int D, int Lmax, float scale, int window, kvattn_stream_t stream_,
-               const char *who) {
+               const char *who, int T = 1) {
     t_last_error[0] = 0;
     const bool fused = k_new != nullptr || v_new != nullptr;
     if (!q || !k_cache || !v_cache || !seq_lens || !out || (fused && (!k_new || !v_new)))
@@ -358,6 +375,8 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         return fail(KVATTN_ERR_INVALID_ARG, "%s: scale must be finite", who);
     if (window < 1)
         return fail(KVATTN_ERR_INVALID_ARG, "%s: window must be >= 1 (got %d)", who, window);
+    if (T < 1 || T > 64)
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: T must be in [1, 64] (got %d)", who, T);
     int rc = check_sizes(B, Hq, Hkv, D, Lmax);
     if (rc) return rc;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -371,7 +390,7 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         std::lock_guard<std::mutex> lk(g_mu);
         if ((rc = device_state(dev, &ds))) return rc;
         if ((rc = get_encoder())) return rc;
-        if ((rc = make_plan(B, Hq, Hkv, D, Lmax, ds->num_sms, &pl))) return rc;
+        if ((rc = make_plan(B, Hq, Hkv, D, Lmax, ds->num_sms, &pl, T))) return rc;
         if ((rc = get_workspace(dev, stream, (size_t)pl.pub.workspace_bytes, &ws))) return rc;
     }
     const kvattn_plan &P = pl.pub;
@@ -401,13 +420,16 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     p.tile = P.tile_positions;
     p.cost_piece = pl.cost_piece;
     p.window = window < Lmax ? window : Lmax;
+    p.T = T;
+    // bytes of one piece's q box: (64 columns x rows) per 64-column slab
+    p.q_bytes = (D / 64) * (T == 1 ? pl.np : p.G * T) * 128;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaError_t e;
     if (P.path == 2) {
         CUtensorMap tmq;
-        if ((rc = encode_q_map(&tmq, q, D, B * Hq, pl.np))) return rc;
-        e = tc_prepare(D, pl.np);
+        if ((rc = encode_q_map(&tmq, q, D, B, T, Hq, p.G, pl.np))) return rc;
+        e = tc_prepare(D, pl.np, T > 1);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         e = launch_decode_tc(tmk, tmv, tmq, p, pl.np, P.num_ctas, stream);
     } else {
@@ -430,6 +452,13 @@ int gqa_decode_attn(const void *q, const void *k_cache, const void *v_cache,
                     float scale, kvattn_stream_t stream) {
     return run_decode(q, k_cache, v_cache, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, Lmax,
                       scale, Lmax, stream, "gqa_decode_attn");
+}
+
+int gqa_decode_attn_multi(const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *seq_lens, float *out, int B, int T, int Hq, int Hkv,
+                          int D, int Lmax, float scale, kvattn_stream_t stream) {
+    return run_decode(q, k_cache, v_cache, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, Lmax,
+                      scale, Lmax, stream, "gqa_decode_attn_multi", T);
 }
 
 int gqa_decode_attn_window(const void *q, const void *k_cache, const void *v_cache,

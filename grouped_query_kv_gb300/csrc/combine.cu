@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
     const int kvh = seg / p.head_groups;
     const int hg = seg % p.head_groups;
     const int h0 = kvh * p.G + hg * p.heads_per_seg;
-    const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
+    const int gvalid = p.T == 1 ? min(p.heads_per_seg, p.G - hg * p.heads_per_seg)
+                                : p.heads_per_seg;  // (token, head) columns
     const int D = p.D;
     const int x = (blockIdx.y * kThreads + tid) * 4;
     const int g = x / D, d = x % D;
@@ -118,7 +119,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
         mrun = mx;
     }
     const float inv = (den > 0.f) ? 1.f / den : 0.f;
-    *reinterpret_cast<float4 *>(p.out + ((size_t)b * p.Hq + h0 + g) * D + d) =
+    const int t = p.T == 1 ? 0 : g / p.G, gg = p.T == 1 ? g : g % p.G;
+    *reinterpret_cast<float4 *>(p.out + (((size_t)b * p.T + t) * p.Hq + h0 + gg) * D + d) =
         make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
 }
 

@@ -147,7 +147,10 @@ __device__ __forceinline__ bool chunk_is_v(long long m, long long n, long long *
     return false;
 }
 
-template <int D, int NP>
+// MT: several new tokens per sequence (columns are (token, head), causal
+// limits on the last tile); a separate instantiation, so the one-token
+// kernel carries none of it.
+template <int D, int NP, bool MT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
@@ -277,12 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&bs.q_full[qs], C::QB);
-                        const int row = itk.b * p.Hq + kvh * p.G + hg * p.heads_per_seg;
+                        // one token: q as (D, B*Hq, 1), the NP rows from the group's
+                        // first head; T tokens: q as (D, Hq, B*T), the group's heads
+                        // of each of the sequence's T tokens, rows ordered (token, head)
+                        mbar_arrive_expect_tx(&bs.q_full[qs], (uint32_t)p.q_bytes);
+                        const int h0 = kvh * p.G + hg * p.heads_per_seg;
+                        const int qy = MT ? h0 : itk.b * p.Hq + h0;
+                        const int qz = MT ? itk.b * p.T : 0;
 #pragma unroll
                         for (int sl = 0; sl < D / 64; ++sl)
-                            tma_load_2d(qbuf + qs * C::QB + sl * NP * 128, &tmq, &bs.q_full[qs],
-                                        sl * 64, row);
+                            tma_load_3d_plain(qbuf + qs * C::QB + sl * NP * 128, &tmq,
+                                              &bs.q_full[qs], sl * 64, qy, qz);
                     }
                     ++piece;
                 }
@@ -483,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row == 0 && q4 == 0 && t0 == 0 && (it.len < 0 || it.len > p.Lmax))
             set_error(p.err, DEV_ERR_BOUNDS);
         const int h0 = kvh * p.G + hg * p.heads_per_seg;
-        const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
+        // columns: (token, head) for T new tokens, heads of one group otherwise
+        const int gvalid = MT ? p.heads_per_seg : min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
         const long long i0 = i;
 #pragma unroll
         for (int g = 0; g < NP; ++g) l[g] = 0.f;
@@ -522,6 +531,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s[g + 3] = valid ? s[g + 3] * p.scale_log2 : -INFINITY;
                 over |= (s[g] > m4.x + kTau) | (s[g + 1] > m4.y + kTau) |
                         (s[g + 2] > m4.z + kTau) | (s[g + 3] > m4.w + kTau);
+            }
+            if (MT && r0 + kT - 1 >= len - (p.T - 1)) {
+                // the tile holds new tokens: token t sees positions < len - (T-1-t)
+                // (a column masked here after voting at most costs an exact max)
+                const int pos = r0 + row;
+                int t = 0, gg = 0;
+#pragma unroll
+                for (int g = 0; g < NP; ++g) {
+                    if (pos >= len - (p.T - 1 - t)) s[g] = -INFINITY;
+                    if (++gg == p.G) {
+                        gg = 0;
+                        ++t;
+                    }
+                }
             }
             if (named_bar_sync_or(kBarSoftmax, 128, over || fail)) {
                 if (named_bar_sync_or(kBarSoftmax, 128, fail || *abort_flag != 0)) {
@@ -647,7 +670,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 16; ++k) o[c * 16 + k] = v[k] + w[k];
             }
             const int d = db * 128 + row;
-            if (complete) {
+            if (complete && MT) {
+                // column (t, gg) -> out row (b*T + t)*Hq + h0 + gg
+                int t = 0, gg = 0;
+#pragma unroll
+                for (int g = 0; g < NP; ++g) {
+                    if (g < gvalid) {
+                        const float lt = ltot_s[g];
+                        p.out[(((size_t)b * p.T + t) * p.Hq + h0 + gg) * D + d] =
+                            (lt > 0.f) ? o[g] / lt : 0.f;
+                    }
+                    if (++gg == p.G) {
+                        gg = 0;
+                        ++t;
+                    }
+                }
+            } else if (complete) {
 #pragma unroll
                 for (int g = 0; g < NP; ++g) {
                     if (g < gvalid) {
@@ -681,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(kBarEnd, 160);
 }
 
-template <int D, int NP>
+template <int D, int NP, bool MT>
 cudaError_t launch_t(const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmq,
                      const DecodeParams &p, int num_ctas, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -694,17 +732,17 @@ cudaError_t launch_t(const CUtensorMap &tmk, const CUtensorMap &tmv, const CUten
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NP>, tmk, tmv, tmq, p);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NP, MT>, tmk, tmv, tmq, p);
 }
 
-template <int D, int NP>
+template <int D, int NP, bool MT>
 cudaError_t prepare_t() {
     static int done_for_device[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && done_for_device[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_tc_kernel<D, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_tc_kernel<D, NP, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              TcCfg<D, NP>::alloc);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done_for_device[dev] = 1;
     return e;
@@ -735,6 +773,18 @@ bool tc_supported(int D, int G) { return (D == 128 || D == 256) && G >= 1; }
         case 256 * 1000 + 48: return FN<256, 48>(__VA_ARGS__); \
         default: break;                                   \
     }
+// the same, choosing the one-token or the several-token kernel
+#define KVATTN_TC_DISPATCH_MT(FN, mt, ...)                                             \
+    switch (D * 1000 + np) {                                                          \
+        case 128 * 1000 + 16: return mt ? FN<128, 16, true>(__VA_ARGS__) : FN<128, 16, false>(__VA_ARGS__); \
+        case 128 * 1000 + 32: return mt ? FN<128, 32, true>(__VA_ARGS__) : FN<128, 32, false>(__VA_ARGS__); \
+        case 128 * 1000 + 48: return mt ? FN<128, 48, true>(__VA_ARGS__) : FN<128, 48, false>(__VA_ARGS__); \
+        case 128 * 1000 + 64: return mt ? FN<128, 64, true>(__VA_ARGS__) : FN<128, 64, false>(__VA_ARGS__); \
+        case 256 * 1000 + 16: return mt ? FN<256, 16, true>(__VA_ARGS__) : FN<256, 16, false>(__VA_ARGS__); \
+        case 256 * 1000 + 32: return mt ? FN<256, 32, true>(__VA_ARGS__) : FN<256, 32, false>(__VA_ARGS__); \
+        case 256 * 1000 + 48: return mt ? FN<256, 48, true>(__VA_ARGS__) : FN<256, 48, false>(__VA_ARGS__); \
+        default: break;                                                               \
+    }
 
 template <int D, int NP>
 int smem_of() { return TcCfg<D, NP>::alloc; }
@@ -750,8 +800,8 @@ int tc_stages(int D, int np) {
     return -1;
 }
 
-cudaError_t tc_prepare(int D, int np) {
-    KVATTN_TC_DISPATCH(prepare_t)
+cudaError_t tc_prepare(int D, int np, bool several_tokens) {
+    KVATTN_TC_DISPATCH_MT(prepare_t, several_tokens)
     return cudaErrorInvalidValue;
 }
 
@@ -759,7 +809,7 @@ cudaError_t launch_decode_tc(const CUtensorMap &tmk, const CUtensorMap &tmv,
                              const CUtensorMap &tmq, const DecodeParams &p, int np, int num_ctas,
                              cudaStream_t stream) {
     const int D = p.D;
-    KVATTN_TC_DISPATCH(launch_t, tmk, tmv, tmq, p, num_ctas, stream)
+    KVATTN_TC_DISPATCH_MT(launch_t, p.T > 1, tmk, tmv, tmq, p, num_ctas, stream)
     return cudaErrorInvalidValue;
 }
 

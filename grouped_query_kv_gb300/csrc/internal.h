@@ -42,6 +42,9 @@ struct DecodeParams {
     int head_groups;          // ceil(G / heads_per_seg)
     int tile;                 // positions per tile
     int window;               // positions attended at most (>= Lmax: all)
+    int T;                    // new tokens (queries) per sequence, >= 1; q and out are
+                              // [B, T, Hq, D] and token t attends [0, len - T + 1 + t)
+    int q_bytes;              // tensor-core path: bytes of one piece's q load
     int cost_piece;           // schedule cost of starting and finishing a piece, in
                               // units where a tile costs 32
     float scale_log2;         // scale * log2(e)
@@ -71,7 +74,7 @@ int tc_tile();
 int tc_threads();
 int tc_smem_bytes(int D, int np);
 int tc_stages(int D, int np);
-cudaError_t tc_prepare(int D, int np);
+cudaError_t tc_prepare(int D, int np, bool several_tokens);
 cudaError_t launch_decode_tc(const CUtensorMap &tmk, const CUtensorMap &tmv,
                              const CUtensorMap &tmq, const DecodeParams &p, int np, int num_ctas,
                              cudaStream_t stream);

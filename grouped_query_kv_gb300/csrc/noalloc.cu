@@ -128,6 +128,8 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
     p.tile = tile;
     p.cost_piece = 16;  // the regular entry point's schedule weight for this path
     p.window = Lmax;    // full attention
+    p.T = 1;
+    p.q_bytes = 0;      // (the CUDA-core kernel reads q itself)
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

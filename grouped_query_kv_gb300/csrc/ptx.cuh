@@ -116,6 +116,16 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
+// 3-D tiled TMA load global -> shared, no cache hint.
+__device__ __forceinline__ void tma_load_3d_plain(void *smem_dst, const void *tmap, uint64_t *bar,
+                                                  int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // L2 eviction-priority hint for data read exactly once (the KV stream).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;

@@ -43,6 +43,9 @@ class Workload:
     # a local (sliding-window) attention layer: attend the last `window`
     # positions only; None is the full attention
     window: Optional[int] = None
+    # new tokens (queries) per sequence scored in one pass, causal among
+    # themselves (speculative sampling); their K/V rows are already cached
+    T: int = 1
     note: str = ""
 
     @property
@@ -75,6 +78,10 @@ WORKLOADS = {w.name: w for w in [
     Workload("palm540b_long_mqa", B=8, Hq=48, Hkv=1, D=256, Lmax=32768,
              scale=1.0 / 16.0, lens=(32768,), k_scale=0.5,
              note="PaLM-540B-shaped long-context MQA decode, k scaled by 0.5"),
+    Workload("llama70b_spec4", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
+             scale=1.0 / math.sqrt(128), ragged=True, T=4,
+             note="Llama-70B-shaped GQA scoring 4 drafted tokens per sequence in "
+                  "one pass (speculative sampling), lengths uniform in [4, 8192]"),
     Workload("local_gqa_w4096", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
              scale=1.0 / math.sqrt(128), lens=(8192,), window=4096,
              note="Llama-70B-shaped GQA decode through a local attention layer: "
@@ -91,7 +98,7 @@ def attn_lens(w: Workload, seed: int = 0) -> torch.Tensor:
     the device the values are drawn on)."""
     if w.ragged:
         g = torch.Generator().manual_seed(seed + 7919)
-        return torch.randint(1, w.Lmax + 1, (w.B,), generator=g,
+        return torch.randint(w.T, w.Lmax + 1, (w.B,), generator=g,
                              dtype=torch.int64).to(torch.int32)
     if len(w.lens) == 1:
         return torch.full((w.B,), w.lens[0], dtype=torch.int32)
@@ -110,7 +117,7 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", lens=None):
     """Draw one decode step's inputs.
 
     Returns a dict of tensors on `device`:
-      q        bf16 [B, Hq, D]
+      q        bf16 [B, Hq, D], or [B, T, Hq, D] for T new tokens
       k_cache  bf16 [B, Hkv, Lmax, D]   (every row drawn, padding included)
       v_cache  bf16 [B, Hkv, Lmax, D]
       k_new    bf16 [B, Hkv, D]         this step's new token
@@ -123,7 +130,7 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", lens=None):
     al = attn_lens(w, seed) if lens is None else torch.as_tensor(lens, dtype=torch.int32)
     assert al.shape == (w.B,)
     assert int(al.min()) >= 1 and int(al.max()) <= w.Lmax
-    q = _normal_bf16((w.B, w.Hq, w.D), gen, device)
+    q = _normal_bf16((w.B, w.Hq, w.D) if w.T == 1 else (w.B, w.T, w.Hq, w.D), gen, device)
     k_cache = _normal_bf16((w.B, w.Hkv, w.Lmax, w.D), gen, device, w.k_scale)
     v_cache = _normal_bf16((w.B, w.Hkv, w.Lmax, w.D), gen, device)
     k_new = _normal_bf16((w.B, w.Hkv, w.D), gen, device, w.k_scale)

@@ -147,6 +147,30 @@ KVATTN_API int gqa_decode_step(const void *q, const void *k_new, const void *v_n
                                float scale, kvattn_stream_t stream);
 
 /*
+ * gqa_decode_attn_multi -- attention for T new tokens per sequence, causal
+ * among themselves: the scoring pass of speculative sampling ("The Basics of
+ * Transformer Inference": the big model scores a run of drafted tokens in
+ * one pass, sharing the KV-cache loads among them).  The tokens' K/V rows
+ * are already in the cache at positions seq_lens[b] - T .. seq_lens[b] - 1;
+ * token t attends positions [0, seq_lens[b] - T + 1 + t) -- the cached prefix
+ * and the new tokens up to itself -- and gets a zero row when that is empty.
+ * Every K/V tile is read from HBM once for all T tokens.
+ *
+ *   q        : bf16 [B, T, Hq, D]
+ *   k_cache, v_cache, seq_lens : as for gqa_decode_attn (seq_lens counts the
+ *              new tokens too)
+ *   out      : fp32 [B, T, Hq, D]
+ *   T        : 1 .. 64; needs D in {128, 256} and G * T query rows per K/V
+ *              head within one pass (64 at D = 128, 48 at D = 256), else
+ *              KVATTN_ERR_UNSUPPORTED.  T = 1 is gqa_decode_attn.
+ * Ownership, streams and device-side errors are those of gqa_decode_attn.
+ */
+KVATTN_API int gqa_decode_attn_multi(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *seq_lens, float *out, int B, int T, int Hq,
+                                     int Hkv, int D, int Lmax, float scale,
+                                     kvattn_stream_t stream);
+
+/*
  * gqa_decode_attn_window, gqa_decode_step_window -- the same two calls for a
  * local (sliding-window) attention layer: the query at position len_b - 1
  * attends only positions [max(0, len_b - window), len_b), the token itself

@@ -430,3 +430,56 @@ def test_local_window_must_be_positive():
     x = wl.make_inputs(w, seed=0, device=dev)
     with pytest.raises(g.KvAttnError):
         g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale, window=0)
+
+
+# --------------------------------------------- several new tokens (speculative)
+# "The Basics of Transformer Inference", speculative sampling: T drafted
+# tokens scored in one pass; token t attends the prefix and the new tokens up
+# to itself.
+
+def _multi_case(B, T, Hq, Hkv, D, Lmax, lens, seed, nan_pad=True):
+    dev = torch.device("cuda")
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    q = torch.randn((B, T, Hq, D), generator=gen).to(torch.bfloat16).to(dev)
+    k = torch.randn((B, Hkv, Lmax, D), generator=gen).to(torch.bfloat16).to(dev)
+    v = torch.randn((B, Hkv, Lmax, D), generator=gen).to(torch.bfloat16).to(dev)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+    if nan_pad:
+        for b, n in enumerate(lens):
+            k[b, :, n:] = float("nan")
+            v[b, :, n:] = float("inf")
+    scale = 1.0 / np.sqrt(D)
+    out = g.gqa_decode_attn_multi(q, k, v, lens_t, scale)
+    g.check_device_error()
+    lens_np = np.array(lens, np.int32)
+    ref = oracle.gqa_decode_multi(bits(q), bits(k), bits(v), lens_np, scale,
+                                  nthreads=oracle_threads())
+    assert_close(out.reshape(B * T, Hq, D), ref.reshape(B * T, Hq, D), bits(v), lens_np)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,T", [(128, 64, 8, 1), (128, 64, 8, 2), (128, 64, 8, 4),
+                                        (128, 64, 8, 8), (128, 16, 16, 2), (128, 16, 16, 8),
+                                        (128, 4, 4, 64), (256, 16, 1, 2), (256, 16, 1, 3),
+                                        (256, 8, 8, 5)])
+def test_new_tokens_attend_causally(D, Hq, Hkv, T):
+    lens = (700, T, 129, 256, 1000, 383, max(1, T - 1), 128)
+    _multi_case(len(lens), T, Hq, Hkv, D, 1000, lens, seed=T * 7 + D + Hq)
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 152, 400])
+def test_new_tokens_with_split_pieces(ctas):
+    g.set_tuning(0, ctas)
+    try:
+        _multi_case(3, 4, 32, 4, 128, 3000, (3000, 130, 2047), seed=ctas)
+    finally:
+        g.set_tuning(0, 0)
+
+
+def test_new_tokens_reject_what_one_pass_cannot_hold():
+    dev = torch.device("cuda")
+    for (B, T, Hq, Hkv, D) in [(1, 5, 16, 1, 256), (1, 9, 64, 8, 128), (1, 2, 4, 1, 64)]:
+        q = torch.zeros((B, T, Hq, D), dtype=torch.bfloat16, device=dev)
+        k = torch.zeros((B, Hkv, 256, D), dtype=torch.bfloat16, device=dev)
+        lens = torch.full((B,), 100, dtype=torch.int32, device=dev)
+        with pytest.raises(g.KvAttnError):
+            g.gqa_decode_attn_multi(q, k, k, lens, 0.1)
