@@ -55,6 +55,7 @@ _VP = ctypes.c_void_p
 _I = ctypes.c_int
 _SIGS = {
     "kv_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    "kv_append_multi": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "gqa_decode_attn": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                              ctypes.c_float, _VP]),
     "gqa_decode_step": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
@@ -154,6 +155,29 @@ def kv_append(k_cache, v_cache, k_new, v_new, seq_lens, stream=None):
     _need(seq_lens, "seq_lens", torch.int32, (B,))
     _check(lib().kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
                            _ptr(seq_lens), B, Hkv, D, Lmax, _stream_ptr(stream)))
+
+
+def kv_append_multi(k_cache, v_cache, k_new, v_new, seq_lens, stream=None):
+    """Write T new tokens' K/V rows: token t into row seq_lens[b] + t.
+
+    k_cache, v_cache: bf16 [B, Hkv, Lmax, D] (in place); k_new, v_new: bf16
+    [B, T, Hkv, D]; seq_lens: int32 [B], tokens cached before them (not
+    modified).
+    """
+    import torch
+    _need(k_cache, "k_cache", torch.bfloat16)
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must be [B, Hkv, Lmax, D]")
+    B, Hkv, Lmax, D = k_cache.shape
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lmax, D))
+    _need(k_new, "k_new", torch.bfloat16)
+    if k_new.dim() != 4 or k_new.shape[0] != B or k_new.shape[2:] != (Hkv, D):
+        raise ValueError("k_new must be [B, T, Hkv, D]")
+    T = k_new.shape[1]
+    _need(v_new, "v_new", torch.bfloat16, (B, T, Hkv, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    _check(lib().kv_append_multi(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                                 _ptr(seq_lens), B, T, Hkv, D, Lmax, _stream_ptr(stream)))
 
 
 def gqa_decode_attn(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None,

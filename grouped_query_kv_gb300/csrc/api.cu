@@ -285,6 +285,33 @@ int api_cuda_fail(cudaError_t e, const char *what) { return cuda_fail(e, what); 
 
 }  // namespace kvattn
 
+namespace {
+
+int append_rows(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                const int32_t *seq_lens, int B, int T, int Hkv, int D, int Lmax,
+                kvattn_stream_t stream, const char *who) {
+    if (!k_cache || !v_cache || !k_new || !v_new || !seq_lens)
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: null pointer", who);
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", who);
+    int rc = check_sizes(B, Hkv, Hkv, D, Lmax);
+    if (rc) return rc;
+    int dev;
+    if ((rc = current_device(&dev))) return rc;
+    DeviceState *ds;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if ((rc = device_state(dev, &ds))) return rc;
+    }
+    cudaError_t e = launch_kv_append(k_cache, v_cache, k_new, v_new, seq_lens, B, T, Hkv, D,
+                                     Lmax, ds->err, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return KVATTN_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char *kvattn_status_string(int status) {
@@ -330,27 +357,21 @@ int kvattn_get_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, kvattn
     return KVATTN_OK;
 }
 
+int kv_append_multi(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                    const int32_t *seq_lens, int B, int T, int Hkv, int D, int Lmax,
+                    kvattn_stream_t stream) {
+    t_last_error[0] = 0;
+    if (T < 1 || T > 64)
+        return fail(KVATTN_ERR_INVALID_ARG, "kv_append_multi: T must be in [1, 64] (got %d)", T);
+    return append_rows(k_cache, v_cache, k_new, v_new, seq_lens, B, T, Hkv, D, Lmax, stream,
+                       "kv_append_multi");
+}
+
 int kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
               const int32_t *seq_lens, int B, int Hkv, int D, int Lmax, kvattn_stream_t stream) {
     t_last_error[0] = 0;
-    if (!k_cache || !v_cache || !k_new || !v_new || !seq_lens)
-        return fail(KVATTN_ERR_INVALID_ARG, "kv_append: null pointer");
-    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
-        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-        return fail(KVATTN_ERR_INVALID_ARG, "kv_append: pointers must be 16-byte aligned");
-    int rc = check_sizes(B, Hkv, Hkv, D, Lmax);
-    if (rc) return rc;
-    int dev;
-    if ((rc = current_device(&dev))) return rc;
-    DeviceState *ds;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if ((rc = device_state(dev, &ds))) return rc;
-    }
-    cudaError_t e = launch_kv_append(k_cache, v_cache, k_new, v_new, seq_lens, B, Hkv, D, Lmax,
-                                     ds->err, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
-    return KVATTN_OK;
+    return append_rows(k_cache, v_cache, k_new, v_new, seq_lens, B, 1, Hkv, D, Lmax, stream,
+                       "kv_append");
 }
 
 }  // extern "C"

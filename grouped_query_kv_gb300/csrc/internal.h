@@ -52,7 +52,7 @@ struct DecodeParams {
 
 // Host launchers (return cudaError_t of the launch).
 cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
-                             const int32_t *seq_lens, int B, int Hkv, int D, int Lmax,
+                             const int32_t *seq_lens, int B, int T, int Hkv, int D, int Lmax,
                              unsigned int *err, cudaStream_t stream);
 
 // FMA split-KV kernel; heads_per_seg must be the value plan_fma() returned.

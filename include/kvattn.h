@@ -147,6 +147,23 @@ KVATTN_API int gqa_decode_step(const void *q, const void *k_new, const void *v_n
                                float scale, kvattn_stream_t stream);
 
 /*
+ * kv_append_multi -- kv_append for T new tokens per sequence (the drafted
+ * tokens of speculative sampling): token t's rows go into row
+ * seq_lens[b] + t.
+ *
+ *   k_new, v_new : bf16 [B, T, Hkv, D]
+ *   seq_lens     : int32 [B] (device), tokens cached before the T new ones;
+ *                  not modified
+ *   T            : 1 .. 64 (KVATTN_ERR_INVALID_ARG otherwise)
+ * The rest as for kv_append; a sequence whose T rows do not all fit
+ * (seq_lens[b] + T > Lmax, or seq_lens[b] < 0) is left untouched and sets
+ * KVATTN_ERR_DEVICE_BOUNDS.  Bit-exact.
+ */
+KVATTN_API int kv_append_multi(void *k_cache, void *v_cache, const void *k_new,
+                               const void *v_new, const int32_t *seq_lens, int B, int T,
+                               int Hkv, int D, int Lmax, kvattn_stream_t stream);
+
+/*
  * gqa_decode_attn_multi -- attention for T new tokens per sequence, causal
  * among themselves: the scoring pass of speculative sampling ("The Basics of
  * Transformer Inference": the big model scores a run of drafted tokens in

@@ -483,3 +483,42 @@ def test_new_tokens_reject_what_one_pass_cannot_hold():
         lens = torch.full((B,), 100, dtype=torch.int32, device=dev)
         with pytest.raises(g.KvAttnError):
             g.gqa_decode_attn_multi(q, k, k, lens, 0.1)
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_appending_several_tokens_is_bit_exact(T):
+    # T single-row appends in the oracle, one call on the GPU; then the same
+    # tokens scored together
+    dev = torch.device("cuda")
+    B, Hq, Hkv, D, Lmax = 4, 32, 4, 128, 600
+    before = np.array([0, 37, 590 - T, 300], np.int32)
+    gen = torch.Generator(device="cpu").manual_seed(T)
+    k = torch.randn((B, Hkv, Lmax, D), generator=gen).to(torch.bfloat16).to(dev)
+    v = torch.randn((B, Hkv, Lmax, D), generator=gen).to(torch.bfloat16).to(dev)
+    kn = torch.randn((B, T, Hkv, D), generator=gen).to(torch.bfloat16).to(dev)
+    vn = torch.randn((B, T, Hkv, D), generator=gen).to(torch.bfloat16).to(dev)
+    q = torch.randn((B, T, Hq, D), generator=gen).to(torch.bfloat16).to(dev)
+    k_ref, v_ref = bits(k), bits(v)
+    for t in range(T):
+        oracle.kv_append(k_ref, v_ref, np.ascontiguousarray(bits(kn)[:, t]),
+                         np.ascontiguousarray(bits(vn)[:, t]), before + t)
+    g.kv_append_multi(k, v, kn, vn, torch.tensor(before, device=dev))
+    g.check_device_error()
+    assert np.array_equal(bits(k), k_ref) and np.array_equal(bits(v), v_ref)
+    lens = before + T
+    out = g.gqa_decode_attn_multi(q, k, v, torch.tensor(lens, device=dev), 0.088)
+    ref = oracle.gqa_decode_multi(bits(q), k_ref, v_ref, lens, 0.088, nthreads=oracle_threads())
+    assert_close(out.reshape(B * T, Hq, D), ref.reshape(B * T, Hq, D), v_ref, lens)
+
+
+def test_appending_rows_that_do_not_fit_is_flagged_and_skipped():
+    dev = torch.device("cuda")
+    B, T, Hkv, D, Lmax = 2, 4, 2, 128, 64
+    k = torch.zeros((B, Hkv, Lmax, D), dtype=torch.bfloat16, device=dev)
+    v = torch.zeros_like(k)
+    kn = torch.ones((B, T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    before = torch.tensor([10, Lmax - T + 1], dtype=torch.int32, device=dev)
+    g.kv_append_multi(k, v, kn, kn, before)
+    with pytest.raises(g.KvAttnError):
+        g.check_device_error()
+    assert torch.all(k[1] == 0) and torch.all(k[0, :, 10:14] == 1)
