@@ -213,11 +213,51 @@ class Oracle:
         return out
 
 
+    def gather_paged(self, pool, block_table, seq_lens, block_size):
+        """The contiguous cache [B, Hkv, Lmax, D] a paged cache stands for
+        ("Machine Learning Engineering and AI Systems at Scale", section "The
+        key and value cache": fixed-size blocks and a per-sequence block
+        table that maps logical positions to physical blocks).  Position p of
+        sequence b lives in row p % block_size of physical block
+        block_table[b, p // block_size]; pool is [num_blocks, Hkv,
+        block_size, D].  Rows past a sequence's length are left zero.
+        A plain copy -- no arithmetic."""
+        pool = np.ascontiguousarray(pool)
+        table = np.asarray(block_table)
+        lens = np.asarray(seq_lens)
+        nblk, Hkv, bs, D = pool.shape
+        if bs != block_size:
+            raise ValueError("block_size mismatch")
+        B, maxb = table.shape
+        out = np.zeros((B, Hkv, maxb * bs, D), dtype=pool.dtype)
+        for b in range(B):
+            n = int(lens[b])
+            if n < 0 or n > maxb * bs:
+                raise ValueError("length outside the block table")
+            for p in range(n):
+                blk = int(table[b, p // bs])
+                if blk < 0 or blk >= nblk:
+                    raise ValueError("block index outside the pool")
+                out[b, :, p] = pool[blk, :, p % bs]
+        return out
+
+    def gqa_decode_paged(self, q, k_pool, v_pool, block_table, seq_lens, block_size, scale,
+                         nthreads=1):
+        """Decode attention over a paged cache: the same softmax(scale q K^T) V
+        over the positions the block table maps, i.e. gqa_decode on the
+        gathered contiguous cache."""
+        k = self.gather_paged(k_pool, block_table, seq_lens, block_size)
+        v = self.gather_paged(v_pool, block_table, seq_lens, block_size)
+        return self.gqa_decode(q, k, v, seq_lens, scale, nthreads=nthreads)
+
+
 _default = Oracle()
 bf16_to_double = _default.bf16_to_double
 kv_append = _default.kv_append
 gqa_decode = _default.gqa_decode
 gqa_decode_multi = _default.gqa_decode_multi
+gather_paged = _default.gather_paged
+gqa_decode_paged = _default.gqa_decode_paged
 
 
 def _u16(a):

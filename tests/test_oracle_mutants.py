@@ -153,3 +153,71 @@ def test_planted_mistake_is_caught(name, tmp_path):
     assert src.count(old) >= 1, "mutation anchor not found: " + name
     so = oracle.compile_variant(src.replace(old, new), str(tmp_path))
     assert not pins_pass(oracle.Oracle(so)), name
+
+
+# ------------------------------------------------------- paged cache gather
+# The paged oracle is a plain gather through the block table followed by the
+# contiguous decode; mistakes are planted in copies of the gather.
+
+def _paged_pins_pass(orc) -> bool:
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, D, bs, nb = 3, 4, 2, 16, 8, 4
+    L = bs * nb
+    q = _bits(rng.standard_normal((B, Hq, D)))
+    k = _bits(rng.standard_normal((B, Hkv, L, D)))
+    v = _bits(rng.standard_normal((B, Hkv, L, D)))
+    lens = np.array([32, 19, 9], np.int32)
+    # identity table over a pool made by numpy reshapes
+    kp = np.ascontiguousarray(k.reshape(B, Hkv, nb, bs, D).transpose(0, 2, 1, 3, 4).reshape(-1, Hkv, bs, D))
+    vp = np.ascontiguousarray(v.reshape(B, Hkv, nb, bs, D).transpose(0, 2, 1, 3, 4).reshape(-1, Hkv, bs, D))
+    table = np.arange(B * nb, dtype=np.int32).reshape(B, nb)
+    try:
+        out = orc.gqa_decode_paged(q, kp, vp, table, lens, bs, 0.25)
+    except (ValueError, IndexError):
+        return False
+    if not np.array_equal(out, orc.gqa_decode(q, k, v, lens, 0.25)):
+        return False
+    # blocks moved around the pool
+    perm = rng.permutation(B * nb)
+    kq, vq = np.empty_like(kp), np.empty_like(vp)
+    kq[perm], vq[perm] = kp, vp
+    try:
+        out2 = orc.gqa_decode_paged(q, kq, vq, perm[table].astype(np.int32), lens, bs, 0.25)
+    except (ValueError, IndexError):
+        return False
+    return np.array_equal(out2, out)
+
+
+class _PagedMutant(oracle.Oracle):
+    def __init__(self, kind):
+        super().__init__()
+        self.kind = kind
+
+    def gather_paged(self, pool, block_table, seq_lens, block_size):
+        nblk, Hkv, bs, D = pool.shape
+        table = np.asarray(block_table)
+        B, maxb = table.shape
+        out = np.zeros((B, Hkv, maxb * bs, D), dtype=pool.dtype)
+        for b in range(B):
+            for p in range(int(seq_lens[b])):
+                if self.kind == "row_and_block_swapped":
+                    blk, r = int(table[b, p % maxb]), p // maxb
+                    r = min(r, bs - 1)
+                elif self.kind == "block_table_of_sequence_zero":
+                    blk, r = int(table[0, p // bs]), p % bs
+                elif self.kind == "table_read_one_block_late":
+                    blk, r = int(table[b, min(p // bs + 1, maxb - 1)]), p % bs
+                else:  # "row_within_block_ignored"
+                    blk, r = int(table[b, p // bs]), 0
+                out[b, :, p] = pool[blk, :, r]
+        return out
+
+
+def test_unmodified_paged_oracle_passes():
+    assert _paged_pins_pass(oracle.Oracle())
+
+
+@pytest.mark.parametrize("kind", ["row_and_block_swapped", "block_table_of_sequence_zero",
+                                  "table_read_one_block_late", "row_within_block_ignored"])
+def test_planted_paged_mistake_is_caught(kind):
+    assert not _paged_pins_pass(_PagedMutant(kind)), kind

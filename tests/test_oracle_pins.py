@@ -455,3 +455,62 @@ def test_new_tokens_before_the_start_of_the_sequence_get_zero_rows():
     out = oracle.gqa_decode_multi(q, k, v, np.array([3], np.int32), 0.5)
     assert np.all(out[0, :2] == 0.0)                 # len - T + 1 + t <= 0
     assert np.array_equal(out[0, 2], unbits(v[0, 0, 0])[None].repeat(2, 0))  # sees one row
+
+
+# --------------------------------------------------------------- paged KV cache
+# "Machine Learning Engineering and AI Systems at Scale", "The key and value
+# cache" (PagedAttention):
+# fixed-size blocks of positions and a per-sequence block table mapping
+# logical positions to physical blocks; shared prefixes share blocks.
+
+def _pool_from_contiguous(k, bs):
+    """[B, Hkv, L, D] -> pool [B*L/bs, Hkv, bs, D] with the identity table,
+    by numpy reshapes (a library routine, independent of the oracle)."""
+    B, Hkv, L, D = k.shape
+    pool = k.reshape(B, Hkv, L // bs, bs, D).transpose(0, 2, 1, 3, 4).reshape(-1, Hkv, bs, D)
+    table = np.arange(B * (L // bs), dtype=np.int32).reshape(B, L // bs)
+    return np.ascontiguousarray(pool), table
+
+
+def test_paged_with_the_identity_table_is_the_contiguous_cache():
+    rng = np.random.default_rng(80)
+    q, k, v, lens = rand_case(rng, 3, 8, 2, 16, 64, lens=[64, 17, 1])
+    kp, table = _pool_from_contiguous(k, 16)
+    vp, _ = _pool_from_contiguous(v, 16)
+    out = oracle.gqa_decode_paged(q, kp, vp, table, lens, 16, 0.25)
+    assert np.array_equal(out, oracle.gqa_decode(q, k, v, lens, 0.25))
+
+
+def test_paged_result_does_not_depend_on_where_blocks_live():
+    rng = np.random.default_rng(81)
+    q, k, v, lens = rand_case(rng, 2, 4, 1, 8, 48, lens=[48, 30])
+    kp, table = _pool_from_contiguous(k, 8)
+    vp, _ = _pool_from_contiguous(v, 8)
+    perm = rng.permutation(kp.shape[0])            # physical block i moves to perm[i]
+    kq, vq = np.empty_like(kp), np.empty_like(vp)
+    kq[perm], vq[perm] = kp, vp
+    out = oracle.gqa_decode_paged(q, kq, vq, perm[table].astype(np.int32), lens, 8, 0.5)
+    assert np.array_equal(out, oracle.gqa_decode_paged(q, kp, vp, table, lens, 8, 0.5))
+
+
+def test_sequences_sharing_prefix_blocks_match_private_copies():
+    rng = np.random.default_rng(82)
+    bs, Hkv, D = 8, 2, 16
+    shared = rng.integers(0, 2 ** 15, size=(3, Hkv, bs, D)).astype(np.uint16) & 0x3FFF
+    own = rng.integers(0, 2 ** 15, size=(2, Hkv, bs, D)).astype(np.uint16) & 0x3FFF
+    pool = np.concatenate([shared, own])
+    table = np.array([[0, 1, 2, 3], [0, 1, 2, 4]], np.int32)   # 3 prefix blocks shared
+    lens = np.array([29, 32], np.int32)
+    q = bits(rng.standard_normal((2, 4, D)))
+    out = oracle.gqa_decode_paged(q, pool, pool, table, lens, bs, 0.3)
+    # the same sequences with private copies of the prefix
+    priv = np.concatenate([shared, own[:1], shared, own[1:]])
+    table2 = np.array([[0, 1, 2, 3], [4, 5, 6, 7]], np.int32)
+    assert np.array_equal(out, oracle.gqa_decode_paged(q, priv, priv, table2, lens, bs, 0.3))
+
+
+def test_paged_rejects_tables_outside_the_pool():
+    rng = np.random.default_rng(83)
+    pool = np.zeros((2, 1, 8, 8), np.uint16)
+    with pytest.raises(ValueError):
+        oracle.gather_paged(pool, np.array([[0, 5]], np.int32), np.array([12]), 8)
