@@ -191,19 +191,11 @@ def oracle_sample(w, seed, target_s, max_seqs=None):
     lens_all = wl.attn_lens(w, seed)
 
     def inputs(nb):
-        sub = dataclasses.replace(w, B=nb, lens=None, ragged=False)
-        x = wl.make_inputs(sub, seed=seed, device="cpu", lens=lens_all[:nb])
-        q, k, v = (wl.bf16_bits(x[n]) for n in ("q", "k_cache", "v_cache"))
-        lens = x["attn_lens"].numpy()
-        return q, k, v, lens, accounting.kv_bytes_read(lens, w.Hkv, w.D, window=w.window)
+        return _oracle_inputs(w, seed, nb, lens_all)
 
     def once(x):
-        q, k, v, lens, _ = x
         t = time.perf_counter()
-        if w.T > 1:
-            oracle.gqa_decode_multi(q, k, v, lens, w.scale, nthreads=threads)
-        else:
-            oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
+        _oracle_call(w, x, threads)
         return time.perf_counter() - t
 
     x1 = inputs(1)
@@ -240,7 +232,8 @@ def reference_arm(a, w):
         "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B_sampled": nb, "B": w.B, "Hq": w.Hq,
-                   "Hkv": w.Hkv, "D": w.D, "Lmax": w.Lmax, "window": w.window},
+                   "Hkv": w.Hkv, "D": w.D, "Lmax": w.Lmax, "window": w.window,
+                   "T": w.T, "block_size": w.block_size},
         "seq_steps_per_s": nb * len(times) / tot,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": "%d of %d sequences (all heads) per step; %s" %
@@ -252,30 +245,48 @@ def reference_arm(a, w):
     return 0
 
 
+def _oracle_inputs(w, seed, nb, lens_all):
+    """The first nb sequences of the workload as the oracle takes them
+    (bf16 bits; pools and a block table for a paged workload), with their
+    algorithmic bytes."""
+    import dataclasses
+
+    from grouped_query_kv_gb300 import accounting
+    from grouped_query_kv_gb300 import workloads as wl
+    sub = dataclasses.replace(w, B=nb, lens=None, ragged=False)
+    x = wl.make_inputs(sub, seed=seed, device="cpu", lens=lens_all[:nb])
+    lens = x["attn_lens"].numpy()
+    by = accounting.kv_bytes_read(lens, w.Hkv, w.D, window=w.window)
+    if w.block_size:
+        pg = wl.make_paged(sub, x, seed=seed)
+        return (wl.bf16_bits(x["q"]), wl.bf16_bits(pg["k_pool"]), wl.bf16_bits(pg["v_pool"]),
+                lens, by, pg["block_table"].numpy())
+    return tuple(wl.bf16_bits(x[n]) for n in ("q", "k_cache", "v_cache")) + (lens, by, None)
+
+
+def _oracle_call(w, x, threads):
+    import oracle
+    q, k, v, lens, _, table = x
+    if table is not None:
+        oracle.gqa_decode_paged(q, k, v, table, lens, w.block_size, w.scale, nthreads=threads)
+    elif w.T > 1:
+        oracle.gqa_decode_multi(q, k, v, lens, w.scale, nthreads=threads)
+    else:
+        oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
+
+
 _FIXED_CACHE = {}
 
 
 def _oracle_fixed(w, seed, nb, threads):
-    import dataclasses
-
-    import oracle
-    from grouped_query_kv_gb300 import accounting
     from grouped_query_kv_gb300 import workloads as wl
     key = (w.name, seed, nb)
     if key not in _FIXED_CACHE:
-        lens_all = wl.attn_lens(w, seed)
-        sub = dataclasses.replace(w, B=nb, lens=None, ragged=False)
-        x = wl.make_inputs(sub, seed=seed, device="cpu", lens=lens_all[:nb])
-        _FIXED_CACHE[key] = tuple(wl.bf16_bits(x[n]) for n in ("q", "k_cache", "v_cache")) + \
-            (x["attn_lens"].numpy(),)
-    q, k, v, lens = _FIXED_CACHE[key]
+        _FIXED_CACHE[key] = _oracle_inputs(w, seed, nb, wl.attn_lens(w, seed))
+    x = _FIXED_CACHE[key]
     t = time.perf_counter()
-    if w.T > 1:
-        oracle.gqa_decode_multi(q, k, v, lens, w.scale, nthreads=threads)
-    else:
-        oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=threads, window=w.window)
-    return (time.perf_counter() - t, nb,
-            accounting.kv_bytes_read(lens, w.Hkv, w.D, window=w.window), threads)
+    _oracle_call(w, x, threads)
+    return time.perf_counter() - t, nb, x[4], threads
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -306,6 +317,17 @@ def gpu_arm(a, w):
     ncopies = max(1, int(math.ceil(4 * l2 / read_bytes)))
     ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
     x = wl.make_inputs(w, seed=a.seed + 1000 * rank, device=dev)
+    table = None
+    if w.block_size:
+        # paged: the pools hold only the blocks the sequences use, scattered
+        pg = wl.make_paged(w, x, seed=a.seed + 1000 * rank)
+        del x["k_cache"], x["v_cache"]
+        x["k_cache"], x["v_cache"], table = pg["k_pool"], pg["v_pool"], pg["block_table"]
+        cache_bytes = 2 * x["k_cache"].numel() * 2
+        ncopies = max(1, int(math.ceil(4 * l2 / read_bytes)))
+        ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
+        nblk, _, bs, _ = x["k_cache"].shape
+        maxb = table.shape[1]
     caches = [(x["k_cache"], x["v_cache"])]
     for r in range(1, ncopies):
         caches.append((x["k_cache"].clone(), x["v_cache"].clone()))
@@ -320,11 +342,16 @@ def gpu_arm(a, w):
     q_p, kn_p, vn_p, pos_p, out_p = map(P, (x["q"], x["k_new"], x["v_new"], pos, out))
 
     lens_p = P(lens)
+    table_p = P(table) if table is not None else None
 
     def call_step(r):
         # one decode step: append this token's K/V and attend (fused kernel);
         # for T drafted tokens, their scoring pass over the cache
-        if w.T > 1:
+        if table is not None:
+            rc = lib.gqa_decode_step_paged(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]),
+                                           table_p, pos_p, out_p, w.B, w.Hq, w.Hkv, w.D, nblk,
+                                           bs, maxb, float(w.scale), sp)
+        elif w.T > 1:
             rc = lib.gqa_decode_attn_multi(q_p, P(caches[r][0]), P(caches[r][1]), lens_p, out_p,
                                            w.B, w.T, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
         elif w.window is None:
@@ -406,6 +433,11 @@ def gpu_arm(a, w):
     dlens = torch.empty_like(lens)
     # bytes each e2e step moves, counted from the tensors it copies
     inputs_h = (hq, hlens) if w.T > 1 else (hq, hkn, hvn, hpos)
+    if table is not None:
+        # a paged server sends the block table with every step
+        htable = table.cpu().pin_memory()
+        dtable = torch.empty_like(table)
+        inputs_h = inputs_h + (htable,)
     io = {"h2d": sum(t.numel() * t.element_size() for t in inputs_h),
           "d2h": hout.numel() * hout.element_size()}
 
@@ -416,6 +448,13 @@ def gpu_arm(a, w):
             dlens.copy_(hlens, non_blocking=True)
             g.gqa_decode_attn_multi(dq, caches[r][0], caches[r][1], dlens, w.scale, out=out,
                                     stream=stream)
+        elif table is not None:
+            dkn.copy_(hkn, non_blocking=True)
+            dvn.copy_(hvn, non_blocking=True)
+            dpos.copy_(hpos, non_blocking=True)
+            dtable.copy_(htable, non_blocking=True)
+            g.gqa_decode_step_paged(dq, dkn, dvn, caches[r][0], caches[r][1], dtable, dpos,
+                                    w.scale, out=out, stream=stream)
         else:
             dkn.copy_(hkn, non_blocking=True)
             dvn.copy_(hvn, non_blocking=True)
@@ -450,8 +489,11 @@ def gpu_arm(a, w):
                    "kv_bytes_per_step": kv_bytes,
                    "l2": "inputs larger than L2: %d rotating cache copies, %.0f MB (%.1fx L2)"
                          % (ncopies, ncopies * cache_bytes / 1e6, ncopies * cache_bytes / l2),
-                   "T": w.T,
-                   "step": ("gqa_decode_attn_multi (T new tokens scored in one pass over the "
+                   "T": w.T, "block_size": w.block_size,
+                   "step": ("gqa_decode_step_paged (kv_append fused into the attention kernel, "
+                            "K/V reached through the block table), steps chained in CUDA graphs"
+                            if table is not None else
+                            "gqa_decode_attn_multi (T new tokens scored in one pass over the "
                             "cache, which already holds their rows), steps chained in CUDA graphs"
                             if w.T > 1 else
                             "gqa_decode_step (kv_append fused into the attention kernel), "
@@ -466,7 +508,9 @@ def gpu_arm(a, w):
                      "frac": achieved / peak,
                      "traffic": sum(traffic.values()) if traffic else None,
                      "traffic_by_kernel": traffic,
-                     "kernel": ("gqa_decode_attn_multi (split-KV kernel + combine), " if w.T > 1
+                     "kernel": ("gqa_decode_step_paged (fused append + split-KV kernel over "
+                                "the block table + combine), " if table is not None else
+                                "gqa_decode_attn_multi (split-KV kernel + combine), " if w.T > 1
                                 else "gqa_decode_step (fused append + split-KV kernel + combine), ")
                                +
                                "average over the timed steps",
@@ -475,7 +519,8 @@ def gpu_arm(a, w):
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
                 "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms,
                 "api": "grouped_query_kv_gb300.%s (eager)"
-                       % ("gqa_decode_attn_multi" if w.T > 1 else "gqa_decode_step")},
+                       % ("gqa_decode_step_paged" if table is not None else
+                          "gqa_decode_attn_multi" if w.T > 1 else "gqa_decode_step")},
         "gpu_launches": 2 * a.steps,
         "clocks": clk,
     }

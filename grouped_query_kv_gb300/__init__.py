@@ -15,7 +15,9 @@ import os
 import threading
 
 __all__ = [
-    "kv_append", "gqa_decode_attn", "gqa_decode_step", "check_device_error", "get_plan",
+    "kv_append", "kv_append_multi", "kv_append_paged", "gqa_decode_attn", "gqa_decode_step",
+    "gqa_decode_attn_multi", "gqa_decode_attn_paged", "gqa_decode_step_paged",
+    "check_device_error", "get_plan",
     "set_tuning", "release", "KvAttnError", "library_path", "lib",
     "KVATTN_OK", "KVATTN_ERR_INVALID_ARG", "KVATTN_ERR_UNSUPPORTED",
     "KVATTN_ERR_CUDA", "KVATTN_ERR_OOM", "KVATTN_ERR_DEVICE_BOUNDS",
@@ -68,6 +70,11 @@ _SIGS = {
                                     ctypes.c_float, _I, _VP]),
     "gqa_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                      ctypes.c_float, _VP]),
+    "kv_append_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "gqa_decode_attn_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
+                                   _I, ctypes.c_float, _VP]),
+    "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
+                                   _I, _I, _I, ctypes.c_float, _VP]),
     "kvattn_status_string": (ctypes.c_char_p, [_I]),
     "kvattn_last_error": (ctypes.c_char_p, []),
     "kvattn_check_device_error": (_I, [_VP]),
@@ -277,6 +284,107 @@ def gqa_decode_attn_multi(q, k_cache, v_cache, seq_lens, scale, out=None, stream
     _need(out, "out", torch.float32, (B, T, Hq, D))
     _check(lib().gqa_decode_attn_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
                                        _ptr(out), B, T, Hq, Hkv, D, Lmax, float(scale),
+                                       _stream_ptr(stream)))
+    return out
+
+
+def _pool_shape(k_pool, block_table, name="k_pool"):
+    """(num_blocks, Hkv, block_size, D, B, max_blocks) of a paged cache."""
+    import torch
+    _need(k_pool, name, torch.bfloat16)
+    if k_pool.dim() != 4:
+        raise ValueError("%s must be [num_blocks, Hkv, block_size, D]" % name)
+    _need(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [B, max_blocks]")
+    return tuple(k_pool.shape) + tuple(block_table.shape)
+
+
+def kv_append_paged(k_pool, v_pool, k_new, v_new, block_table, seq_lens, stream=None):
+    """Write new K/V rows into a paged pool: token t of sequence b goes to
+    position seq_lens[b] + t, i.e. row (seq_lens[b] + t) % block_size of block
+    block_table[b, (seq_lens[b] + t) // block_size].
+
+    k_pool, v_pool: bf16 [num_blocks, Hkv, block_size, D] (in place);
+    k_new, v_new: bf16 [B, Hkv, D] (one token) or [B, T, Hkv, D];
+    block_table: int32 [B, max_blocks]; seq_lens: int32 [B], tokens cached
+    before the new ones (not modified).
+    """
+    import torch
+    nblk, Hkv, bs, D, B, maxb = _pool_shape(k_pool, block_table)
+    _need(v_pool, "v_pool", torch.bfloat16, (nblk, Hkv, bs, D))
+    _need(k_new, "k_new", torch.bfloat16)
+    if k_new.dim() == 3:
+        T = 1
+    elif k_new.dim() == 4:
+        T = k_new.shape[1]
+    else:
+        raise ValueError("k_new must be [B, Hkv, D] or [B, T, Hkv, D]")
+    if k_new.shape[0] != B or tuple(k_new.shape[-2:]) != (Hkv, D):
+        raise ValueError("k_new must be [B, (T,) Hkv, D] matching the pool")
+    _need(v_new, "v_new", torch.bfloat16, tuple(k_new.shape))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    _check(lib().kv_append_paged(_ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
+                                 _ptr(block_table), _ptr(seq_lens), B, T, Hkv, D, nblk, bs,
+                                 maxb, _stream_ptr(stream)))
+
+
+def gqa_decode_attn_paged(q, k_pool, v_pool, block_table, seq_lens, scale, out=None,
+                          stream=None):
+    """gqa_decode_attn (q [B, Hq, D]) or gqa_decode_attn_multi (q [B, T, Hq, D])
+    over a paged cache: position j of sequence b is row j % block_size of
+    block block_table[b, j // block_size] of the pools.
+
+    k_pool, v_pool: bf16 [num_blocks, Hkv, block_size, D]; block_table: int32
+    [B, max_blocks]; seq_lens: int32 [B]; out: optional fp32 shaped like q.
+    Returns out.
+    """
+    import torch
+    _need(q, "q", torch.bfloat16)
+    if q.dim() not in (3, 4):
+        raise ValueError("q must be [B, Hq, D] or [B, T, Hq, D]")
+    B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]
+    T = 1 if q.dim() == 3 else q.shape[1]
+    nblk, Hkv, bs, Dp, Bt, maxb = _pool_shape(k_pool, block_table)
+    if Dp != D or Bt != B:
+        raise ValueError("k_pool / block_table do not match q")
+    _need(v_pool, "v_pool", torch.bfloat16, (nblk, Hkv, bs, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty(tuple(q.shape), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, tuple(q.shape))
+    _check(lib().gqa_decode_attn_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                       _ptr(seq_lens), _ptr(out), B, T, Hq, Hkv, D, nblk, bs,
+                                       maxb, float(scale), _stream_ptr(stream)))
+    return out
+
+
+def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, scale,
+                          out=None, stream=None):
+    """gqa_decode_step over a paged cache: the new token's rows go to position
+    seq_lens[b] through the block table, then attention over [0, seq_lens[b] + 1).
+
+    q: bf16 [B, Hq, D]; k_new, v_new: bf16 [B, Hkv, D]; pools and table as
+    for gqa_decode_attn_paged; seq_lens: tokens cached before this step.
+    """
+    import torch
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    B, Hq, D = q.shape
+    nblk, Hkv, bs, Dp, Bt, maxb = _pool_shape(k_pool, block_table)
+    if Dp != D or Bt != B:
+        raise ValueError("k_pool / block_table do not match q")
+    _need(v_pool, "v_pool", torch.bfloat16, (nblk, Hkv, bs, D))
+    _need(k_new, "k_new", torch.bfloat16, (B, Hkv, D))
+    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, (B, Hq, D))
+    _check(lib().gqa_decode_step_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                                       _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+                                       _ptr(out), B, Hq, Hkv, D, nblk, bs, maxb, float(scale),
                                        _stream_ptr(stream)))
     return out
 

@@ -110,6 +110,51 @@ int encode_cache_map(CUtensorMap *m, const void *base, int D, int Lmax, int BH, 
     return KVATTN_OK;
 }
 
+// 3-D map over a paged pool [num_blocks, Hkv, block_size, D] viewed as
+// (D, block_size, num_blocks*Hkv): box (64, min(block_size, 128), 1), the
+// same 128-byte swizzle; a tile is min(block_size, 128)-row boxes stacked.
+int encode_pool_map(CUtensorMap *m, const void *base, int D, int block_size, long long rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)block_size, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * (cuuint64_t)block_size};
+    cuuint32_t box[3] = {64, (cuuint32_t)(block_size < 128 ? block_size : 128), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVATTN_ERR_CUDA, "cuTensorMapEncodeTiled(pool) failed (%d)", (int)r);
+    return KVATTN_OK;
+}
+
+// A paged cache: pools [num_blocks, Hkv, block_size, D] and the block table.
+struct Paged {
+    const int32_t *table;  // [B, max_blocks]
+    int block_size, max_blocks, num_blocks;
+};
+
+// Checks a paged cache's sizes; on success *lg = log2(block_size) and
+// *Lmax = the positions a table row can address.
+int check_paged(const Paged &pg, int Hkv, const char *who, int *lg, int *Lmax) {
+    if (!pg.table) return fail(KVATTN_ERR_INVALID_ARG, "%s: null block table", who);
+    if (reinterpret_cast<uintptr_t>(pg.table) & 3u)
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: block table must be 4-byte aligned", who);
+    const int bs = pg.block_size;
+    if (bs < 16 || bs > (1 << 20) || (bs & (bs - 1)))
+        return fail(KVATTN_ERR_UNSUPPORTED, "%s: block_size must be a power of two in [16, 2^20] (got %d)",
+                    who, bs);
+    if (pg.max_blocks <= 0 || pg.num_blocks <= 0)
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: max_blocks and num_blocks must be positive", who);
+    if ((long long)pg.num_blocks * Hkv > 0x7fffffffLL)
+        return fail(KVATTN_ERR_UNSUPPORTED, "%s: num_blocks * Hkv beyond 2^31", who);
+    if ((long long)pg.max_blocks * bs > (1LL << 24))
+        return fail(KVATTN_ERR_UNSUPPORTED, "%s: max_blocks * block_size beyond 2^24", who);
+    int l = 0;
+    while ((1 << l) < bs) ++l;
+    *lg = l;
+    *Lmax = pg.max_blocks * bs;
+    return KVATTN_OK;
+}
+
 struct Plan {
     kvattn_plan pub;
     int heads_per_seg;
@@ -289,14 +334,15 @@ namespace {
 
 int append_rows(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
                 const int32_t *seq_lens, int B, int T, int Hkv, int D, int Lmax,
-                kvattn_stream_t stream, const char *who) {
+                kvattn_stream_t stream, const char *who, const Paged *pg = nullptr) {
     if (!k_cache || !v_cache || !k_new || !v_new || !seq_lens)
         return fail(KVATTN_ERR_INVALID_ARG, "%s: null pointer", who);
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
         (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return fail(KVATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", who);
-    int rc = check_sizes(B, Hkv, Hkv, D, Lmax);
-    if (rc) return rc;
+    int rc, lg = 0;
+    if (pg && (rc = check_paged(*pg, Hkv, who, &lg, &Lmax))) return rc;
+    if ((rc = check_sizes(B, Hkv, Hkv, D, Lmax))) return rc;
     int dev;
     if ((rc = current_device(&dev))) return rc;
     DeviceState *ds;
@@ -305,7 +351,9 @@ int append_rows(void *k_cache, void *v_cache, const void *k_new, const void *v_n
         if ((rc = device_state(dev, &ds))) return rc;
     }
     cudaError_t e = launch_kv_append(k_cache, v_cache, k_new, v_new, seq_lens, B, T, Hkv, D,
-                                     Lmax, ds->err, reinterpret_cast<cudaStream_t>(stream));
+                                     Lmax, pg ? pg->table : nullptr, lg, pg ? pg->max_blocks : 0,
+                                     pg ? pg->num_blocks : 0, ds->err,
+                                     reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     return KVATTN_OK;
 }
@@ -374,6 +422,18 @@ int kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new
                        "kv_append");
 }
 
+int kv_append_paged(void *k_pool, void *v_pool, const void *k_new, const void *v_new,
+                    const int32_t *block_table, const int32_t *seq_lens, int B, int T, int Hkv,
+                    int D, int num_blocks, int block_size, int max_blocks,
+                    kvattn_stream_t stream) {
+    t_last_error[0] = 0;
+    if (T < 1 || T > 64)
+        return fail(KVATTN_ERR_INVALID_ARG, "kv_append_paged: T must be in [1, 64] (got %d)", T);
+    const Paged pg{block_table, block_size, max_blocks, num_blocks};
+    return append_rows(k_pool, v_pool, k_new, v_new, seq_lens, B, T, Hkv, D, 0, stream,
+                       "kv_append_paged", &pg);
+}
+
 }  // extern "C"
 
 namespace {
@@ -383,7 +443,7 @@ namespace {
 int run_decode(const void *q, const void *k_cache, const void *v_cache, const void *k_new,
                const void *v_new, const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
                int D, int Lmax, float scale, int window, kvattn_stream_t stream_,
-               const char *who, int T = 1) {
+               const char *who, int T = 1, const Paged *pg = nullptr) {
     t_last_error[0] = 0;
     const bool fused = k_new != nullptr || v_new != nullptr;
     if (!q || !k_cache || !v_cache || !seq_lens || !out || (fused && (!k_new || !v_new)))
@@ -398,8 +458,14 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         return fail(KVATTN_ERR_INVALID_ARG, "%s: window must be >= 1 (got %d)", who, window);
     if (T < 1 || T > 64)
         return fail(KVATTN_ERR_INVALID_ARG, "%s: T must be in [1, 64] (got %d)", who, T);
-    int rc = check_sizes(B, Hq, Hkv, D, Lmax);
-    if (rc) return rc;
+    int rc, lg = 0;
+    if (pg) {
+        if ((rc = check_paged(*pg, Hkv, who, &lg, &Lmax))) return rc;
+        window = Lmax;
+        if (D != 128 && D != 256)
+            return fail(KVATTN_ERR_UNSUPPORTED, "%s: a paged cache needs D in {128, 256} (D=%d)", who, D);
+    }
+    if ((rc = check_sizes(B, Hq, Hkv, D, Lmax))) return rc;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
     int dev;
@@ -412,13 +478,21 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         if ((rc = device_state(dev, &ds))) return rc;
         if ((rc = get_encoder())) return rc;
         if ((rc = make_plan(B, Hq, Hkv, D, Lmax, ds->num_sms, &pl, T))) return rc;
+        if (pg && pl.pub.path != 2)
+            return fail(KVATTN_ERR_UNSUPPORTED, "%s: a paged cache needs the tensor-core path", who);
         if ((rc = get_workspace(dev, stream, (size_t)pl.pub.workspace_bytes, &ws))) return rc;
     }
     const kvattn_plan &P = pl.pub;
 
     CUtensorMap tmk, tmv;
-    if ((rc = encode_cache_map(&tmk, k_cache, D, Lmax, B * Hkv, P.tile_positions))) return rc;
-    if ((rc = encode_cache_map(&tmv, v_cache, D, Lmax, B * Hkv, P.tile_positions))) return rc;
+    if (pg) {
+        const long long rows = (long long)pg->num_blocks * Hkv;
+        if ((rc = encode_pool_map(&tmk, k_cache, D, pg->block_size, rows))) return rc;
+        if ((rc = encode_pool_map(&tmv, v_cache, D, pg->block_size, rows))) return rc;
+    } else {
+        if ((rc = encode_cache_map(&tmk, k_cache, D, Lmax, B * Hkv, P.tile_positions))) return rc;
+        if ((rc = encode_cache_map(&tmv, v_cache, D, Lmax, B * Hkv, P.tile_positions))) return rc;
+    }
 
     DecodeParams p;
     p.q = static_cast<const uint16_t *>(q);
@@ -445,14 +519,19 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     // bytes of one piece's q box: (64 columns x rows) per 64-column slab
     p.q_bytes = (D / 64) * (T == 1 ? pl.np : p.G * T) * 128;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.block_table = pg ? pg->table : nullptr;
+    p.block_lg = lg;
+    p.max_blocks = pg ? pg->max_blocks : 0;
+    p.num_blocks = pg ? pg->num_blocks : 0;
 
     cudaError_t e;
     if (P.path == 2) {
         CUtensorMap tmq;
         if ((rc = encode_q_map(&tmq, q, D, B, T, Hq, p.G, pl.np))) return rc;
-        e = tc_prepare(D, pl.np, T > 1);
+        e = pg ? tc_prepare_paged(D, pl.np, T > 1) : tc_prepare(D, pl.np, T > 1);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        e = launch_decode_tc(tmk, tmv, tmq, p, pl.np, P.num_ctas, stream);
+        e = pg ? launch_decode_tc_paged(tmk, tmv, tmq, p, pl.np, P.num_ctas, stream)
+               : launch_decode_tc(tmk, tmv, tmq, p, pl.np, P.num_ctas, stream);
     } else {
         e = fma_prepare(D, pl.heads_per_seg, P.smem_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
@@ -510,6 +589,28 @@ int gqa_decode_step_window(const void *q, const void *k_new, const void *v_new, 
     }
     return run_decode(q, k_cache, v_cache, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, Lmax,
                       scale, window, stream, "gqa_decode_step_window");
+}
+
+int gqa_decode_attn_paged(const void *q, const void *k_pool, const void *v_pool,
+                          const int32_t *block_table, const int32_t *seq_lens, float *out, int B,
+                          int T, int Hq, int Hkv, int D, int num_blocks, int block_size,
+                          int max_blocks, float scale, kvattn_stream_t stream) {
+    const Paged pg{block_table, block_size, max_blocks, num_blocks};
+    return run_decode(q, k_pool, v_pool, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, 0, scale,
+                      1, stream, "gqa_decode_attn_paged", T, &pg);
+}
+
+int gqa_decode_step_paged(const void *q, const void *k_new, const void *v_new, void *k_pool,
+                          void *v_pool, const int32_t *block_table, const int32_t *seq_lens,
+                          float *out, int B, int Hq, int Hkv, int D, int num_blocks,
+                          int block_size, int max_blocks, float scale, kvattn_stream_t stream) {
+    if (!k_new || !v_new) {
+        t_last_error[0] = 0;
+        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_step_paged: null pointer");
+    }
+    const Paged pg{block_table, block_size, max_blocks, num_blocks};
+    return run_decode(q, k_pool, v_pool, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, 0, scale, 1,
+                      stream, "gqa_decode_step_paged", 1, &pg);
 }
 
 int kvattn_check_device_error(kvattn_stream_t stream) {

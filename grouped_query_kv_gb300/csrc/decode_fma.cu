@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int y = it.first_pos();
             // fused append: this tile holds the new token's row
             if (p.len_add && it.last_tile_of_segment() && it.len >= 1 && it.len <= p.Lmax)
-                append_row_warp(p, z, it.len - 1, D, lane);
+                append_row_warp(p, z, (size_t)z * p.Lmax + (it.len - 1), D, lane);
             if (lane == 0) {
                 uint8_t *kdst = smem + s * S::stage_bytes;
                 uint8_t *vdst = kdst + C::TILE_BYTES;

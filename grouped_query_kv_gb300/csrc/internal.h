@@ -48,12 +48,23 @@ struct DecodeParams {
     int cost_piece;           // schedule cost of starting and finishing a piece, in
                               // units where a tile costs 32
     float scale_log2;         // scale * log2(e)
+    // Paged cache (block_table non-null): k_cache/v_cache are pools
+    // [num_blocks, Hkv, 2^block_lg, D]; position j of sequence b is row
+    // j mod 2^block_lg of block block_table[b * max_blocks + (j >> block_lg)],
+    // and Lmax = max_blocks << block_lg.
+    const int32_t *block_table;
+    int block_lg;
+    int max_blocks;
+    int num_blocks;
 };
 
 // Host launchers (return cudaError_t of the launch).
+// block_table null: contiguous caches [B, Hkv, Lmax, D]; else pools as in
+// DecodeParams (Lmax = max_blocks << block_lg).
 cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
                              const int32_t *seq_lens, int B, int T, int Hkv, int D, int Lmax,
-                             unsigned int *err, cudaStream_t stream);
+                             const int32_t *block_table, int block_lg, int max_blocks,
+                             int num_blocks, unsigned int *err, cudaStream_t stream);
 
 // FMA split-KV kernel; heads_per_seg must be the value plan_fma() returned.
 cudaError_t launch_decode_fma(const CUtensorMap &tmk, const CUtensorMap &tmv,
@@ -78,6 +89,12 @@ cudaError_t tc_prepare(int D, int np, bool several_tokens);
 cudaError_t launch_decode_tc(const CUtensorMap &tmk, const CUtensorMap &tmv,
                              const CUtensorMap &tmq, const DecodeParams &p, int np, int num_ctas,
                              cudaStream_t stream);
+// the same kernel reading a paged cache (p.block_table set; the K/V maps are
+// over the pools, box rows min(block size, 128))
+cudaError_t tc_prepare_paged(int D, int np, bool several_tokens);
+cudaError_t launch_decode_tc_paged(const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   const CUtensorMap &tmq, const DecodeParams &p, int np,
+                                   int num_ctas, cudaStream_t stream);
 
 cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream);
 

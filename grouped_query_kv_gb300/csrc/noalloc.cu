@@ -130,6 +130,10 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
     p.window = Lmax;    // full attention
     p.T = 1;
     p.q_bytes = 0;      // (the CUDA-core kernel reads q itself)
+    p.block_table = nullptr;  // contiguous cache
+    p.block_lg = 0;
+    p.max_blocks = 0;
+    p.num_blocks = 0;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

@@ -272,13 +272,15 @@ __device__ inline void sched_split_record(LenView lens, int B, int Lmax, int til
 // the tensor-copy (async) proxy.  Every CTA that loads the tile writes the
 // row itself (head groups of one K/V head write identical bytes), so no
 // reader depends on another CTA's write.
-__device__ __forceinline__ void append_row_warp(const DecodeParams &p, int z, int pos, int D,
+// Row src (b * Hkv + kvh) of k_new/v_new goes into cache row dst (a row
+// index of the [.., D] view of the cache or pool).
+__device__ __forceinline__ void append_row_warp(const DecodeParams &p, int src, size_t dst, int D,
                                                 int lane) {
     const int vecs = D / 8;  // 16-byte vectors per row
-    const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new) + (size_t)z * vecs;
-    const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new) + (size_t)z * vecs;
-    uint4 *kd = reinterpret_cast<uint4 *>(p.k_cache) + ((size_t)z * p.Lmax + pos) * vecs;
-    uint4 *vd = reinterpret_cast<uint4 *>(p.v_cache) + ((size_t)z * p.Lmax + pos) * vecs;
+    const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new) + (size_t)src * vecs;
+    const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new) + (size_t)src * vecs;
+    uint4 *kd = reinterpret_cast<uint4 *>(p.k_cache) + dst * vecs;
+    uint4 *vd = reinterpret_cast<uint4 *>(p.v_cache) + dst * vecs;
     for (int i = lane; i < vecs; i += 32) {
         kd[i] = ks[i];
         vd[i] = vs[i];

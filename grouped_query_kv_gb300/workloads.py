@@ -46,6 +46,9 @@ class Workload:
     # new tokens (queries) per sequence scored in one pass, causal among
     # themselves (speculative sampling); their K/V rows are already cached
     T: int = 1
+    # a paged cache: positions grouped in blocks of `block_size` in a shared
+    # pool, reached through a per-sequence block table; None: contiguous
+    block_size: Optional[int] = None
     note: str = ""
 
     @property
@@ -86,6 +89,13 @@ WORKLOADS = {w.name: w for w in [
              scale=1.0 / math.sqrt(128), lens=(8192,), window=4096,
              note="Llama-70B-shaped GQA decode through a local attention layer: "
                   "8192-token caches, the last 4096 positions attended"),
+    Workload("llama70b_paged16", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
+             scale=1.0 / math.sqrt(128), ragged=True, block_size=16,
+             note="Llama-70B-shaped GQA decode over a paged cache: 16-position "
+                  "blocks scattered through one pool, lengths uniform in [1, 8192]"),
+    Workload("llama70b_paged64", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
+             scale=1.0 / math.sqrt(128), ragged=True, block_size=64,
+             note="the same over 64-position blocks"),
 ] + _sweep()}
 
 # the five configurations in the order the benchmark suite lists them
@@ -145,3 +155,59 @@ def bf16_bits(t: torch.Tensor):
     import numpy as np
     assert t.dtype == torch.bfloat16
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def make_paged(w: Workload, x: dict, seed: int = 0, spare_blocks: int = 0,
+               fill_unused=None):
+    """A paged copy of make_inputs' caches: each sequence's first
+    ceil(attn_lens[b] / block_size) blocks of positions are moved to blocks
+    of one pool in a seeded random order (the way an allocator hands out
+    free blocks), and the block table records where each went.
+
+    Returns dict(k_pool, v_pool: bf16 [num_blocks, Hkv, block_size, D],
+    block_table: int32 [B, ceil(Lmax / block_size)]).  Table entries of
+    blocks a sequence does not use are -1; `spare_blocks` unused blocks are
+    added to the pool, and fill_unused (a bf16 bit pattern, e.g. 0x7FC0 for
+    NaN) overwrites every pool row no sequence position maps to.  A plain
+    copy: no attention arithmetic."""
+    bs = w.block_size
+    assert bs and bs & (bs - 1) == 0
+    k, v = x["k_cache"], x["v_cache"]
+    dev = k.device
+    B, Hkv, L, D = k.shape
+    maxb = (L + bs - 1) // bs
+    if maxb * bs != L:  # pad the positions to whole blocks
+        pad = maxb * bs - L
+        k = torch.cat([k, k.new_zeros((B, Hkv, pad, D))], dim=2)
+        v = torch.cat([v, v.new_zeros((B, Hkv, pad, D))], dim=2)
+    lens = x["attn_lens"].cpu().to(torch.int64)
+    nb = (lens + bs - 1) // bs
+    used = torch.arange(maxb)[None, :] < nb[:, None]            # [B, maxb]
+    n_used = int(used.sum())
+    total = n_used + spare_blocks
+    g = torch.Generator().manual_seed(seed + 104729)
+    phys = torch.randperm(total, generator=g)[:n_used]
+    table = torch.full((B, maxb), -1, dtype=torch.int32)
+    table[used] = phys.to(torch.int32)
+    kb = k.view(B, Hkv, maxb, bs, D).transpose(1, 2)            # [B, maxb, Hkv, bs, D]
+    vb = v.view(B, Hkv, maxb, bs, D).transpose(1, 2)
+    used_d = used.to(dev)
+    k_pool = torch.zeros((total, Hkv, bs, D), dtype=k.dtype, device=dev)
+    v_pool = torch.zeros((total, Hkv, bs, D), dtype=v.dtype, device=dev)
+    phys_d = phys.to(dev)
+    k_pool[phys_d] = kb[used_d]
+    v_pool[phys_d] = vb[used_d]
+    if fill_unused is not None:
+        pat = torch.tensor([fill_unused], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+        mask = torch.ones((total, bs), dtype=torch.bool)
+        mask[phys] = False                                      # blocks in use...
+        last = (lens - 1).clamp(min=0)                          # ...but rows past the length
+        for b in range(B):
+            n = int(lens[b])
+            if n > 0:
+                r = n - int(last[b]) // bs * bs
+                mask[int(table[b, int(last[b]) // bs]), r:] = True
+        m = mask.to(dev)[:, None, :].expand(total, Hkv, bs)
+        k_pool[m] = pat.to(dev)
+        v_pool[m] = pat.to(dev)
+    return dict(k_pool=k_pool, v_pool=v_pool, block_table=table.to(dev))

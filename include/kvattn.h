@@ -212,6 +212,79 @@ KVATTN_API int gqa_decode_step_window(const void *q, const void *k_new, const vo
                                       float scale, int window, kvattn_stream_t stream);
 
 /*
+ * Paged KV cache.  Instead of one contiguous [Lmax] run of rows per sequence,
+ * the cache is a pool of fixed-size blocks and each sequence keeps a block
+ * table mapping its logical positions to physical blocks; sequences that
+ * share a prefix may point at the same blocks ("Machine Learning
+ * Engineering and AI Systems at Scale", section "The key and value cache",
+ * on PagedAttention; "The Basics of Transformer Inference", item "Using
+ * ragged HBM reads and Paged Attention").  Position j of sequence b is row
+ * j % block_size of block block_table[b, j / block_size]:
+ *
+ *   k_pool, v_pool : bf16 [num_blocks, Hkv, block_size, D]
+ *   block_table    : int32 [B, max_blocks] (device, 4-byte aligned); a
+ *                    sequence may use max_blocks * block_size positions
+ *   block_size     : a power of two in [16, 2^20] (vLLM-style 16-position
+ *                    blocks as well as blocks of a few hundred positions)
+ *   max_blocks * block_size <= 2^24; num_blocks * Hkv < 2^31
+ *
+ * Table entries of blocks wholly past a sequence's length are never read;
+ * pool rows at and past the length in its last block are never read either
+ * (they may hold anything).  A table entry that is read and lies outside
+ * [0, num_blocks) sets KVATTN_ERR_DEVICE_BOUNDS in the sticky word; that
+ * block then reads as zeros (attention) or is not written (append) -- the
+ * sequence's output is then meaningless but no memory outside the pool is
+ * touched.  Results are those of the contiguous calls on the cache the
+ * table describes.  The attention calls need D in {128, 256} (the
+ * tensor-core kernel; KVATTN_ERR_UNSUPPORTED otherwise) and attend every
+ * position (no local window).
+ */
+
+/*
+ * kv_append_paged -- kv_append / kv_append_multi into a paged pool: token t
+ * of sequence b goes to position seq_lens[b] + t.
+ *
+ *   k_new, v_new : bf16 [B, T, Hkv, D]; T in [1, 64]
+ *   seq_lens     : int32 [B] (device), tokens cached before the T new ones
+ * A sequence whose T rows do not all fit in max_blocks * block_size
+ * positions is left untouched and sets KVATTN_ERR_DEVICE_BOUNDS.  Bit-exact.
+ */
+KVATTN_API int kv_append_paged(void *k_pool, void *v_pool, const void *k_new,
+                               const void *v_new, const int32_t *block_table,
+                               const int32_t *seq_lens, int B, int T, int Hkv, int D,
+                               int num_blocks, int block_size, int max_blocks,
+                               kvattn_stream_t stream);
+
+/*
+ * gqa_decode_attn_paged -- gqa_decode_attn (T = 1) or gqa_decode_attn_multi
+ * (T new tokens, causal among themselves) over a paged pool.
+ *
+ *   q        : bf16 [B, T, Hq, D]
+ *   seq_lens : int32 [B] (device), positions attended per sequence,
+ *              0 <= seq_lens[b] <= max_blocks * block_size (for T > 1 they
+ *              count the new tokens too)
+ *   out      : fp32 [B, T, Hq, D]
+ * The rest as for gqa_decode_attn / gqa_decode_attn_multi.
+ */
+KVATTN_API int gqa_decode_attn_paged(const void *q, const void *k_pool, const void *v_pool,
+                                     const int32_t *block_table, const int32_t *seq_lens,
+                                     float *out, int B, int T, int Hq, int Hkv, int D,
+                                     int num_blocks, int block_size, int max_blocks,
+                                     float scale, kvattn_stream_t stream);
+
+/*
+ * gqa_decode_step_paged -- gqa_decode_step over a paged pool: the new
+ * token's rows go to position seq_lens[b] (through the block table), then
+ * its query attends positions [0, seq_lens[b] + 1).  Arguments as for
+ * gqa_decode_step, with the pools and table above in place of the caches.
+ */
+KVATTN_API int gqa_decode_step_paged(const void *q, const void *k_new, const void *v_new,
+                                     void *k_pool, void *v_pool, const int32_t *block_table,
+                                     const int32_t *seq_lens, float *out, int B, int Hq,
+                                     int Hkv, int D, int num_blocks, int block_size,
+                                     int max_blocks, float scale, kvattn_stream_t stream);
+
+/*
  * gqa_decode_attn_noalloc -- the same computation as gqa_decode_attn, for
  * callers that must not have the library allocate device memory (for
  * example a server that gives all free GPU memory to its own pool at
