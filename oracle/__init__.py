@@ -65,6 +65,21 @@ def _bind(path):
     lib.oracle_gqa_decode_multi.argtypes = [u16p, u16p, u16p, i32p, f64p,
                                             i64, i64, i64, i64, i64, i64,
                                             ctypes.c_double, ctypes.c_int]
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_e4m3_encode_n.restype = None
+    lib.oracle_e4m3_encode_n.argtypes = [f32p, u8p, i64]
+    lib.oracle_e4m3_decode_n.restype = None
+    lib.oracle_e4m3_decode_n.argtypes = [u8p, f64p, i64]
+    lib.oracle_quantize_fp8.restype = None
+    lib.oracle_quantize_fp8.argtypes = [u16p, u8p, f32p, i64, i64]
+    lib.oracle_kv_append_fp8.restype = ctypes.c_int
+    lib.oracle_kv_append_fp8.argtypes = [u8p, u8p, f32p, f32p, u16p, u16p, i32p,
+                                         i64, i64, i64, i64]
+    lib.oracle_gqa_decode_fp8.restype = ctypes.c_int
+    lib.oracle_gqa_decode_fp8.argtypes = [u16p, u8p, u8p, f32p, f32p, i32p, f64p,
+                                          i64, i64, i64, i64, i64, ctypes.c_double,
+                                          ctypes.c_int]
     lib.oracle_gqa_decode_pairs.restype = ctypes.c_int
     lib.oracle_gqa_decode_pairs.argtypes = [u16p, u16p, u16p, i32p, f64p,
                                             i64, i64, i64, i64, i64,
@@ -251,13 +266,121 @@ class Oracle:
         return self.gqa_decode(q, k, v, seq_lens, scale, nthreads=nthreads)
 
 
+    # ------------------------------------------------------------ 8-bit cache
+    # ("The Basics of Transformer Inference", item "Quantization"; "Machine
+    # Learning Engineering and AI Systems at Scale", section "Quantization":
+    # FP8 E4M3; the rule itself is the reading in kvattn_oracle.c's header)
+
+    def e4m3_encode(self, x):
+        """float32 values -> E4M3 codes (nearest, ties to even, saturating)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(x.shape, dtype=np.uint8)
+        self.lib.oracle_e4m3_encode_n(x.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                      out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+                                      x.size)
+        return out
+
+    def e4m3_decode(self, codes):
+        """E4M3 codes -> float64 values (exact)."""
+        c, c_p = _u8(codes)
+        out = np.empty(c.shape, dtype=np.float64)
+        self.lib.oracle_e4m3_decode_n(c_p, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                      c.size)
+        return out
+
+    def quantize_fp8(self, rows):
+        """bf16 bits [..., D] -> (codes uint8 [..., D], scales float32 [...]):
+        one scale per row of D values."""
+        r, r_p = _u16(rows)
+        D = r.shape[-1]
+        n = r.size // D if D else 0
+        codes = np.empty(r.shape, dtype=np.uint8)
+        scales = np.empty(r.shape[:-1], dtype=np.float32)
+        self.lib.oracle_quantize_fp8(r_p, codes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+                                     scales.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), n, D)
+        return codes, scales
+
+    def dequantize_fp8(self, codes, scales):
+        """codes [..., D] and scales [...] -> float64 values, code * scale."""
+        return self.e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[..., None]
+
+    def kv_append_fp8(self, k_codes, v_codes, k_scale, v_scale, k_new, v_new, seq_lens):
+        """Quantize each sequence's new K/V rows into position seq_lens[b] of
+        an 8-bit cache, in place (codes uint8 [B, Hkv, Lmax, D], scales
+        float32 [B, Hkv, Lmax]; k_new, v_new bf16 bits [B, Hkv, D])."""
+        B, Hkv, Lmax, D = k_codes.shape
+        for a, dt in ((k_codes, np.uint8), (v_codes, np.uint8), (k_scale, np.float32),
+                      (v_scale, np.float32)):
+            if a.dtype != dt or not a.flags.c_contiguous:
+                raise TypeError("8-bit cache arrays must be contiguous uint8 / float32")
+        if v_codes.shape != k_codes.shape or k_scale.shape != (B, Hkv, Lmax) or \
+                v_scale.shape != (B, Hkv, Lmax):
+            raise ValueError("shape mismatch")
+        kn, kn_p = _u16(k_new)
+        vn, vn_p = _u16(v_new)
+        sl, sl_p = _i32(seq_lens)
+        if kn.shape != (B, Hkv, D) or vn.shape != (B, Hkv, D) or sl.shape != (B,):
+            raise ValueError("shape mismatch")
+        u8 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))  # noqa: E731
+        f32 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))  # noqa: E731
+        rc = self.lib.oracle_kv_append_fp8(u8(k_codes), u8(v_codes), f32(k_scale), f32(v_scale),
+                                           kn_p, vn_p, sl_p, B, Hkv, D, Lmax)
+        if rc != 0:
+            raise ValueError("oracle_kv_append_fp8: length outside [0, Lmax)")
+
+    def gqa_decode_fp8(self, q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale,
+                       nthreads=1):
+        """gqa_decode over an 8-bit cache: K = e4m3(code) * k_scale per row,
+        V likewise, in double.  q bf16 bits [B, Hq, D]; codes uint8
+        [B, Hkv, Lmax, D]; scales float32 [B, Hkv, Lmax].  Returns float64
+        [B, Hq, D]."""
+        qq, q_p = _u16(q)
+        kc, kc_p = _u8(k_codes)
+        vc, vc_p = _u8(v_codes)
+        ks, ks_p = _f32(k_scale)
+        vs, vs_p = _f32(v_scale)
+        sl, sl_p = _i32(seq_lens)
+        B, Hq, D = qq.shape
+        Hkv, Lmax = kc.shape[1], kc.shape[2]
+        if kc.shape != (B, Hkv, Lmax, D) or vc.shape != kc.shape or \
+                ks.shape != (B, Hkv, Lmax) or vs.shape != ks.shape or sl.shape != (B,):
+            raise ValueError("shape mismatch")
+        out = np.zeros((B, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_gqa_decode_fp8(q_p, kc_p, vc_p, ks_p, vs_p, sl_p,
+                                            out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                            B, Hq, Hkv, D, Lmax, float(scale), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_gqa_decode_fp8: bad arguments (heads or lengths)")
+        return out
+
+
 _default = Oracle()
 bf16_to_double = _default.bf16_to_double
 kv_append = _default.kv_append
 gqa_decode = _default.gqa_decode
 gqa_decode_multi = _default.gqa_decode_multi
 gather_paged = _default.gather_paged
+e4m3_encode = _default.e4m3_encode
+e4m3_decode = _default.e4m3_decode
+quantize_fp8 = _default.quantize_fp8
+dequantize_fp8 = _default.dequantize_fp8
+kv_append_fp8 = _default.kv_append_fp8
+gqa_decode_fp8 = _default.gqa_decode_fp8
 gqa_decode_paged = _default.gqa_decode_paged
+
+
+def _u8(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("E4M3 codes must be uint8")
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+
+
+def _f32(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.float32:
+        raise TypeError("scales must be float32")
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
 
 
 def _u16(a):
