@@ -115,8 +115,8 @@ MUTANTS = {
     "flipped sign in weights": ("double p = exp(s_buf[j] - m) / denom;",
                                 "double p = exp(m - s_buf[j]) / denom;"),
     "keys and values swapped": (
-        "oracle_bf16_to_double(V[(j0 + j) * D + d]);",
-        "oracle_bf16_to_double(K[(j0 + j) * D + d]);"),
+        "oracle_cache_at(v_cache, q8->v, q8->v_scale, row0, j0 + j, D, d)",
+        "oracle_cache_at(k_cache, q8->k, q8->k_scale, row0, j0 + j, D, d)"),
     "wrong query row": ("const uint16_t *qh = q + ((b * T + t) * Hq + h) * D;",
                         "const uint16_t *qh = q + ((b * T + t) * Hq + kvh) * D;"),
     "reads one row past the length": (
@@ -137,8 +137,8 @@ MUTANTS = {
                                   "const int64_t j0 = len > window ? len - window + 1 : 0;"),
     "window one position long": ("const int64_t j0 = len > window ? len - window : 0;",
                                  "const int64_t j0 = len > window ? len - window - 1 : 0;"),
-    "window values not shifted": ("oracle_bf16_to_double(V[(j0 + j) * D + d]);",
-                                  "oracle_bf16_to_double(V[j * D + d]);"),
+    "window values not shifted": ("oracle_cache_at(v_cache, q8->v, q8->v_scale, row0, j0 + j, D, d)",
+                                  "oracle_cache_at(v_cache, q8->v, q8->v_scale, row0, j, D, d)"),
 }
 
 
