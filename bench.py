@@ -257,6 +257,12 @@ def _oracle_inputs(w, seed, nb, lens_all):
     x = wl.make_inputs(sub, seed=seed, device="cpu", lens=lens_all[:nb])
     lens = x["attn_lens"].numpy()
     by = accounting.kv_bytes_read(lens, w.Hkv, w.D, window=w.window)
+    if w.kv_dtype == "fp8":
+        import oracle
+        kc, ks = oracle.quantize_fp8(wl.bf16_bits(x["k_cache"]))
+        vc, vs = oracle.quantize_fp8(wl.bf16_bits(x["v_cache"]))
+        by = accounting.kv_bytes_read_fp8(lens, w.Hkv, w.D)
+        return (wl.bf16_bits(x["q"]), kc, vc, lens, by, ("fp8", ks, vs))
     if w.block_size:
         pg = wl.make_paged(sub, x, seed=seed)
         return (wl.bf16_bits(x["q"]), wl.bf16_bits(pg["k_pool"]), wl.bf16_bits(pg["v_pool"]),
@@ -267,7 +273,9 @@ def _oracle_inputs(w, seed, nb, lens_all):
 def _oracle_call(w, x, threads):
     import oracle
     q, k, v, lens, _, table = x
-    if table is not None:
+    if isinstance(table, tuple):
+        oracle.gqa_decode_fp8(q, k, v, table[1], table[2], lens, w.scale, nthreads=threads)
+    elif table is not None:
         oracle.gqa_decode_paged(q, k, v, table, lens, w.block_size, w.scale, nthreads=threads)
     elif w.T > 1:
         oracle.gqa_decode_multi(q, k, v, lens, w.scale, nthreads=threads)
@@ -328,13 +336,31 @@ def gpu_arm(a, w):
         ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
         nblk, _, bs, _ = x["k_cache"].shape
         maxb = table.shape[1]
-    caches = [(x["k_cache"], x["v_cache"])]
-    for r in range(1, ncopies):
-        caches.append((x["k_cache"].clone(), x["v_cache"].clone()))
+    fp8 = w.kv_dtype == "fp8"
+    if fp8:
+        # the 8-bit cache: codes and per-row scales quantized on the GPU
+        kc, ks = g.kv_quantize_fp8(x["k_cache"])
+        vc, vs = g.kv_quantize_fp8(x["v_cache"])
+        del x["k_cache"], x["v_cache"]
+        x["k_cache"], x["v_cache"] = kc, vc
+        cache_bytes = 2 * (kc.numel() + 4 * ks.numel())
+        ncopies = max(1, int(math.ceil(4 * l2 / (read_bytes * (w.D + 4) / (2 * w.D)))))
+        ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
+        caches = [(kc, vc, ks, vs)]
+        for r in range(1, ncopies):
+            caches.append((kc.clone(), vc.clone(), ks.clone(), vs.clone()))
+    else:
+        caches = [(x["k_cache"], x["v_cache"])]
+        for r in range(1, ncopies):
+            caches.append((x["k_cache"].clone(), x["v_cache"].clone()))
     lens = x["attn_lens"]
     pos = x["append_pos"]
     out = torch.empty(tuple(x["q"].shape), dtype=torch.float32, device=dev)
     kv_bytes = accounting.kv_bytes_read(lens.cpu().tolist(), w.Hkv, w.D, window=w.window)
+    # bf16-equivalent bytes: what the same attention reads from a bf16 cache
+    kv_bytes_bf16 = kv_bytes
+    if fp8:
+        kv_bytes = accounting.kv_bytes_read_fp8(lens.cpu().tolist(), w.Hkv, w.D)
 
     stream = torch.cuda.Stream(device=dev)
     sp = ctypes_void(stream.cuda_stream)
@@ -347,7 +373,14 @@ def gpu_arm(a, w):
     def call_step(r):
         # one decode step: append this token's K/V and attend (fused kernel);
         # for T drafted tokens, their scoring pass over the cache
-        if table is not None:
+        if fp8:
+            c = caches[r]
+            rc = lib.kv_append_fp8(P(c[0]), P(c[1]), P(c[2]), P(c[3]), kn_p, vn_p, pos_p, w.B,
+                                   w.Hkv, w.D, w.Lmax, sp)
+            assert rc == 0, lib.kvattn_last_error()
+            rc = lib.gqa_decode_attn_fp8(q_p, P(c[0]), P(c[1]), P(c[2]), P(c[3]), lens_p, out_p,
+                                         w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+        elif table is not None:
             rc = lib.gqa_decode_step_paged(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]),
                                            table_p, pos_p, out_p, w.B, w.Hq, w.Hkv, w.D, nblk,
                                            bs, maxb, float(w.scale), sp)
@@ -433,6 +466,8 @@ def gpu_arm(a, w):
     dlens = torch.empty_like(lens)
     # bytes each e2e step moves, counted from the tensors it copies
     inputs_h = (hq, hlens) if w.T > 1 else (hq, hkn, hvn, hpos)
+    if fp8:
+        inputs_h = (hq, hkn, hvn, hpos, hlens)
     if table is not None:
         # a paged server sends the block table with every step
         htable = table.cpu().pin_memory()
@@ -448,6 +483,15 @@ def gpu_arm(a, w):
             dlens.copy_(hlens, non_blocking=True)
             g.gqa_decode_attn_multi(dq, caches[r][0], caches[r][1], dlens, w.scale, out=out,
                                     stream=stream)
+        elif fp8:
+            dkn.copy_(hkn, non_blocking=True)
+            dvn.copy_(hvn, non_blocking=True)
+            dpos.copy_(hpos, non_blocking=True)
+            dlens.copy_(hlens, non_blocking=True)
+            c = caches[r]
+            g.kv_append_fp8(c[0], c[1], c[2], c[3], dkn, dvn, dpos, stream=stream)
+            g.gqa_decode_attn_fp8(dq, c[0], c[1], c[2], c[3], dlens, w.scale, out=out,
+                                  stream=stream)
         elif table is not None:
             dkn.copy_(hkn, non_blocking=True)
             dvn.copy_(hvn, non_blocking=True)
@@ -489,8 +533,11 @@ def gpu_arm(a, w):
                    "kv_bytes_per_step": kv_bytes,
                    "l2": "inputs larger than L2: %d rotating cache copies, %.0f MB (%.1fx L2)"
                          % (ncopies, ncopies * cache_bytes / 1e6, ncopies * cache_bytes / l2),
-                   "T": w.T, "block_size": w.block_size,
-                   "step": ("gqa_decode_step_paged (kv_append fused into the attention kernel, "
+                   "T": w.T, "block_size": w.block_size, "kv_dtype": w.kv_dtype,
+                   "step": ("kv_append_fp8 then gqa_decode_attn_fp8 (8-bit cache: E4M3 codes and "
+                            "one fp32 scale per row; kv_bytes_per_step counts codes and scales), "
+                            "steps chained in CUDA graphs" if fp8 else
+                            "gqa_decode_step_paged (kv_append fused into the attention kernel, "
                             "K/V reached through the block table), steps chained in CUDA graphs"
                             if table is not None else
                             "gqa_decode_attn_multi (T new tokens scored in one pass over the "
@@ -502,13 +549,16 @@ def gpu_arm(a, w):
                    "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
         "seq_steps_per_s": world * w.B * a.steps / (ms_total / 1e3),
         "tokens_scored_per_s": world * w.B * w.T * a.steps / (ms_total / 1e3),
+        "bf16_equivalent_gbs": world * kv_bytes_bf16 * a.steps / (ms_total / 1e3) / 1e9,
         "us_per_step": 1e3 * ms_step,
         "hbm_fraction": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": sum(traffic.values()) if traffic else None,
                      "traffic_by_kernel": traffic,
-                     "kernel": ("gqa_decode_step_paged (fused append + split-KV kernel over "
+                     "kernel": ("kv_append_fp8 + gqa_decode_attn_fp8 (append, 8-bit split-KV "
+                                "kernel, combine), " if fp8 else
+                                "gqa_decode_step_paged (fused append + split-KV kernel over "
                                 "the block table + combine), " if table is not None else
                                 "gqa_decode_attn_multi (split-KV kernel + combine), " if w.T > 1
                                 else "gqa_decode_step (fused append + split-KV kernel + combine), ")
@@ -519,9 +569,10 @@ def gpu_arm(a, w):
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
                 "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms,
                 "api": "grouped_query_kv_gb300.%s (eager)"
-                       % ("gqa_decode_step_paged" if table is not None else
+                       % ("kv_append_fp8 + gqa_decode_attn_fp8" if fp8 else
+                          "gqa_decode_step_paged" if table is not None else
                           "gqa_decode_attn_multi" if w.T > 1 else "gqa_decode_step")},
-        "gpu_launches": 2 * a.steps,
+        "gpu_launches": (3 if fp8 else 2) * a.steps,
         "clocks": clk,
     }
     if rank == 0 and not a.no_cpu_baseline:

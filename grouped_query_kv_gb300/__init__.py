@@ -17,6 +17,7 @@ import threading
 __all__ = [
     "kv_append", "kv_append_multi", "kv_append_paged", "gqa_decode_attn", "gqa_decode_step",
     "gqa_decode_attn_multi", "gqa_decode_attn_paged", "gqa_decode_step_paged",
+    "kv_quantize_fp8", "kv_append_fp8", "gqa_decode_attn_fp8",
     "check_device_error", "get_plan",
     "set_tuning", "release", "KvAttnError", "library_path", "lib",
     "KVATTN_OK", "KVATTN_ERR_INVALID_ARG", "KVATTN_ERR_UNSUPPORTED",
@@ -71,6 +72,10 @@ _SIGS = {
     "gqa_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                      ctypes.c_float, _VP]),
     "kv_append_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "kv_quantize_fp8": (_I, [_VP, _VP, _VP, ctypes.c_longlong, _I, _VP]),
+    "kv_append_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    "gqa_decode_attn_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
+                                 ctypes.c_float, _VP]),
     "gqa_decode_attn_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
                                    _I, ctypes.c_float, _VP]),
     "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
@@ -386,6 +391,73 @@ def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens
                                        _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
                                        _ptr(out), B, Hq, Hkv, D, nblk, bs, maxb, float(scale),
                                        _stream_ptr(stream)))
+    return out
+
+
+def kv_quantize_fp8(src, codes=None, scales=None, stream=None):
+    """Quantize bf16 rows [..., D] into E4M3 codes (uint8 [..., D]) and one
+    fp32 scale per row ([...]): scale = absmax / 448, code = E4M3(x / scale).
+    Returns (codes, scales)."""
+    import torch
+    _need(src, "src", torch.bfloat16)
+    D = src.shape[-1]
+    rows = src.numel() // D if D else 0
+    if codes is None:
+        codes = torch.empty(tuple(src.shape), dtype=torch.uint8, device=src.device)
+    if scales is None:
+        scales = torch.empty(tuple(src.shape[:-1]), dtype=torch.float32, device=src.device)
+    _need(codes, "codes", torch.uint8, tuple(src.shape))
+    _need(scales, "scales", torch.float32, tuple(src.shape[:-1]))
+    _check(lib().kv_quantize_fp8(_ptr(src), _ptr(codes), _ptr(scales), rows, D,
+                                 _stream_ptr(stream)))
+    return codes, scales
+
+
+def kv_append_fp8(k_codes, v_codes, k_scale, v_scale, k_new, v_new, seq_lens, stream=None):
+    """Quantize the new token's K/V rows into position seq_lens[b] of an
+    8-bit cache (codes uint8 [B, Hkv, Lmax, D], scales fp32 [B, Hkv, Lmax];
+    k_new, v_new bf16 [B, Hkv, D])."""
+    import torch
+    _need(k_codes, "k_codes", torch.uint8)
+    if k_codes.dim() != 4:
+        raise ValueError("k_codes must be [B, Hkv, Lmax, D]")
+    B, Hkv, Lmax, D = k_codes.shape
+    _need(v_codes, "v_codes", torch.uint8, (B, Hkv, Lmax, D))
+    _need(k_scale, "k_scale", torch.float32, (B, Hkv, Lmax))
+    _need(v_scale, "v_scale", torch.float32, (B, Hkv, Lmax))
+    _need(k_new, "k_new", torch.bfloat16, (B, Hkv, D))
+    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    _check(lib().kv_append_fp8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+                               _ptr(k_new), _ptr(v_new), _ptr(seq_lens), B, Hkv, D, Lmax,
+                               _stream_ptr(stream)))
+
+
+def gqa_decode_attn_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale, out=None,
+                        stream=None):
+    """gqa_decode_attn over an 8-bit cache: K = E4M3(k_codes) * k_scale per
+    row, V likewise.  q bf16 [B, Hq, D]; codes uint8 [B, Hkv, Lmax, D];
+    scales fp32 [B, Hkv, Lmax]; seq_lens int32 [B]; out optional fp32
+    [B, Hq, D].  Returns out."""
+    import torch
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    B, Hq, D = q.shape
+    _need(k_codes, "k_codes", torch.uint8)
+    if k_codes.dim() != 4 or k_codes.shape[0] != B or k_codes.shape[3] != D:
+        raise ValueError("k_codes must be [B, Hkv, Lmax, D] matching q")
+    Hkv, Lmax = k_codes.shape[1], k_codes.shape[2]
+    _need(v_codes, "v_codes", torch.uint8, (B, Hkv, Lmax, D))
+    _need(k_scale, "k_scale", torch.float32, (B, Hkv, Lmax))
+    _need(v_scale, "v_scale", torch.float32, (B, Hkv, Lmax))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, (B, Hq, D))
+    _check(lib().gqa_decode_attn_fp8(_ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D,
+                                     Lmax, float(scale), _stream_ptr(stream)))
     return out
 
 

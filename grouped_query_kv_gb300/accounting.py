@@ -40,6 +40,12 @@ def kv_bytes_read(attn_lens, Hkv: int, D: int, elem_bytes: int = 2, window=None)
     return attended_positions(attn_lens, window) * Hkv * D * 2 * elem_bytes
 
 
+def kv_bytes_read_fp8(attn_lens, Hkv: int, D: int, window=None) -> int:
+    """The same for an 8-bit cache: one byte per element plus one fp32
+    scale per cached row, for K and for V."""
+    return attended_positions(attn_lens, window) * Hkv * 2 * (D + 4)
+
+
 def attn_flops(attn_lens, Hq: int, D: int, window=None) -> int:
     """Algorithmic FLOPs of one call: 2*D for q.k plus 2*D for p*v per query
     head and position."""

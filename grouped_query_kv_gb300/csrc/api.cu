@@ -155,6 +155,22 @@ int check_paged(const Paged &pg, int Hkv, const char *who, int *lg, int *Lmax) {
     return KVATTN_OK;
 }
 
+// 3-D map over an 8-bit cache [B*Hkv, Lmax, D] of one-byte codes: dims
+// (D, Lmax, B*Hkv), box (D, tile, 1), 128-byte swizzle (D = 128: one
+// 128-byte row per position).
+int encode_fp8_map(CUtensorMap *m, const void *base, int D, int Lmax, int BH, int tile) {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Lmax, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)D * (cuuint64_t)Lmax};
+    cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)tile, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVATTN_ERR_CUDA, "cuTensorMapEncodeTiled(fp8) failed (%d)", (int)r);
+    return KVATTN_OK;
+}
+
 struct Plan {
     kvattn_plan pub;
     int heads_per_seg;
@@ -523,6 +539,8 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     p.block_lg = lg;
     p.max_blocks = pg ? pg->max_blocks : 0;
     p.num_blocks = pg ? pg->num_blocks : 0;
+    p.k_scale = nullptr;
+    p.v_scale = nullptr;
 
     cudaError_t e;
     if (P.path == 2) {
@@ -538,6 +556,74 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         e = launch_decode_fma(tmk, tmv, p, P.num_ctas, P.smem_bytes, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    e = launch_combine(p, P.num_ctas, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    return KVATTN_OK;
+}
+
+// gqa_decode_attn over an 8-bit cache (decode_fp8.cu), D = 128.
+int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, const float *k_scale,
+                   const float *v_scale, const int32_t *seq_lens, float *out, int B, int Hq,
+                   int Hkv, int D, int Lmax, float scale, kvattn_stream_t stream_) {
+    const char *who = "gqa_decode_attn_fp8";
+    t_last_error[0] = 0;
+    if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !seq_lens || !out)
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: null pointer", who);
+    if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(KVATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned (scales 4)", who);
+    if (!std::isfinite(scale)) return fail(KVATTN_ERR_INVALID_ARG, "%s: scale must be finite", who);
+    int rc = check_sizes(B, Hq, Hkv, D, Lmax);
+    if (rc) return rc;
+    if (D != 128) return fail(KVATTN_ERR_UNSUPPORTED, "%s: an 8-bit cache needs D = 128 (D=%d)", who, D);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev;
+    if ((rc = current_device(&dev))) return rc;
+    DeviceState *ds;
+    Plan pl;
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if ((rc = device_state(dev, &ds))) return rc;
+        if ((rc = get_encoder())) return rc;
+        const int saved = g_force_path;
+        g_force_path = 2;  // the plan of the tensor-core kernel (heads per pass, grid)
+        rc = make_plan(B, Hq, Hkv, D, Lmax, ds->num_sms, &pl);
+        g_force_path = saved;
+        if (rc) return rc;
+        if ((rc = get_workspace(dev, stream, (size_t)pl.pub.workspace_bytes, &ws))) return rc;
+    }
+    const kvattn_plan &P = pl.pub;
+    CUtensorMap tmk, tmv;
+    if ((rc = encode_fp8_map(&tmk, k_codes, D, Lmax, B * Hkv, P.tile_positions))) return rc;
+    if ((rc = encode_fp8_map(&tmv, v_codes, D, Lmax, B * Hkv, P.tile_positions))) return rc;
+
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    p.q = static_cast<const uint16_t *>(q);
+    p.seq_lens = seq_lens;
+    p.len_add = 0;
+    p.out = out;
+    p.ws_o = static_cast<float *>(ws);
+    p.ws_ml = p.ws_o + (size_t)2 * P.num_ctas * pl.heads_per_seg * D;
+    p.split = reinterpret_cast<int *>(p.ws_ml + (size_t)2 * P.num_ctas * pl.heads_per_seg * 2);
+    p.err = ds->err;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.Lmax = Lmax;
+    p.G = Hq / Hkv;
+    p.heads_per_seg = pl.heads_per_seg;
+    p.head_groups = P.head_groups;
+    p.tile = P.tile_positions;
+    // a tile carries half the bytes of a bf16 tile; a piece's fixed work
+    // weighs twice as many tiles
+    p.cost_piece = 2 * pl.cost_piece;
+    p.window = Lmax;
+    p.T = 1;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    cudaError_t e = launch_decode_q8(tmk, tmv, p, pl.np, P.num_ctas, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fp8 decode kernel launch");
     e = launch_combine(p, P.num_ctas, stream);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     return KVATTN_OK;
@@ -611,6 +697,58 @@ int gqa_decode_step_paged(const void *q, const void *k_new, const void *v_new, v
     const Paged pg{block_table, block_size, max_blocks, num_blocks};
     return run_decode(q, k_pool, v_pool, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, 0, scale, 1,
                       stream, "gqa_decode_step_paged", 1, &pg);
+}
+
+int gqa_decode_attn_fp8(const void *q, const void *k_codes, const void *v_codes,
+                        const float *k_scale, const float *v_scale, const int32_t *seq_lens,
+                        float *out, int B, int Hq, int Hkv, int D, int Lmax, float scale,
+                        kvattn_stream_t stream) {
+    return run_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, out, B, Hq, Hkv, D,
+                          Lmax, scale, stream);
+}
+
+int kv_quantize_fp8(const void *src, void *codes, float *scales, long long rows, int D,
+                    kvattn_stream_t stream) {
+    t_last_error[0] = 0;
+    if (!src || !codes || !scales) return fail(KVATTN_ERR_INVALID_ARG, "kv_quantize_fp8: null pointer");
+    if (!aligned16(src) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+        return fail(KVATTN_ERR_INVALID_ARG, "kv_quantize_fp8: pointers must be 16-byte aligned (scales 4)");
+    if (rows < 0 || rows > (1LL << 40))
+        return fail(KVATTN_ERR_INVALID_ARG, "kv_quantize_fp8: rows out of range");
+    if (D != 64 && D != 128 && D != 256)
+        return fail(KVATTN_ERR_UNSUPPORTED, "kv_quantize_fp8: D=%d not in {64, 128, 256}", D);
+    if ((rows + 3) / 4 > 0x7fffffffLL)
+        return fail(KVATTN_ERR_UNSUPPORTED, "kv_quantize_fp8: too many rows for one launch");
+    cudaError_t e = launch_quantize_fp8(src, codes, scales, rows, D,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    return KVATTN_OK;
+}
+
+int kv_append_fp8(void *k_codes, void *v_codes, float *k_scale, float *v_scale,
+                  const void *k_new, const void *v_new, const int32_t *seq_lens, int B, int Hkv,
+                  int D, int Lmax, kvattn_stream_t stream) {
+    t_last_error[0] = 0;
+    if (!k_codes || !v_codes || !k_scale || !v_scale || !k_new || !v_new || !seq_lens)
+        return fail(KVATTN_ERR_INVALID_ARG, "kv_append_fp8: null pointer");
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_new) || !aligned16(v_new) ||
+        (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(KVATTN_ERR_INVALID_ARG, "kv_append_fp8: pointers must be 16-byte aligned (scales 4)");
+    int rc = check_sizes(B, Hkv, Hkv, D, Lmax);
+    if (rc) return rc;
+    int dev;
+    if ((rc = current_device(&dev))) return rc;
+    DeviceState *ds;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if ((rc = device_state(dev, &ds))) return rc;
+    }
+    cudaError_t e = launch_kv_append_fp8(k_codes, v_codes, k_scale, v_scale, k_new, v_new, seq_lens,
+                                         B, Hkv, D, Lmax, ds->err,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fp8 append launch");
+    return KVATTN_OK;
 }
 
 int kvattn_check_device_error(kvattn_stream_t stream) {

@@ -1,0 +1,682 @@
+// decode_fp8.cu -- split-KV decode attention over an 8-bit KV cache: FP8
+// E4M3 codes with one fp32 scale per cached row ("The Basics of Transformer
+// Inference", item "Quantization": an int8 / fp8 KV cache saves memory
+// bandwidth; "Machine Learning Engineering and AI Systems at Scale", section
+// "Quantization": E4M3 is the inference format).  Row j of a (b, kvh) block
+// stands for K[j, :] = e4m3(code[j, :]) * k_scale[j] (V likewise), so the
+// cache read per position is D + 4 bytes for K and as much for V instead of
+// 2 D.
+//
+// The same tiles, schedule, softmax and combine as the bf16 tensor-core
+// kernel (decode_tc.cuh), with three changes:
+//   * warp 0 brings each 128-position tile of codes (16 KB at D = 128) into
+//     a staging ring with one TMA box;
+//   * warps 6-7 widen each staged tile to f16 (every E4M3 value is exactly
+//     an f16 value: cvt.rn.f16x2.e4m3x2) into the 128-byte-swizzled layout
+//     of the MMA ring, and write the piece's q rows as f16;
+//   * the MMAs multiply f16 by f16 (fp32 accumulate); the softmax thread of
+//     position j scales its scores by k_scale[j] and its probability by
+//     v_scale[j] before writing P as f16 (11 significant bits, so P needs
+//     no hi/lo split here).
+// Limits: D = 128; q entries beyond the f16 range (|q| > 65504) saturate.
+#include <cuda_fp16.h>
+
+#include "decode_tc.cuh"
+
+namespace kvattn {
+
+namespace {
+
+constexpr int kQ8Threads = 256;  // warps 0-5 as in the bf16 kernel, 6-7 convert
+constexpr int kStage = 16384;    // one staged tile: 128 positions x 128 codes
+constexpr int kConvThreads = 64;
+
+template <int NP>
+struct Q8Cfg {
+    static constexpr int D = 128;
+    static constexpr int QB = (D / 64) * NP * 128;  // one f16 q buffer (swizzled, K-major)
+    static constexpr int PB = NP * kT * 2;          // one f16 P^T stage
+    static constexpr int PST = 2;
+    static constexpr int NBAR_MAX = 2 * 3 + 2 * 8 + 14;
+    static constexpr int FIXED = 2 * QB + PST * PB + 4 * 64 * 4 + 3 * 64 * 4 + 64 + 1024 +
+                                 NBAR_MAX * 8;
+    // MMA ring (f16 tiles): three slots when the staging ring still gets four
+    static constexpr int NB = (kSmemLimit - FIXED - 3 * kChunk) / kStage >= 4 ? 3 : 2;
+    static constexpr int NS_FIT = (kSmemLimit - FIXED - NB * kChunk) / kStage;
+    static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
+    static_assert(NS >= 2, "staging ring must hold two tiles");
+
+    static constexpr int off_ring = 0;
+    static constexpr int off_stage = NB * kChunk;
+    static constexpr int off_q = off_stage + NS * kStage;
+    static constexpr int off_p = off_q + 2 * QB;
+    static constexpr int off_red = off_p + PST * PB;      // float [4][64]
+    static constexpr int off_ltot = off_red + 4 * 64 * 4;
+    static constexpr int off_mref = off_ltot + 64 * 4;
+    static constexpr int off_alpha = off_mref + 64 * 4;
+    static constexpr int off_bar = off_alpha + 64 * 4;
+    static constexpr int nbar = 2 * NB + 2 * NS + 14;
+    static constexpr int off_misc = off_bar + nbar * 8;
+    static constexpr int bytes = off_misc + 64;
+    static constexpr int alloc = bytes + 1024;
+    static_assert(alloc <= kSmemLimit, "shared memory");
+
+    // TMEM: S0, S1 (NP columns each), then the O^T accumulator (NP columns)
+    static constexpr int TMEM_COLS = pow2_at_least(3 * NP);
+    static constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, true);
+};
+
+// Two E4M3 codes (low byte first) -> f16x2 (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+    return r;
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kQ8Threads, 1)
+    decode_q8_kernel(const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+    using C = Q8Cfg<NP>;
+    constexpr int D = 128;
+    constexpr int NB = C::NB;
+    constexpr int NS = C::NS;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ring = smem + C::off_ring;
+    uint8_t *stage = smem + C::off_stage;
+    uint8_t *qbuf = smem + C::off_q;
+    uint8_t *pbuf = smem + C::off_p;
+    float *red = reinterpret_cast<float *>(smem + C::off_red);
+    float *ltot_s = reinterpret_cast<float *>(smem + C::off_ltot);
+    float *mref_s = reinterpret_cast<float *>(smem + C::off_mref);
+    float *alpha_s = reinterpret_cast<float *>(smem + C::off_alpha);
+    uint64_t *bar_base = reinterpret_cast<uint64_t *>(smem + C::off_bar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::off_misc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::off_misc + 16);
+
+    // chunk_full/chunk_empty: the MMA ring (filled by the converters);
+    // st_full/st_empty: the staging ring (filled by TMA); q_full/q_empty:
+    // the f16 q buffers (filled by the converters)
+    uint64_t *chunk_full = bar_base, *chunk_empty = bar_base + NB;
+    uint64_t *st_full = bar_base + 2 * NB, *st_empty = st_full + NS;
+    uint64_t *q_full = st_empty + NS, *q_empty = q_full + 2;
+    uint64_t *s_full = q_empty + 2, *s_empty = s_full + 2;
+    uint64_t *p_full = s_empty + 2, *pv_done = p_full + 2;
+    uint64_t *o_free = pv_done + 2, *drain = o_free + 1;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int segs_per_b = p.Hkv * p.head_groups;
+
+    if (tid == 0) {
+        for (int s = 0; s < NB; ++s) {
+            mbar_init(&chunk_full[s], 2);  // one arrival per converter warp
+            mbar_init(&chunk_empty[s], 1);
+        }
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&st_full[s], 1);
+            mbar_init(&st_empty[s], 2);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 2);
+            mbar_init(&q_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_empty[s], 4);
+            mbar_init(&p_full[s], 4);
+            mbar_init(&pv_done[s], 1);
+        }
+        mbar_init(o_free, 4);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait_prior();
+    const LenView lens{p.seq_lens, p.len_add, p.window};
+    const SchedCost wcost{p.cost_piece};
+    const SchedStart st = warp_locate(lens, p.B, p.Lmax, kT, segs_per_b, wcost, blockIdx.x, gridDim.x);
+    if (warp == 2) sched_split_record(lens, p.B, p.Lmax, kT, segs_per_b, wcost, blockIdx.x, st, p.split);
+    if (!st.found) {
+        if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+        pdl_launch_dependents();
+        return;
+    }
+    const long long ntiles = st.g_end - st.g_begin;
+    const uint32_t ring_s = smem_u32(ring);
+    const uint32_t qbuf_s = smem_u32(qbuf);
+    const uint32_t pbuf_s = smem_u32(pbuf);
+
+    // ================================================================ producer
+    // Staging order follows the MMA ring: K_0, K_1, V_0, K_2, V_1, ...
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            TileIter itk, itv;
+            itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+            itv.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+            long long n = 0;
+            bool ok = true;
+            auto issue = [&](const void *tm, const TileIter &it) -> bool {
+                const int slot = (int)(n % NS);
+                if (n >= NS &&
+                    !wait_bar(&st_empty[slot], (uint32_t)(((n / NS) - 1) & 1), abort_flag))
+                    return false;
+                mbar_arrive_expect_tx(&st_full[slot], kStage);
+                const int z = it.b * p.Hkv + it.seg / p.head_groups;
+                tma_load_3d(stage + slot * kStage, tm, &st_full[slot], 0, it.row0(), z, pol);
+                ++n;
+                return true;
+            };
+            for (long long r = 0; r <= ntiles && ok; ++r) {
+                if (r < ntiles) {
+                    ok = issue(&tmk, itk);
+                    itk.next();
+                }
+                if (r >= 1 && ok) {
+                    ok = issue(&tmv, itv);
+                    itv.next();
+                }
+            }
+            if (!ok) {
+                set_error(p.err, DEV_ERR_TIMEOUT);
+                *abort_flag = 1;
+                const long long first = n > NS ? n - NS : 0;
+                for (long long k = first; k < n; ++k) {
+                    volatile int never = 0;
+                    wait_bar(&st_full[k % NS], (uint32_t)((k / NS) & 1), &never);
+                }
+            }
+        }
+        __syncwarp();
+        pdl_launch_dependents();
+        return;
+    }
+
+    // ============================================================ converters
+    if (warp >= 6) {
+        const int ct = tid - 192;  // 0 .. 63
+        TileIter itk;
+        itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+        long long n = 0;
+        int piece = 0;
+        bool ok = true;
+        // wait on a barrier with lane 0, the whole warp learning the outcome
+        auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+            bool w = true;
+            if (lane == 0) w = wait_bar(bar, parity, abort_flag);
+            return __shfl_sync(0xffffffffu, w, 0);
+        };
+        // staged chunk n -> MMA ring slot n % NB
+        auto convert = [&]() -> bool {
+            const int ss = (int)(n % NS), fs = (int)(n % NB);
+            if (!wwait(&st_full[ss], (uint32_t)((n / NS) & 1))) return false;
+            if (n >= NB && !wwait(&chunk_empty[fs], (uint32_t)(((n / NB) - 1) & 1))) return false;
+            // thread ct converts column block k = ct mod 8 of rows ct / 8 + 8 i:
+            // the swizzle (row mod 8 is the same for all its rows) fixes its
+            // offsets, and its rows are 1 KB apart in both layouts
+            const int k = ct & 7, rr = (ct >> 3) & 7;
+            const uint8_t *srcp = stage + ss * kStage + (ct >> 3) * 128 + ((k ^ rr) << 4);
+            // codes 16k .. 16k+15 -> f16 columns 16k .. 16k+15: 64-column half
+            // k / 4, 16-byte pieces 2 (k mod 4) and 2 (k mod 4) + 1
+            uint8_t *dstp = ring + fs * kChunk + (k >> 2) * 16384 + (ct >> 3) * 128;
+            const int o0 = ((2 * (k & 3)) ^ rr) << 4, o1 = ((2 * (k & 3) + 1) ^ rr) << 4;
+#pragma unroll
+            for (int i = 0; i < kStage / 16 / kConvThreads; ++i) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(srcp + i * 1024);
+                uint4 a, c;
+                a.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xFFFF));
+                a.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
+                a.z = e4m3x2_to_f16x2((uint16_t)(w.y & 0xFFFF));
+                a.w = e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
+                c.x = e4m3x2_to_f16x2((uint16_t)(w.z & 0xFFFF));
+                c.y = e4m3x2_to_f16x2((uint16_t)(w.z >> 16));
+                c.z = e4m3x2_to_f16x2((uint16_t)(w.w & 0xFFFF));
+                c.w = e4m3x2_to_f16x2((uint16_t)(w.w >> 16));
+                *reinterpret_cast<uint4 *>(dstp + i * 1024 + o0) = a;
+                *reinterpret_cast<uint4 *>(dstp + i * 1024 + o1) = c;
+            }
+            // the MMA reads the ring through the async proxy; TMA then
+            // refills the staging slot
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&chunk_full[fs]);
+                mbar_arrive(&st_empty[ss]);
+            }
+            ++n;
+            return true;
+        };
+        // the piece's q rows, bf16 -> f16, into the swizzled K-major layout
+        auto load_q = [&](const TileIter &it) -> bool {
+            const int qs = piece & 1;
+            if (piece >= 2 && !wwait(&q_empty[qs], (uint32_t)(((piece >> 1) - 1) & 1)))
+                return false;
+            const int kvh = it.seg / p.head_groups, hg = it.seg % p.head_groups;
+            const int h0 = kvh * p.G + hg * p.heads_per_seg;
+            const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
+            const uint4 *qg = reinterpret_cast<const uint4 *>(p.q);
+            for (int e = ct; e < NP * (D / 8); e += kConvThreads) {
+                const int g = e / (D / 8), c8 = e % (D / 8);  // head row, 8-column piece
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (g < gvalid) {
+                    const uint4 raw = qg[((size_t)it.b * p.Hq + h0 + g) * (D / 8) + c8];
+                    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+                    uint32_t outw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float lo = __uint_as_float(in[u] << 16);
+                        float hi = __uint_as_float(in[u] & 0xFFFF0000u);
+                        lo = fminf(fmaxf(lo, -65504.f), 65504.f);
+                        hi = fminf(fmaxf(hi, -65504.f), 65504.f);
+                        const __half2 h2 = __floats2half2_rn(lo, hi);
+                        outw[u] = *reinterpret_cast<const uint32_t *>(&h2);
+                    }
+                    v = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+                }
+                const int half = c8 >> 3, j = c8 & 7;
+                *reinterpret_cast<uint4 *>(qbuf + qs * C::QB + half * NP * 128 + g * 128 +
+                                           ((j ^ (g & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_full[qs]);
+            ++piece;
+            return true;
+        };
+        for (long long r = 0; r <= ntiles && ok; ++r) {
+            if (r < ntiles) {
+                if (r == 0 || itk.t == 0) ok = load_q(itk);
+                if (ok) ok = convert();
+                itk.next();
+            }
+            if (r >= 1 && ok) ok = convert();
+        }
+        if (!ok && lane == 0) {
+            set_error(p.err, DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        return;
+    }
+
+    // ================================================================== MMA
+    if (warp == 1) {
+        if (lane == 0) {
+            TileIter itq, itp;
+            itq.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+            itp.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+            long long iq = 0, ip = 0;
+            int piece_q = 0, piece_pv = 0, qcur = 0;
+            uint32_t idle = 0;
+            bool ok = true;
+            while (ip < ntiles) {
+                bool did = false;
+                if (ip < iq) {  // PV of tile ip
+                    const long long j = ip;
+                    const int pb = (int)(j & 1);
+                    const bool first_pv = (j == 0) || (itp.t == 0);
+                    bool ready = mbar_test(&p_full[pb], (uint32_t)((j >> 1) & 1));
+                    if (ready && first_pv && piece_pv > 0)
+                        ready = mbar_test(o_free, (uint32_t)((piece_pv - 1) & 1));
+                    const long long idx = v_chunk<1>(j, 0, ntiles);
+                    if (ready) ready = mbar_test(&chunk_full[idx % NB], (uint32_t)((idx / NB) & 1));
+                    if (ready) {
+                        if (first_pv) ++piece_pv;
+                        tc_fence_after();
+                        const uint32_t pstage = pbuf_s + (int)(j % C::PST) * C::PB;
+                        const int slot = (int)(idx % NB);
+                        const uint32_t v0 = ring_s + slot * kChunk;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t ad = smem_desc(v0 + kk * 2048, 16384, 1024, 2);
+                            const uint64_t bd = smem_desc(pstage + kk * 256, 128, (kT / 8) * 128, 0);
+                            umma_bf16(tmem + 2 * NP, ad, bd, C::IDESC_PV, !(first_pv && kk == 0));
+                        }
+                        umma_commit(&chunk_empty[slot]);
+                        umma_commit(&pv_done[pb]);
+                        if (j < ntiles - 1) itp.next();
+                        ++ip;
+                        did = true;
+                    }
+                }
+                if (iq < ntiles) {  // QK of tile iq
+                    const long long i = iq;
+                    const int sb = (int)(i & 1);
+                    const bool first_q = (i == 0) || (itq.t == 0);
+                    bool ready = true;
+                    if (first_q) ready = mbar_test(&q_full[piece_q & 1], (uint32_t)((piece_q >> 1) & 1));
+                    if (ready && i >= 2) ready = mbar_test(&s_empty[sb], (uint32_t)(((i >> 1) - 1) & 1));
+                    const long long idx = k_chunk<1>(i, 0);
+                    if (ready && idx >= NB) {
+                        long long vt;
+                        if (chunk_is_v<1>(idx - NB, ntiles, &vt) && vt >= ip) ready = false;
+                    }
+                    if (ready) ready = mbar_test(&chunk_full[idx % NB], (uint32_t)((idx / NB) & 1));
+                    if (ready) {
+                        if (first_q) {
+                            qcur = piece_q & 1;
+                            ++piece_q;
+                        }
+                        tc_fence_after();
+                        const int slot = (int)(idx % NB);
+                        const uint32_t a0 = ring_s + slot * kChunk;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t ad =
+                                smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
+                            const uint64_t bd = smem_desc(
+                                qbuf_s + qcur * C::QB + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16,
+                                1024, 2);
+                            umma_bf16(tmem + sb * NP, ad, bd, C::IDESC_QK, kk != 0);
+                        }
+                        umma_commit(&chunk_empty[slot]);
+                        umma_commit(&s_full[sb]);
+                        if (itq.last_tile_of_segment() || i == ntiles - 1) umma_commit(&q_empty[qcur]);
+                        if (i < ntiles - 1) itq.next();
+                        ++iq;
+                        did = true;
+                    }
+                }
+                if (did) {
+                    idle = 0;
+                    continue;
+                }
+                ++idle;
+                if ((idle & 255u) == 0 && *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (idle >= kMmaIdleLimit) {
+                    ok = false;
+                    *abort_flag = 1;
+                    break;
+                }
+                if (idle > 16) __nanosleep(64);
+            }
+            if (!ok) {
+                set_error(p.err, DEV_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            umma_commit(drain);
+            volatile int never = 0;
+            wait_bar(drain, 0, &never);
+        }
+        __syncwarp();
+        named_bar_sync(kBarEnd, 160);
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+        return;
+    }
+
+    // ============================================================== softmax
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+
+    TileIter it;
+    it.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+    long long i = 0;
+    bool first_piece = true;
+    bool aborted = false;
+    bool carry_fail = false;
+    float l[NP];
+
+    while (i < ntiles && !aborted) {
+        const int b = it.b;
+        const int kvh = it.seg / p.head_groups;
+        const int hg = it.seg % p.head_groups;
+        const int len = seq_valid_len(it.len, p.Lmax);
+        const int t0 = it.t;
+        if (row == 0 && q4 == 0 && t0 == 0 && (it.len < 0 || it.len > p.Lmax))
+            set_error(p.err, DEV_ERR_BOUNDS);
+        const int h0 = kvh * p.G + hg * p.heads_per_seg;
+        const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
+        const size_t zrow = ((size_t)b * p.Hkv + kvh) * p.Lmax;  // first scale of this block
+        const long long i0 = i;
+#pragma unroll
+        for (int g = 0; g < NP; ++g) l[g] = 0.f;
+        if (row < NP) mref_s[row] = -INFINITY;
+        named_bar_sync(kBarSoftmax, 128);
+
+        while (true) {
+            const int sb = (int)(i & 1);
+            const int r0 = it.row0();
+            const int pos = r0 + row;
+            const bool valid = row >= it.first_pos() - r0 && pos < len;
+            // this row's scales, loaded while the scores are made
+            float ksc = 0.f, vsc = 0.f;
+            if (valid) {
+                ksc = p.k_scale[zrow + pos];
+                vsc = p.v_scale[zrow + pos];
+            }
+            bool fail = carry_fail || !wait_bar(&s_full[sb], (uint32_t)((i >> 1) & 1), abort_flag);
+            tc_fence_after();
+            float s[NP];
+#pragma unroll
+            for (int c = 0; c < NP / 16; ++c) {
+                float v[16];
+                tmem_ld16(lane_base + sb * NP + c * 16, v);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) s[c * 16 + k] = v[k];
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[sb]);
+
+            const float sl = p.scale_log2 * ksc;
+            bool over = false;
+#pragma unroll
+            for (int g = 0; g < NP; g += 4) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g);
+                s[g] = valid ? s[g] * sl : -INFINITY;
+                s[g + 1] = valid ? s[g + 1] * sl : -INFINITY;
+                s[g + 2] = valid ? s[g + 2] * sl : -INFINITY;
+                s[g + 3] = valid ? s[g + 3] * sl : -INFINITY;
+                over |= (s[g] > m4.x + kTau) | (s[g + 1] > m4.y + kTau) |
+                        (s[g + 2] > m4.z + kTau) | (s[g + 3] > m4.w + kTau);
+            }
+            if (named_bar_sync_or(kBarSoftmax, 128, over || fail)) {
+                if (named_bar_sync_or(kBarSoftmax, 128, fail || *abort_flag != 0)) {
+                    aborted = true;
+                    break;
+                }
+#pragma unroll
+                for (int g = 0; g < NP; ++g) {
+                    const float mx = warp_max(s[g]);
+                    if (lane == 0) red[q4 * 64 + g] = mx;
+                }
+                named_bar_sync(kBarSoftmax, 128);
+                if (row < NP) {
+                    const int g = row;
+                    const float tmax = fmaxf(fmaxf(red[g], red[64 + g]),
+                                             fmaxf(red[128 + g], red[192 + g]));
+                    const float m_old = mref_s[g];
+                    const float m_new = fmaxf(m_old, tmax);
+                    alpha_s[g] = (m_new == -INFINITY || m_old == m_new) ? 1.f
+                                                                         : fast_exp2(m_old - m_new);
+                    mref_s[g] = m_new;
+                }
+                named_bar_sync(kBarSoftmax, 128);
+#pragma unroll
+                for (int g = 0; g < NP; ++g) l[g] *= alpha_s[g];
+                if (i > i0) {
+                    const long long j = i - 1;
+                    if (!wait_bar(&pv_done[j & 1], (uint32_t)((j >> 1) & 1), abort_flag))
+                        fail = true;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < NP / 16; ++c) {
+                        float v[16];
+                        const uint32_t a = lane_base + 2 * NP + c * 16;
+                        tmem_ld16(a, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) v[k] *= alpha_s[c * 16 + k];
+                        tmem_st16(a, v);
+                    }
+                    tmem_st_wait();
+                }
+            }
+
+            // probabilities p (summed into l) times the row's V scale, as f16
+            uint32_t pk[NP / 2];
+#pragma unroll
+            for (int g4 = 0; g4 < NP; g4 += 4) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g4);
+                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int h = 0; h < 4; h += 2) {
+                    const int g = g4 + h;
+                    const float p0 = (s[g] == -INFINITY) ? 0.f : fast_exp2(s[g] - mm[h]);
+                    const float p1 = (s[g + 1] == -INFINITY) ? 0.f : fast_exp2(s[g + 1] - mm[h + 1]);
+                    l[g] += p0;
+                    l[g + 1] += p1;
+                    const __half2 h2 = __floats2half2_rn(p0 * vsc, p1 * vsc);
+                    pk[g / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
+            }
+            if (i >= C::PST) {
+                const long long jp = i - C::PST;
+                if (!wait_bar(&pv_done[jp & 1], (uint32_t)((jp >> 1) & 1), abort_flag))
+                    fail = true;
+            }
+            uint8_t *pdst = pbuf + (int)(i % C::PST) * C::PB + (row >> 3) * 128 + (row & 7) * 16;
+#pragma unroll
+            for (int c = 0; c < NP / 8; ++c)
+                *reinterpret_cast<uint4 *>(pdst + c * (kT / 8) * 128) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+            carry_fail = fail;
+
+            ++i;
+            if (it.last_tile_of_segment() || i == ntiles) break;
+            it.next();
+        }
+        if (aborted) break;
+
+        // ---- piece end
+        const long long e = i - 1;
+        bool fail = carry_fail || !wait_bar(&pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag);
+        carry_fail = false;
+        tc_fence_after();
+#pragma unroll
+        for (int g = 0; g < NP; ++g) {
+            const float ls = warp_sumf(l[g]);
+            if (lane == 0) red[q4 * 64 + g] = ls;
+        }
+        named_bar_sync(kBarSoftmax, 128);
+        if (row < NP) ltot_s[row] = red[row] + red[64 + row] + red[128 + row] + red[192 + row];
+        named_bar_sync(kBarSoftmax, 128);
+        const bool complete = (t0 == 0) && it.last_tile_of_segment();
+        const size_t slot = 2 * (size_t)blockIdx.x + (first_piece ? 0 : 1);
+        float o[NP];
+#pragma unroll
+        for (int c = 0; c < NP / 16; ++c) {
+            float v[16];
+            tmem_ld16(lane_base + 2 * NP + c * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[c * 16 + k] = v[k];
+        }
+        const int d = row;
+        if (complete) {
+#pragma unroll
+            for (int g = 0; g < NP; ++g) {
+                if (g < gvalid) {
+                    const float lt = ltot_s[g];
+                    p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (lt > 0.f) ? o[g] / lt : 0.f;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < NP; ++g)
+                if (g < gvalid) p.ws_o[(slot * p.heads_per_seg + g) * D + d] = o[g];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+        if (!complete && row < gvalid) {
+            p.ws_ml[(slot * p.heads_per_seg + row) * 2 + 0] = mref_s[row];
+            p.ws_ml[(slot * p.heads_per_seg + row) * 2 + 1] = ltot_s[row];
+        }
+        first_piece = false;
+        if (named_bar_sync_or(kBarSoftmax, 128, fail)) {
+            *abort_flag = 1;
+            aborted = true;
+            break;
+        }
+        if (i < ntiles) it.next();
+    }
+    if (aborted) set_error(p.err, DEV_ERR_TIMEOUT);
+    tc_fence_before();
+    named_bar_sync(kBarEnd, 160);
+}
+
+template <int NP>
+cudaError_t launch_q8(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeParams &p,
+                      int num_ctas, cudaStream_t stream) {
+    static int done_for_device[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!(dev >= 0 && dev < 64 && done_for_device[dev])) {
+        e = cudaFuncSetAttribute(decode_q8_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Q8Cfg<NP>::alloc);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) done_for_device[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_ctas);
+    cfg.blockDim = dim3(kQ8Threads);
+    cfg.dynamicSmemBytes = Q8Cfg<NP>::alloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_q8_kernel<NP>, tmk, tmv, p);
+}
+
+}  // namespace
+
+int q8_smem_bytes(int np) {
+    switch (np) {
+        case 16: return Q8Cfg<16>::alloc;
+        case 32: return Q8Cfg<32>::alloc;
+        case 48: return Q8Cfg<48>::alloc;
+        case 64: return Q8Cfg<64>::alloc;
+        default: return -1;
+    }
+}
+
+cudaError_t launch_decode_q8(const CUtensorMap &tmk, const CUtensorMap &tmv,
+                             const DecodeParams &p, int np, int num_ctas, cudaStream_t stream) {
+    switch (np) {
+        case 16: return launch_q8<16>(tmk, tmv, p, num_ctas, stream);
+        case 32: return launch_q8<32>(tmk, tmv, p, num_ctas, stream);
+        case 48: return launch_q8<48>(tmk, tmv, p, num_ctas, stream);
+        case 64: return launch_q8<64>(tmk, tmv, p, num_ctas, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace kvattn

@@ -56,6 +56,10 @@ struct DecodeParams {
     int block_lg;
     int max_blocks;
     int num_blocks;
+    // 8-bit cache (decode_fp8.cu): one fp32 scale per cached row,
+    // [B, Hkv, Lmax] for K and for V; null otherwise
+    const float *k_scale;
+    const float *v_scale;
 };
 
 // Host launchers (return cudaError_t of the launch).
@@ -97,6 +101,18 @@ cudaError_t launch_decode_tc_paged(const CUtensorMap &tmk, const CUtensorMap &tm
                                    int num_ctas, cudaStream_t stream);
 
 cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream);
+
+// 8-bit (FP8 E4M3) cache: the attention kernel (D = 128; np as tc_np), the
+// row quantizer and the append.
+int q8_smem_bytes(int np);
+cudaError_t launch_decode_q8(const CUtensorMap &tmk, const CUtensorMap &tmv,
+                             const DecodeParams &p, int np, int num_ctas, cudaStream_t stream);
+cudaError_t launch_quantize_fp8(const void *src, void *codes, float *scales, long long rows,
+                                int D, cudaStream_t stream);
+cudaError_t launch_kv_append_fp8(void *k_codes, void *v_codes, float *k_scale, float *v_scale,
+                                 const void *k_new, const void *v_new, const int32_t *seq_lens,
+                                 int B, int Hkv, int D, int Lmax, unsigned int *err,
+                                 cudaStream_t stream);
 
 // Shared with the allocation-free entry point (defined in api.cu).
 int api_fail(int status, const char *msg);

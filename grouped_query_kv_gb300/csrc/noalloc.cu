@@ -134,6 +134,8 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
     p.block_lg = 0;
     p.max_blocks = 0;
     p.num_blocks = 0;
+    p.k_scale = nullptr;
+    p.v_scale = nullptr;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

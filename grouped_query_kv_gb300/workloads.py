@@ -49,6 +49,8 @@ class Workload:
     # a paged cache: positions grouped in blocks of `block_size` in a shared
     # pool, reached through a per-sequence block table; None: contiguous
     block_size: Optional[int] = None
+    # "fp8": an 8-bit cache (E4M3 codes, one fp32 scale per row); "bf16" else
+    kv_dtype: str = "bf16"
     note: str = ""
 
     @property
@@ -93,6 +95,10 @@ WORKLOADS = {w.name: w for w in [
              scale=1.0 / math.sqrt(128), ragged=True, block_size=16,
              note="Llama-70B-shaped GQA decode over a paged cache: 16-position "
                   "blocks scattered through one pool, lengths uniform in [1, 8192]"),
+    Workload("llama70b_fp8", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
+             scale=1.0 / math.sqrt(128), ragged=True, kv_dtype="fp8",
+             note="Llama-70B-shaped GQA decode over an 8-bit (E4M3 + per-row scale) "
+                  "cache, lengths uniform in [1, 8192]"),
     Workload("llama70b_paged64", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
              scale=1.0 / math.sqrt(128), ragged=True, block_size=64,
              note="the same over 64-position blocks"),

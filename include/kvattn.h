@@ -285,6 +285,51 @@ KVATTN_API int gqa_decode_step_paged(const void *q, const void *k_new, const voi
                                      int max_blocks, float scale, kvattn_stream_t stream);
 
 /*
+ * 8-bit KV cache (FP8 E4M3 codes with one fp32 scale per cached row).
+ * Quantizing the KV cache to int8 / fp8 saves memory bandwidth and capacity
+ * ("The Basics of Transformer Inference", item "Quantization"; "Machine
+ * Learning Engineering and AI Systems at Scale", section "Quantization":
+ * E4M3 is the inference format, the KV cache is the second thing to
+ * quantize).  The pages give no rule; this library's: each cached row (one
+ * position of one K/V head, D values) is stored as
+ *     scale  = absmax(row) / 448          (1 for an all-zero row)
+ *     code_d = E4M3(row_d / scale)        nearest, ties to even, saturating
+ * with both divisions in IEEE binary32, and read as code value x scale.
+ * E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals, no
+ * infinities, largest finite 448 (the OCP 8-bit format).  Rows must be
+ * finite.
+ *
+ *   codes  : uint8 [B, Hkv, Lmax, D] (K and V separately)
+ *   scales : fp32  [B, Hkv, Lmax]    (K and V separately)
+ */
+
+/* kv_quantize_fp8 -- quantize `rows` rows of D bf16 values (src [rows, D])
+ * into codes [rows, D] and scales [rows] by the rule above: e.g. a whole
+ * prefilled bf16 cache viewed as B*Hkv*Lmax rows.  D in {64, 128, 256}.
+ * Bit-exact. */
+KVATTN_API int kv_quantize_fp8(const void *src, void *codes, float *scales, long long rows,
+                               int D, kvattn_stream_t stream);
+
+/* kv_append_fp8 -- kv_append into an 8-bit cache: the new token's K and V
+ * rows (bf16 [B, Hkv, D]) are quantized into position seq_lens[b], codes and
+ * scale.  Errors as for kv_append.  Bit-exact. */
+KVATTN_API int kv_append_fp8(void *k_codes, void *v_codes, float *k_scale, float *v_scale,
+                             const void *k_new, const void *v_new, const int32_t *seq_lens,
+                             int B, int Hkv, int D, int Lmax, kvattn_stream_t stream);
+
+/* gqa_decode_attn_fp8 -- gqa_decode_attn over an 8-bit cache: K[b,kvh,j,:] =
+ * E4M3(k_codes[b,kvh,j,:]) * k_scale[b,kvh,j], V likewise.  The cache read
+ * per position and K/V head is 2 (D + 4) bytes instead of 4 D.  q bf16
+ * [B, Hq, D] (entries beyond +-65504 saturate: the products run in f16),
+ * out fp32 [B, Hq, D]; lengths, errors and ownership as gqa_decode_attn.
+ * Needs D = 128 (KVATTN_ERR_UNSUPPORTED otherwise).  Rows at and past
+ * seq_lens[b], codes and scales, are never read. */
+KVATTN_API int gqa_decode_attn_fp8(const void *q, const void *k_codes, const void *v_codes,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
+                                   int D, int Lmax, float scale, kvattn_stream_t stream);
+
+/*
  * gqa_decode_attn_noalloc -- the same computation as gqa_decode_attn, for
  * callers that must not have the library allocate device memory (for
  * example a server that gives all free GPU memory to its own pool at
