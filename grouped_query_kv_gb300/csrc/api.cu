@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <vector>
 #include <mutex>
 #include <utility>
 
@@ -50,6 +51,9 @@ std::map<int, DeviceState> g_dev;
 struct Workspace {
     void *ptr = nullptr;
     size_t bytes = 0;
+    // buffers outgrown by this one: kept until kvattn_release, because work
+    // captured earlier (a CUDA graph) may still use them
+    std::vector<void *> retired;
 };
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
@@ -279,19 +283,17 @@ int check_sizes(int B, int Hq, int Hkv, int D, int Lmax) {
 int get_workspace(int dev, cudaStream_t stream, size_t bytes, void **ptr) {
     Workspace &w = g_ws[std::make_pair(dev, stream)];
     if (w.bytes < bytes) {
-        if (w.ptr) {
-            cudaError_t e = cudaFree(w.ptr);  // synchronises the device first
-            w.ptr = nullptr;
-            w.bytes = 0;
-            if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
-        }
+        // grow at least twofold; the old buffer is retired, not freed
         size_t want = bytes < (1u << 20) ? (1u << 20) : bytes;
-        cudaError_t e = cudaMalloc(&w.ptr, want);
+        if (want < 2 * w.bytes) want = 2 * w.bytes;
+        void *fresh = nullptr;
+        cudaError_t e = cudaMalloc(&fresh, want);
         if (e != cudaSuccess) {
-            w.ptr = nullptr;
             (void)cudaGetLastError();
             return fail(KVATTN_ERR_OOM, "workspace allocation of %zu bytes failed", want);
         }
+        if (w.ptr) w.retired.push_back(w.ptr);
+        w.ptr = fresh;
         w.bytes = want;
     }
     *ptr = w.ptr;
@@ -772,10 +774,9 @@ void kvattn_release(void) {
     int cur = 0;
     cudaGetDevice(&cur);
     for (auto &kv : g_ws) {
-        if (kv.second.ptr) {
-            cudaSetDevice(kv.first.first);
-            cudaFree(kv.second.ptr);
-        }
+        cudaSetDevice(kv.first.first);
+        if (kv.second.ptr) cudaFree(kv.second.ptr);
+        for (void *old : kv.second.retired) cudaFree(old);
     }
     g_ws.clear();
     cudaSetDevice(cur);

@@ -34,7 +34,8 @@
  *    (device, stream) pair, or a call needing a larger workspace than any
  *    before on that pair, allocates device memory (cudaMalloc; it may
  *    serialise with other device work).  Make such a first call before
- *    capturing a stream into a CUDA graph.
+ *    capturing a stream into a CUDA graph.  An outgrown workspace is not
+ *    freed until kvattn_release(), so graphs captured with it stay valid.
  *  - Host-detected errors return a non-zero kvattn_status and launch nothing;
  *    kvattn_last_error() then gives a one-line reason (thread-local).
  *  - Device-detected errors (a length outside the cache) never fault or trap:

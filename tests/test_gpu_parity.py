@@ -522,3 +522,39 @@ def test_appending_rows_that_do_not_fit_is_flagged_and_skipped():
     with pytest.raises(g.KvAttnError):
         g.check_device_error()
     assert torch.all(k[1] == 0) and torch.all(k[0, :, 10:14] == 1)
+
+
+def test_graph_captured_before_the_workspace_grows_stays_valid():
+    # a call that needs a larger workspace retires the old buffer instead of
+    # freeing it, so a graph captured with the old one still replays
+    dev = torch.device("cuda")
+    w = wl.Workload("grow", B=6, Hq=16, Hkv=2, D=128, Lmax=1500, scale=0.1,
+                    lens=(1500, 3, 700, 1200, 129, 64))
+    x = wl.make_inputs(w, seed=21, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    try:
+        g.set_tuning(0, 7)
+        with torch.cuda.stream(s):
+            g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale,
+                              out=out, stream=s)
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale,
+                              out=out, stream=s)
+        g.set_tuning(0, 3000)  # needs a much larger workspace on the same stream
+        with torch.cuda.stream(s):
+            g.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale,
+                              out=torch.empty_like(out), stream=s)
+        s.synchronize()
+        out.zero_()
+        with torch.cuda.stream(s):
+            graph.replay()
+        s.synchronize()
+    finally:
+        g.set_tuning(0, 0)
+    g.check_device_error()
+    ref = oracle.gqa_decode(bits(x["q"]), bits(x["k_cache"]), bits(x["v_cache"]),
+                            x["attn_lens"].cpu().numpy(), w.scale)
+    assert_close(out, ref, bits(x["v_cache"]), list(w.lens))
