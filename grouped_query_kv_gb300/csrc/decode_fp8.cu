@@ -495,11 +495,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                     aborted = true;
                     break;
                 }
-#pragma unroll
-                for (int g = 0; g < NP; ++g) {
-                    const float mx = warp_max(s[g]);
-                    if (lane == 0) red[q4 * 64 + g] = mx;
-                }
+                warp_cols_np<NP>(s, red + q4 * 64, lane, OpMax());
                 named_bar_sync(kBarSoftmax, 128);
                 if (row < NP) {
                     const int g = row;
@@ -577,11 +573,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         bool fail = carry_fail || !wait_bar(&pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag);
         carry_fail = false;
         tc_fence_after();
-#pragma unroll
-        for (int g = 0; g < NP; ++g) {
-            const float ls = warp_sumf(l[g]);
-            if (lane == 0) red[q4 * 64 + g] = ls;
-        }
+        warp_cols_np<NP>(l, red + q4 * 64, lane, OpSum());
         named_bar_sync(kBarSoftmax, 128);
         if (row < NP) ltot_s[row] = red[row] + red[64 + row] + red[128 + row] + red[192 + row];
         named_bar_sync(kBarSoftmax, 128);

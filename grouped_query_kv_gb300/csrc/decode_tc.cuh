@@ -123,6 +123,56 @@ __device__ __forceinline__ float warp_sumf(float v) {
     return v;
 }
 
+struct OpMax {
+    __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct OpSum {
+    __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+};
+
+// Totals over the warp's 32 lanes of N columns (N = 16 or 32), column c's
+// total stored to out[c]: a reduce-scatter in which each butterfly step
+// keeps half of a lane's columns and adds its partner's copy of them, so N/2
+// + N/4 + ... shuffles instead of 5 per column.  For N = 16 two lanes end
+// with each column (both store it).  (Compile-time steps: every index is a
+// constant, so the columns stay in registers.)
+template <int M, int O, class Op>
+__device__ __forceinline__ void warp_cols_step(float (&a)[32], int lane, int &col, Op op) {
+    if constexpr (M > 1) {
+        constexpr int H = M / 2;
+        const bool up = (lane & O) != 0;  // keeps the upper half of its columns
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+            const float keep = up ? a[i + H] : a[i];
+            const float send = up ? a[i] : a[i + H];
+            a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, O));
+        }
+        if (up) col += H;
+        if constexpr (O > 1) warp_cols_step<H, O / 2>(a, lane, col, op);
+    } else {
+        a[0] = op(a[0], __shfl_xor_sync(0xffffffffu, a[0], O));
+        if constexpr (O > 1) warp_cols_step<1, O / 2>(a, lane, col, op);
+    }
+}
+
+template <int N, class Op>
+__device__ __forceinline__ void warp_cols(const float *v, float *out, int lane, Op op) {
+    float a[32];
+#pragma unroll
+    for (int i = 0; i < N; ++i) a[i] = v[i];
+    int col = 0;
+    warp_cols_step<N, 16>(a, lane, col, op);
+    out[col] = a[0];
+}
+
+// NP columns (a multiple of 16) in blocks of 32 and 16.
+template <int NP, class Op>
+__device__ __forceinline__ void warp_cols_np(const float (&v)[NP], float *out, int lane, Op op) {
+#pragma unroll
+    for (int c0 = 0; c0 + 32 <= NP; c0 += 32) warp_cols<32>(v + c0, out + c0, lane, op);
+    if (NP % 32 == 16) warp_cols<16>(v + NP - 16, out + NP - 16, lane, op);
+}
+
 // Ring order of the K/V chunks of a CTA's n tiles (KCH chunks per tile each):
 //     K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}
 // V_i goes in behind K_{i+1}: it is needed only after tile i's scores and
@@ -650,11 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 // exact tile max per head, then move the running max
-#pragma unroll
-                for (int g = 0; g < NP; ++g) {
-                    const float mx = warp_max(s[g]);
-                    if (lane == 0) red[q4 * 64 + g] = mx;
-                }
+                warp_cols_np<NP>(s, red + q4 * 64, lane, OpMax());
                 named_bar_sync(kBarSoftmax, 128);
                 if (row < NP) {
                     const int g = row;
@@ -745,11 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool fail = carry_fail || !wait_bar(&bs.pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag);
         carry_fail = false;
         tc_fence_after();
-#pragma unroll
-        for (int g = 0; g < NP; ++g) {
-            const float ls = warp_sumf(l[g]);
-            if (lane == 0) red[q4 * 64 + g] = ls;
-        }
+        warp_cols_np<NP>(l, red + q4 * 64, lane, OpSum());
         named_bar_sync(kBarSoftmax, 128);
         if (row < NP) ltot_s[row] = red[row] + red[64 + row] + red[128 + row] + red[192 + row];
         named_bar_sync(kBarSoftmax, 128);
