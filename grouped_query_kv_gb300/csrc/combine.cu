@@ -4,8 +4,8 @@
 //            out = sum_s w_s o_s / sum_s w_s l_s.
 // The split-KV kernel leaves one record per CTA; CTA c's record names a
 // segment when c is the first cut inside it.  Block (x, y) merges the
-// segment of the x-th such record (found with a block-wide ballot over the
-// records), y picks a slice of 4 x kThreads of the segment's heads x D
+// segment of record x, or of the x-th record that names one (found with a
+// block-wide ballot over the records), y picks a slice of 4 x kThreads of the segment's heads x D
 // outputs (four consecutive d per thread, as float4).  Each thread loads its
 // head's (m_s, l_s) and its own o_s for a batch of pieces at once -- all
 // independent loads, one round trip -- and forms the weights itself (the
@@ -30,7 +30,12 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p, int num_ctas) {
+// direct: block row c merges the segment CTA c's record names (rows whose
+// record names none exit at once); else block row x finds the x-th record
+// that names a segment.  The host takes direct rows unless they would mean
+// many more blocks (few long segments): placing blocks costs microseconds.
+__global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p, int num_ctas,
+                                                           int direct) {
     __shared__ int s_wcount[kThreads / 32];
     __shared__ int s_owner;
     // the next kernel in the stream may start its prologue while this one
@@ -40,27 +45,32 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int4 *recs = reinterpret_cast<const int4 *>(p.split);
 
-    // the blockIdx.x-th CTA whose record names a segment
-    if (tid == 0) s_owner = -1;
-    int seen = 0;
-    for (int base = 0; base < num_ctas; base += kThreads) {
-        const int c = base + tid;
-        const bool own = c < num_ctas && recs[c].x >= 0;
-        const unsigned m = __ballot_sync(0xffffffffu, own);
-        if (lane == 0) s_wcount[warp] = __popc(m);
-        __syncthreads();
-        int before = seen, total = 0;
-        for (int w = 0; w < kThreads / 32; ++w) {
-            if (w < warp) before += s_wcount[w];
-            total += s_wcount[w];
+    int c = (int)blockIdx.x;
+    if (direct) {
+        if (recs[c].x < 0) return;
+    } else {
+        // the blockIdx.x-th CTA whose record names a segment
+        if (tid == 0) s_owner = -1;
+        int seen = 0;
+        for (int base = 0; base < num_ctas; base += kThreads) {
+            const int cc = base + tid;
+            const bool own = cc < num_ctas && recs[cc].x >= 0;
+            const unsigned m = __ballot_sync(0xffffffffu, own);
+            if (lane == 0) s_wcount[warp] = __popc(m);
+            __syncthreads();
+            int before = seen, total = 0;
+            for (int w = 0; w < kThreads / 32; ++w) {
+                if (w < warp) before += s_wcount[w];
+                total += s_wcount[w];
+            }
+            if (own && before + __popc(m & ((1u << lane) - 1u)) == (int)blockIdx.x) s_owner = cc;
+            __syncthreads();
+            seen += total;
+            if (seen > (int)blockIdx.x) break;
         }
-        if (own && before + __popc(m & ((1u << lane) - 1u)) == (int)blockIdx.x) s_owner = c;
-        __syncthreads();
-        seen += total;
-        if (seen > (int)blockIdx.x) break;
+        c = s_owner;
+        if (c < 0) return;
     }
-    const int c = s_owner;
-    if (c < 0) return;
 
     const int4 rec = recs[c];
     const int b = rec.x, seg = rec.y, first_slot = rec.z, npieces = rec.w;
@@ -129,9 +139,11 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
 cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream) {
     // at most one owner per segment, and at most one per CTA
     const long long segs = (long long)p.B * p.Hkv * p.head_groups;
-    const int rows = (int)(segs < num_ctas ? segs : num_ctas);
+    const int ycount = (p.heads_per_seg * p.D / 4 + kThreads - 1) / kThreads;
+    const int direct = (segs >= num_ctas || (long long)num_ctas * ycount <= 1024) ? 1 : 0;
+    const int rows = direct ? num_ctas : (int)(segs < num_ctas ? segs : num_ctas);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows, (p.heads_per_seg * p.D / 4 + kThreads - 1) / kThreads);
+    cfg.gridDim = dim3(rows, ycount);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -140,7 +152,7 @@ cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t str
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, p, num_ctas);
+    return cudaLaunchKernelEx(&cfg, combine_kernel, p, num_ctas, direct);
 }
 
 }  // namespace kvattn
