@@ -11,7 +11,7 @@
 // kernel (decode_tc.cuh), with three changes:
 //   * warp 0 brings each 128-position tile of codes (16 KB at D = 128) into
 //     a staging ring with one TMA box;
-//   * warps 6-7 widen each staged tile to f16 (every E4M3 value is exactly
+//   * warps 6 .. 5 + CW widen each staged tile to f16 (every E4M3 value is exactly
 //     an f16 value: cvt.rn.f16x2.e4m3x2) into the 128-byte-swizzled layout
 //     of the MMA ring, and write the piece's q rows as f16;
 //   * the MMAs multiply f16 by f16 (fp32 accumulate); the softmax thread of
@@ -27,9 +27,14 @@ namespace kvattn {
 
 namespace {
 
-constexpr int kQ8Threads = 256;  // warps 0-5 as in the bf16 kernel, 6-7 convert
 constexpr int kStage = 16384;    // one staged tile: 128 positions x 128 codes
-constexpr int kConvThreads = 64;
+// Warps 0-5 as in the bf16 kernel; CW more warps widen the codes.  The
+// widening paces the kernel, so passes with fewer heads (fewer registers a
+// thread) get more converter warps.
+template <int CW>
+constexpr int kQ8Threads = 192 + 32 * CW;
+template <int NP>
+constexpr int kConvWarps = NP <= 16 ? 8 : NP <= 32 ? 4 : 2;
 
 template <int NP>
 struct Q8Cfg {
@@ -74,11 +79,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
     return r;
 }
 
-template <int NP>
-__global__ void __launch_bounds__(kQ8Threads, 1)
+template <int NP, int CW>
+__global__ void __launch_bounds__(kQ8Threads<CW>, 1)
     decode_q8_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
     using C = Q8Cfg<NP>;
+    constexpr int kConvThreads = 32 * CW;
     constexpr int D = 128;
     constexpr int NB = C::NB;
     constexpr int NS = C::NS;
@@ -114,15 +120,15 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < NB; ++s) {
-            mbar_init(&chunk_full[s], 2);  // one arrival per converter warp
+            mbar_init(&chunk_full[s], CW);  // one arrival per converter warp
             mbar_init(&chunk_empty[s], 1);
         }
         for (int s = 0; s < NS; ++s) {
             mbar_init(&st_full[s], 1);
-            mbar_init(&st_empty[s], 2);
+            mbar_init(&st_empty[s], CW);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&q_full[s], 2);
+            mbar_init(&q_full[s], CW);
             mbar_init(&q_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&s_empty[s], 4);
@@ -209,7 +215,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
 
     // ============================================================ converters
     if (warp >= 6) {
-        const int ct = tid - 192;  // 0 .. 63
+        const int ct = tid - 192;  // 0 .. 32 CW - 1
         TileIter itk;
         itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
         long long n = 0;
@@ -226,9 +232,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             const int ss = (int)(n % NS), fs = (int)(n % NB);
             if (!wwait(&st_full[ss], (uint32_t)((n / NS) & 1))) return false;
             if (n >= NB && !wwait(&chunk_empty[fs], (uint32_t)(((n / NB) - 1) & 1))) return false;
-            // thread ct converts column block k = ct mod 8 of rows ct / 8 + 8 i:
+            // thread ct converts column block k = ct mod 8 of rows ct / 8 + 4 CW i:
             // the swizzle (row mod 8 is the same for all its rows) fixes its
-            // offsets, and its rows are 1 KB apart in both layouts
+            // offsets, and its rows are 512 CW bytes apart in both layouts
             const int k = ct & 7, rr = (ct >> 3) & 7;
             const uint8_t *srcp = stage + ss * kStage + (ct >> 3) * 128 + ((k ^ rr) << 4);
             // codes 16k .. 16k+15 -> f16 columns 16k .. 16k+15: 64-column half
@@ -237,7 +243,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             const int o0 = ((2 * (k & 3)) ^ rr) << 4, o1 = ((2 * (k & 3) + 1) ^ rr) << 4;
 #pragma unroll
             for (int i = 0; i < kStage / 16 / kConvThreads; ++i) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(srcp + i * 1024);
+                const uint4 w = *reinterpret_cast<const uint4 *>(srcp + i * (kConvThreads / 8) * 128);
                 uint4 a, c;
                 a.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xFFFF));
                 a.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
@@ -247,8 +253,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 c.y = e4m3x2_to_f16x2((uint16_t)(w.z >> 16));
                 c.z = e4m3x2_to_f16x2((uint16_t)(w.w & 0xFFFF));
                 c.w = e4m3x2_to_f16x2((uint16_t)(w.w >> 16));
-                *reinterpret_cast<uint4 *>(dstp + i * 1024 + o0) = a;
-                *reinterpret_cast<uint4 *>(dstp + i * 1024 + o1) = c;
+                *reinterpret_cast<uint4 *>(dstp + i * (kConvThreads / 8) * 128 + o0) = a;
+                *reinterpret_cast<uint4 *>(dstp + i * (kConvThreads / 8) * 128 + o1) = c;
             }
             // the MMA reads the ring through the async proxy; TMA then
             // refills the staging slot
@@ -625,19 +631,20 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
 template <int NP>
 cudaError_t launch_q8(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeParams &p,
                       int num_ctas, cudaStream_t stream) {
+    constexpr int CW = kConvWarps<NP>;
     static int done_for_device[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (!(dev >= 0 && dev < 64 && done_for_device[dev])) {
-        e = cudaFuncSetAttribute(decode_q8_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_q8_kernel<NP, CW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Q8Cfg<NP>::alloc);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) done_for_device[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_ctas);
-    cfg.blockDim = dim3(kQ8Threads);
+    cfg.blockDim = dim3(kQ8Threads<CW>);
     cfg.dynamicSmemBytes = Q8Cfg<NP>::alloc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -645,7 +652,7 @@ cudaError_t launch_q8(const CUtensorMap &tmk, const CUtensorMap &tmv, const Deco
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_q8_kernel<NP>, tmk, tmv, p);
+    return cudaLaunchKernelEx(&cfg, decode_q8_kernel<NP, CW>, tmk, tmv, p);
 }
 
 }  // namespace
