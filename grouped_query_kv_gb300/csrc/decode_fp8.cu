@@ -8,17 +8,27 @@
 // 2 D.
 //
 // The same tiles, schedule, softmax and combine as the bf16 tensor-core
-// kernel (decode_tc.cuh), with three changes:
+// kernel (decode_tc.cuh), with these changes:
 //   * warp 0 brings each 128-position tile of codes (16 KB at D = 128) into
-//     a staging ring with one TMA box;
-//   * warps 6 .. 5 + CW widen each staged tile to f16 (every E4M3 value is exactly
-//     an f16 value: cvt.rn.f16x2.e4m3x2) into the 128-byte-swizzled layout
-//     of the MMA ring, and write the piece's q rows as f16;
-//   * the MMAs multiply f16 by f16 (fp32 accumulate); the softmax thread of
-//     position j scales its scores by k_scale[j] and its probability by
-//     v_scale[j] before writing P as f16 (11 significant bits, so P needs
-//     no hi/lo split here).
-// Limits: D = 128; q entries beyond the f16 range (|q| > 65504) saturate.
+//     one of two staging rings (K tiles, V tiles) with one TMA box;
+//   * Q K^T runs on the 8-bit tensor-core path straight from the staged K
+//     codes.  The piece's q rows go in as two E4M3 parts under a per-head
+//     power-of-two scale 2^c (c puts the head's largest |q| in [128, 256)):
+//     hi = e4m3(q 2^c), lo = e4m3(q 2^c - hi).  A bf16 value has 8
+//     significant bits and E4M3 4, and the remainder after rounding to 4
+//     bits is a multiple of the bf16 ulp no larger than 8 of them, so
+//     hi + lo is q 2^c exactly for entries within 2^9 of the head's
+//     largest (smaller ones are off by at most 2^-17 of it: the remainder
+//     falls below E4M3's smallest step).  Both parts multiply the same K
+//     codes into one accumulator (8 MMAs of 32 codes); the softmax scales
+//     the sum by 2^-c k_scale[j];
+//   * warps 6 .. 5 + CW widen each staged V tile to f16 (every E4M3 value
+//     is exactly an f16 value: cvt.rn.f16x2.e4m3x2) into the 128-byte-
+//     swizzled layout of the P V operand ring, and write the q parts;
+//   * P V multiplies f16 by f16 (fp32 accumulate); the softmax thread of
+//     position j scales its probability by v_scale[j] before writing P as
+//     f16 (11 significant bits, so P needs no hi/lo split here).
+// Limits: D = 128.
 #include <cuda_fp16.h>
 
 #include "decode_tc.cuh"
@@ -28,7 +38,7 @@ namespace kvattn {
 namespace {
 
 constexpr int kStage = 16384;    // one staged tile: 128 positions x 128 codes
-// Warps 0-5 as in the bf16 kernel; CW more warps widen the codes.  The
+// Warps 0-5 as in the bf16 kernel; CW more warps widen the V codes.  The
 // widening paces the kernel, so passes with fewer heads (fewer registers a
 // thread) get more converter warps.
 template <int CW>
@@ -39,36 +49,40 @@ constexpr int kConvWarps = NP <= 16 ? 8 : NP <= 32 ? 4 : 2;
 template <int NP>
 struct Q8Cfg {
     static constexpr int D = 128;
-    static constexpr int QB = (D / 64) * NP * 128;  // one f16 q buffer (swizzled, K-major)
-    static constexpr int PB = NP * kT * 2;          // one f16 P^T stage
+    static constexpr int QB = 2 * NP * 128;   // one q buffer: NP hi rows, then NP lo rows (E4M3, swizzled)
+    static constexpr int PB = NP * kT * 2;    // one f16 P^T stage
     static constexpr int PST = 2;
-    static constexpr int NBAR_MAX = 2 * 3 + 2 * 8 + 14;
-    static constexpr int FIXED = 2 * QB + PST * PB + 4 * 64 * 4 + 3 * 64 * 4 + 64 + 1024 +
-                                 NBAR_MAX * 8;
-    // MMA ring (f16 tiles): three slots when the staging ring still gets four
-    static constexpr int NB = (kSmemLimit - FIXED - 3 * kChunk) / kStage >= 4 ? 3 : 2;
+    static constexpr int NB = 2;              // f16 V ring slots
+    static constexpr int NBAR_MAX = 2 * NB + 2 * 8 + 14;
+    static constexpr int FIXED = 2 * QB + PST * PB + 4 * 64 * 4 + 3 * 64 * 4 + 2 * 64 * 4 +
+                                 64 + 1024 + NBAR_MAX * 8;
     static constexpr int NS_FIT = (kSmemLimit - FIXED - NB * kChunk) / kStage;
-    static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
-    static_assert(NS >= 2, "staging ring must hold two tiles");
+    static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;   // staging slots, both rings
+    static constexpr int NSV = NS / 2;                   // V staging slots
+    static constexpr int NSK = NS - NSV;                 // K staging slots
+    static_assert(NSV >= 2 && NSK >= 2, "staging rings must hold two tiles each");
 
     static constexpr int off_ring = 0;
-    static constexpr int off_stage = NB * kChunk;
-    static constexpr int off_q = off_stage + NS * kStage;
+    static constexpr int off_kst = NB * kChunk;
+    static constexpr int off_vst = off_kst + NSK * kStage;
+    static constexpr int off_q = off_vst + NSV * kStage;
     static constexpr int off_p = off_q + 2 * QB;
     static constexpr int off_red = off_p + PST * PB;      // float [4][64]
     static constexpr int off_ltot = off_red + 4 * 64 * 4;
     static constexpr int off_mref = off_ltot + 64 * 4;
     static constexpr int off_alpha = off_mref + 64 * 4;
-    static constexpr int off_bar = off_alpha + 64 * 4;
+    static constexpr int off_qinv = off_alpha + 64 * 4;   // float [2][64]: 2^-c per head
+    static constexpr int off_bar = off_qinv + 2 * 64 * 4;
     static constexpr int nbar = 2 * NB + 2 * NS + 14;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int bytes = off_misc + 64;
     static constexpr int alloc = bytes + 1024;
     static_assert(alloc <= kSmemLimit, "shared memory");
+    static_assert(off_q % 1024 == 0 && off_p % 1024 == 0 && QB % 1024 == 0, "swizzle atoms");
 
     // TMEM: S0, S1 (NP columns each), then the O^T accumulator (NP columns)
     static constexpr int TMEM_COLS = pow2_at_least(3 * NP);
-    static constexpr uint32_t IDESC_QK = idesc_f16_f32(128, NP, false, false);
+    static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, NP);
     static constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, true);
 };
 
@@ -79,6 +93,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
     return r;
 }
 
+// Two binary32 values -> two E4M3 codes (nearest, ties to even,
+// saturating), a in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2_of(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+__device__ __forceinline__ float2 e4m3x2_value(uint16_t two) {
+    const uint32_t h = e4m3x2_to_f16x2(two);
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
 template <int NP, int CW>
 __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
     decode_q8_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -87,29 +114,34 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
     constexpr int kConvThreads = 32 * CW;
     constexpr int D = 128;
     constexpr int NB = C::NB;
-    constexpr int NS = C::NS;
+    constexpr int NSK = C::NSK;
+    constexpr int NSV = C::NSV;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem + C::off_ring;
-    uint8_t *stage = smem + C::off_stage;
+    uint8_t *kst = smem + C::off_kst;
+    uint8_t *vst = smem + C::off_vst;
     uint8_t *qbuf = smem + C::off_q;
     uint8_t *pbuf = smem + C::off_p;
     float *red = reinterpret_cast<float *>(smem + C::off_red);
     float *ltot_s = reinterpret_cast<float *>(smem + C::off_ltot);
     float *mref_s = reinterpret_cast<float *>(smem + C::off_mref);
     float *alpha_s = reinterpret_cast<float *>(smem + C::off_alpha);
+    float *qinv_s = reinterpret_cast<float *>(smem + C::off_qinv);
     uint64_t *bar_base = reinterpret_cast<uint64_t *>(smem + C::off_bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::off_misc + 16);
 
-    // chunk_full/chunk_empty: the MMA ring (filled by the converters);
-    // st_full/st_empty: the staging ring (filled by TMA); q_full/q_empty:
-    // the f16 q buffers (filled by the converters)
-    uint64_t *chunk_full = bar_base, *chunk_empty = bar_base + NB;
-    uint64_t *st_full = bar_base + 2 * NB, *st_empty = st_full + NS;
-    uint64_t *q_full = st_empty + NS, *q_empty = q_full + 2;
+    // vf_full/vf_empty: the f16 V ring (filled by the converters);
+    // kst_*: the K staging ring (TMA -> MMA); vst_*: the V staging ring
+    // (TMA -> converters); q_full/q_empty: the q parts and 2^-c (filled by
+    // the converters, freed by the last Q K^T of the piece and the softmax)
+    uint64_t *vf_full = bar_base, *vf_empty = bar_base + NB;
+    uint64_t *kst_full = bar_base + 2 * NB, *kst_empty = kst_full + NSK;
+    uint64_t *vst_full = kst_empty + NSK, *vst_empty = vst_full + NSV;
+    uint64_t *q_full = vst_empty + NSV, *q_empty = q_full + 2;
     uint64_t *s_full = q_empty + 2, *s_empty = s_full + 2;
     uint64_t *p_full = s_empty + 2, *pv_done = p_full + 2;
     uint64_t *o_free = pv_done + 2, *drain = o_free + 1;
@@ -120,16 +152,20 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
 
     if (tid == 0) {
         for (int s = 0; s < NB; ++s) {
-            mbar_init(&chunk_full[s], CW);  // one arrival per converter warp
-            mbar_init(&chunk_empty[s], 1);
+            mbar_init(&vf_full[s], CW);  // one arrival per converter warp
+            mbar_init(&vf_empty[s], 1);
         }
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&st_full[s], 1);
-            mbar_init(&st_empty[s], CW);
+        for (int s = 0; s < NSK; ++s) {
+            mbar_init(&kst_full[s], 1);
+            mbar_init(&kst_empty[s], 1);
+        }
+        for (int s = 0; s < NSV; ++s) {
+            mbar_init(&vst_full[s], 1);
+            mbar_init(&vst_empty[s], CW);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&q_full[s], CW);
-            mbar_init(&q_empty[s], 1);
+            mbar_init(&q_empty[s], 1 + 4);  // the MMA commit and the 4 softmax warps
             mbar_init(&s_full[s], 1);
             mbar_init(&s_empty[s], 4);
             mbar_init(&p_full[s], 4);
@@ -164,48 +200,49 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
     }
     const long long ntiles = st.g_end - st.g_begin;
     const uint32_t ring_s = smem_u32(ring);
+    const uint32_t kst_s = smem_u32(kst);
     const uint32_t qbuf_s = smem_u32(qbuf);
     const uint32_t pbuf_s = smem_u32(pbuf);
 
     // ================================================================ producer
-    // Staging order follows the MMA ring: K_0, K_1, V_0, K_2, V_1, ...
+    // Issue order K_0, K_1, V_0, K_2, V_1, ... (each ring in its own order)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             TileIter itk, itv;
             itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
             itv.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
-            long long n = 0;
+            long long nk = 0, nv = 0;
             bool ok = true;
-            auto issue = [&](const void *tm, const TileIter &it) -> bool {
-                const int slot = (int)(n % NS);
-                if (n >= NS &&
-                    !wait_bar(&st_empty[slot], (uint32_t)(((n / NS) - 1) & 1), abort_flag))
+            auto issue = [&](const void *tm, const TileIter &it, uint8_t *base, uint64_t *full,
+                             uint64_t *empty, int ns, long long &n) -> bool {
+                const int slot = (int)(n % ns);
+                if (n >= ns && !wait_bar(&empty[slot], (uint32_t)(((n / ns) - 1) & 1), abort_flag))
                     return false;
-                mbar_arrive_expect_tx(&st_full[slot], kStage);
+                mbar_arrive_expect_tx(&full[slot], kStage);
                 const int z = it.b * p.Hkv + it.seg / p.head_groups;
-                tma_load_3d(stage + slot * kStage, tm, &st_full[slot], 0, it.row0(), z, pol);
+                tma_load_3d(base + slot * kStage, tm, &full[slot], 0, it.row0(), z, pol);
                 ++n;
                 return true;
             };
             for (long long r = 0; r <= ntiles && ok; ++r) {
                 if (r < ntiles) {
-                    ok = issue(&tmk, itk);
+                    ok = issue(&tmk, itk, kst, kst_full, kst_empty, NSK, nk);
                     itk.next();
                 }
                 if (r >= 1 && ok) {
-                    ok = issue(&tmv, itv);
+                    ok = issue(&tmv, itv, vst, vst_full, vst_empty, NSV, nv);
                     itv.next();
                 }
             }
             if (!ok) {
                 set_error(p.err, DEV_ERR_TIMEOUT);
                 *abort_flag = 1;
-                const long long first = n > NS ? n - NS : 0;
-                for (long long k = first; k < n; ++k) {
-                    volatile int never = 0;
-                    wait_bar(&st_full[k % NS], (uint32_t)((k / NS) & 1), &never);
-                }
+                volatile int never = 0;
+                for (long long k = nk > NSK ? nk - NSK : 0; k < nk; ++k)
+                    wait_bar(&kst_full[k % NSK], (uint32_t)((k / NSK) & 1), &never);
+                for (long long k = nv > NSV ? nv - NSV : 0; k < nv; ++k)
+                    wait_bar(&vst_full[k % NSV], (uint32_t)((k / NSV) & 1), &never);
             }
         }
         __syncwarp();
@@ -216,8 +253,9 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
     // ============================================================ converters
     if (warp >= 6) {
         const int ct = tid - 192;  // 0 .. 32 CW - 1
-        TileIter itk;
-        itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+        const int cw = warp - 6;
+        TileIter itq;
+        itq.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
         long long n = 0;
         int piece = 0;
         bool ok = true;
@@ -227,16 +265,16 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
             if (lane == 0) w = wait_bar(bar, parity, abort_flag);
             return __shfl_sync(0xffffffffu, w, 0);
         };
-        // staged chunk n -> MMA ring slot n % NB
+        // staged V tile n -> f16 ring slot n % NB
         auto convert = [&]() -> bool {
-            const int ss = (int)(n % NS), fs = (int)(n % NB);
-            if (!wwait(&st_full[ss], (uint32_t)((n / NS) & 1))) return false;
-            if (n >= NB && !wwait(&chunk_empty[fs], (uint32_t)(((n / NB) - 1) & 1))) return false;
+            const int ss = (int)(n % NSV), fs = (int)(n % NB);
+            if (!wwait(&vst_full[ss], (uint32_t)((n / NSV) & 1))) return false;
+            if (n >= NB && !wwait(&vf_empty[fs], (uint32_t)(((n / NB) - 1) & 1))) return false;
             // thread ct converts column block k = ct mod 8 of rows ct / 8 + 4 CW i:
             // the swizzle (row mod 8 is the same for all its rows) fixes its
             // offsets, and its rows are 512 CW bytes apart in both layouts
             const int k = ct & 7, rr = (ct >> 3) & 7;
-            const uint8_t *srcp = stage + ss * kStage + (ct >> 3) * 128 + ((k ^ rr) << 4);
+            const uint8_t *srcp = vst + ss * kStage + (ct >> 3) * 128 + ((k ^ rr) << 4);
             // codes 16k .. 16k+15 -> f16 columns 16k .. 16k+15: 64-column half
             // k / 4, 16-byte pieces 2 (k mod 4) and 2 (k mod 4) + 1
             uint8_t *dstp = ring + fs * kChunk + (k >> 2) * 16384 + (ct >> 3) * 128;
@@ -261,13 +299,14 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&chunk_full[fs]);
-                mbar_arrive(&st_empty[ss]);
+                mbar_arrive(&vf_full[fs]);
+                mbar_arrive(&vst_empty[ss]);
             }
             ++n;
             return true;
         };
-        // the piece's q rows, bf16 -> f16, into the swizzled K-major layout
+        // the piece's q rows as E4M3 hi / lo parts, swizzled K-major rows
+        // (hi of head g in row g, lo in row NP + g), and 2^-c per head
         auto load_q = [&](const TileIter &it) -> bool {
             const int qs = piece & 1;
             if (piece >= 2 && !wwait(&q_empty[qs], (uint32_t)(((piece >> 1) - 1) & 1)))
@@ -275,28 +314,36 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
             const int kvh = it.seg / p.head_groups, hg = it.seg % p.head_groups;
             const int h0 = kvh * p.G + hg * p.heads_per_seg;
             const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
-            const uint4 *qg = reinterpret_cast<const uint4 *>(p.q);
-            for (int e = ct; e < NP * (D / 8); e += kConvThreads) {
-                const int g = e / (D / 8), c8 = e % (D / 8);  // head row, 8-column piece
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (g < gvalid) {
-                    const uint4 raw = qg[((size_t)it.b * p.Hq + h0 + g) * (D / 8) + c8];
-                    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
-                    uint32_t outw[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float lo = __uint_as_float(in[u] << 16);
-                        float hi = __uint_as_float(in[u] & 0xFFFF0000u);
-                        lo = fminf(fmaxf(lo, -65504.f), 65504.f);
-                        hi = fminf(fmaxf(hi, -65504.f), 65504.f);
-                        const __half2 h2 = __floats2half2_rn(lo, hi);
-                        outw[u] = *reinterpret_cast<const uint32_t *>(&h2);
-                    }
-                    v = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            uint8_t *qb = qbuf + qs * C::QB;
+            for (int g = cw; g < NP; g += CW) {
+                float x[4] = {0.f, 0.f, 0.f, 0.f};
+                if (g < gvalid) {  // lane l holds columns 4l .. 4l + 3
+                    const uint2 raw = reinterpret_cast<const uint2 *>(
+                        p.q)[((size_t)it.b * p.Hq + h0 + g) * (D / 4) + lane];
+                    x[0] = __uint_as_float(raw.x << 16);
+                    x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+                    x[2] = __uint_as_float(raw.y << 16);
+                    x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
                 }
-                const int half = c8 >> 3, j = c8 & 7;
-                *reinterpret_cast<uint4 *>(qbuf + qs * C::QB + half * NP * 128 + g * 128 +
-                                           ((j ^ (g & 7)) << 4)) = v;
+                float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                // c = 7 - floor(log2 amax), kept where 2^c and 2^-c are normal
+                int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+                e = max(-119, min(e, 120));
+                const float sc = __uint_as_float((uint32_t)(127 + 7 - e) << 23);
+                float y[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) y[u] = x[u] * sc;  // exact: a power of two
+                const uint16_t h01 = e4m3x2_of(y[0], y[1]), h23 = e4m3x2_of(y[2], y[3]);
+                const float2 v01 = e4m3x2_value(h01), v23 = e4m3x2_value(h23);
+                const uint16_t l01 = e4m3x2_of(y[0] - v01.x, y[1] - v01.y);
+                const uint16_t l23 = e4m3x2_of(y[2] - v23.x, y[3] - v23.y);
+                const int off = (((lane >> 2) ^ (g & 7)) << 4) + 4 * (lane & 3);
+                *reinterpret_cast<uint32_t *>(qb + g * 128 + off) = (uint32_t)h01 | ((uint32_t)h23 << 16);
+                *reinterpret_cast<uint32_t *>(qb + (NP + g) * 128 + off) = (uint32_t)l01 | ((uint32_t)l23 << 16);
+                if (lane == 0)
+                    qinv_s[qs * 64 + g] = (g < gvalid) ? __uint_as_float((uint32_t)(127 - 7 + e) << 23) : 0.f;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -306,9 +353,8 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
         };
         for (long long r = 0; r <= ntiles && ok; ++r) {
             if (r < ntiles) {
-                if (r == 0 || itk.t == 0) ok = load_q(itk);
-                if (ok) ok = convert();
-                itk.next();
+                if (r == 0 || itq.t == 0) ok = load_q(itq);
+                itq.next();
             }
             if (r >= 1 && ok) ok = convert();
         }
@@ -331,20 +377,19 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
             bool ok = true;
             while (ip < ntiles) {
                 bool did = false;
-                if (ip < iq) {  // PV of tile ip
+                if (ip < iq) {  // P V of tile ip
                     const long long j = ip;
                     const int pb = (int)(j & 1);
                     const bool first_pv = (j == 0) || (itp.t == 0);
                     bool ready = mbar_test(&p_full[pb], (uint32_t)((j >> 1) & 1));
                     if (ready && first_pv && piece_pv > 0)
                         ready = mbar_test(o_free, (uint32_t)((piece_pv - 1) & 1));
-                    const long long idx = v_chunk<1>(j, 0, ntiles);
-                    if (ready) ready = mbar_test(&chunk_full[idx % NB], (uint32_t)((idx / NB) & 1));
+                    const int slot = (int)(j % NB);
+                    if (ready) ready = mbar_test(&vf_full[slot], (uint32_t)((j / NB) & 1));
                     if (ready) {
                         if (first_pv) ++piece_pv;
                         tc_fence_after();
                         const uint32_t pstage = pbuf_s + (int)(j % C::PST) * C::PB;
-                        const int slot = (int)(idx % NB);
                         const uint32_t v0 = ring_s + slot * kChunk;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
@@ -352,44 +397,38 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
                             const uint64_t bd = smem_desc(pstage + kk * 256, 128, (kT / 8) * 128, 0);
                             umma_bf16(tmem + 2 * NP, ad, bd, C::IDESC_PV, !(first_pv && kk == 0));
                         }
-                        umma_commit(&chunk_empty[slot]);
+                        umma_commit(&vf_empty[slot]);
                         umma_commit(&pv_done[pb]);
                         if (j < ntiles - 1) itp.next();
                         ++ip;
                         did = true;
                     }
                 }
-                if (iq < ntiles) {  // QK of tile iq
+                if (iq < ntiles) {  // Q K^T of tile iq: hi part, then lo part
                     const long long i = iq;
                     const int sb = (int)(i & 1);
                     const bool first_q = (i == 0) || (itq.t == 0);
                     bool ready = true;
                     if (first_q) ready = mbar_test(&q_full[piece_q & 1], (uint32_t)((piece_q >> 1) & 1));
                     if (ready && i >= 2) ready = mbar_test(&s_empty[sb], (uint32_t)(((i >> 1) - 1) & 1));
-                    const long long idx = k_chunk<1>(i, 0);
-                    if (ready && idx >= NB) {
-                        long long vt;
-                        if (chunk_is_v<1>(idx - NB, ntiles, &vt) && vt >= ip) ready = false;
-                    }
-                    if (ready) ready = mbar_test(&chunk_full[idx % NB], (uint32_t)((idx / NB) & 1));
+                    const int slot = (int)(i % NSK);
+                    if (ready) ready = mbar_test(&kst_full[slot], (uint32_t)((i / NSK) & 1));
                     if (ready) {
                         if (first_q) {
                             qcur = piece_q & 1;
                             ++piece_q;
                         }
                         tc_fence_after();
-                        const int slot = (int)(idx % NB);
-                        const uint32_t a0 = ring_s + slot * kChunk;
+                        const uint32_t a0 = kst_s + slot * kStage;
+                        const uint32_t b0 = qbuf_s + qcur * C::QB;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t ad =
-                                smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
-                            const uint64_t bd = smem_desc(
-                                qbuf_s + qcur * C::QB + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16,
-                                1024, 2);
-                            umma_bf16(tmem + sb * NP, ad, bd, C::IDESC_QK, kk != 0);
+                        for (int kk = 0; kk < 8; ++kk) {  // 32 codes per MMA
+                            const uint64_t ad = smem_desc(a0 + (kk & 3) * 32, 16, 1024, 2);
+                            const uint64_t bd =
+                                smem_desc(b0 + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024, 2);
+                            umma_f8(tmem + sb * NP, ad, bd, C::IDESC_QK, kk != 0);
                         }
-                        umma_commit(&chunk_empty[slot]);
+                        umma_commit(&kst_empty[slot]);
                         umma_commit(&s_full[sb]);
                         if (itq.last_tile_of_segment() || i == ntiles - 1) umma_commit(&q_empty[qcur]);
                         if (i < ntiles - 1) itq.next();
@@ -436,6 +475,7 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
     TileIter it;
     it.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
     long long i = 0;
+    int spiece = 0;
     bool first_piece = true;
     bool aborted = false;
     bool carry_fail = false;
@@ -453,9 +493,13 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
         const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
         const size_t zrow = ((size_t)b * p.Hkv + kvh) * p.Lmax;  // first scale of this block
         const long long i0 = i;
+        const int qs = spiece & 1;
+        const float *qinv = qinv_s + qs * 64;
 #pragma unroll
         for (int g = 0; g < NP; ++g) l[g] = 0.f;
         if (row < NP) mref_s[row] = -INFINITY;
+        // the piece's 2^-c (written by the converters)
+        carry_fail = carry_fail || !wait_bar(&q_full[qs], (uint32_t)((spiece >> 1) & 1), abort_flag);
         named_bar_sync(kBarSoftmax, 128);
 
         while (true) {
@@ -489,10 +533,11 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
 #pragma unroll
             for (int g = 0; g < NP; g += 4) {
                 const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g);
-                s[g] = valid ? s[g] * sl : -INFINITY;
-                s[g + 1] = valid ? s[g + 1] * sl : -INFINITY;
-                s[g + 2] = valid ? s[g + 2] * sl : -INFINITY;
-                s[g + 3] = valid ? s[g + 3] * sl : -INFINITY;
+                const float4 c4 = *reinterpret_cast<const float4 *>(qinv + g);
+                s[g] = valid ? s[g] * (c4.x * sl) : -INFINITY;
+                s[g + 1] = valid ? s[g + 1] * (c4.y * sl) : -INFINITY;
+                s[g + 2] = valid ? s[g + 2] * (c4.z * sl) : -INFINITY;
+                s[g + 3] = valid ? s[g + 3] * (c4.w * sl) : -INFINITY;
                 over |= (s[g] > m4.x + kTau) | (s[g + 1] > m4.y + kTau) |
                         (s[g + 2] > m4.z + kTau) | (s[g + 3] > m4.w + kTau);
             }
@@ -573,6 +618,10 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
             it.next();
         }
         if (aborted) break;
+        // this warp is done with the piece's 2^-c
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_empty[qs]);
+        ++spiece;
 
         // ---- piece end
         const long long e = i - 1;
