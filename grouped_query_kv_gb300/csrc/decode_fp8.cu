@@ -8,26 +8,42 @@
 // 2 D.
 //
 // The same tiles, schedule, softmax and combine as the bf16 tensor-core
-// kernel (decode_tc.cuh), with these changes:
-//   * warp 0 brings each 128-position tile of codes (16 KB at D = 128) into
-//     one of two staging rings (K tiles, V tiles) with one TMA box;
-//   * Q K^T runs on the 8-bit tensor-core path straight from the staged K
-//     codes.  The piece's q rows go in as two E4M3 parts under a per-head
+// kernel (decode_tc.cuh).  Both products run on the 8-bit tensor-core path
+// (kind::f8f6f4, fp32 accumulation) straight from the staged codes: warp 0
+// brings each 128-position tile of K codes and of V codes (16 KB at
+// D = 128) into its staging ring with one TMA box, and the MMAs read them
+// there -- no widening pass.  A tcgen05 MMA of M = 128 costs the tensor pipe
+// about the same time at any N up to 256, so what paces a decode tile is the
+// number of MMAs, not their width; this layout takes 8 per tile (4 for
+// Q K^T, 4 for P V) where 16-bit operands take 16.
+//
+//   * Q K^T.  The piece's q rows go in as two E4M3 parts under a per-head
 //     power-of-two scale 2^c (c puts the head's largest |q| in [128, 256)):
 //     hi = e4m3(q 2^c), lo = e4m3(q 2^c - hi).  A bf16 value has 8
 //     significant bits and E4M3 4, and the remainder after rounding to 4
 //     bits is a multiple of the bf16 ulp no larger than 8 of them, so
 //     hi + lo is q 2^c exactly for entries within 2^9 of the head's
 //     largest (smaller ones are off by at most 2^-17 of it: the remainder
-//     falls below E4M3's smallest step).  Both parts multiply the same K
-//     codes into one accumulator (8 MMAs of 32 codes); the softmax scales
-//     the sum by 2^-c k_scale[j];
-//   * warps 6 .. 5 + CW widen each staged V tile to f16 (every E4M3 value
-//     is exactly an f16 value: cvt.rn.f16x2.e4m3x2) into the 128-byte-
-//     swizzled layout of the P V operand ring, and write the q parts;
-//   * P V multiplies f16 by f16 (fp32 accumulate); the softmax thread of
-//     position j scales its probability by v_scale[j] before writing P as
-//     f16 (11 significant bits, so P needs no hi/lo split here).
+//     falls below E4M3's smallest step).  For passes of up to 32 heads the
+//     parts sit side by side as the 2 NP columns of one B operand and the
+//     softmax adds the two partial scores; wider passes, short of registers
+//     for that, run the lo part as 4 more MMAs into the same accumulator.
+//     Warps 6-7 write the parts; the softmax scales the score by
+//     2^-c k_scale[j].
+//   * P V.  The weight of position j for head g is w = p v_scale[j]
+//     (p = 2^(s - m) the unnormalised probability).  Scaled by a
+//     power of two 2^cv that the CTA keeps per piece (the largest v_scale
+//     met so far times 2^cv in [32, 64)) and with p <= 4 between rescales
+//     (the running max is refreshed once a score passes it by 2), w 2^cv
+//     stays <= 256, inside E4M3's range, and goes in as three E4M3 parts
+//     hi + mid + lo (each the rounded remainder of the previous), about 12
+//     significant bits -- the f16 P of a widening design carries 11.  The
+//     parts sit side by side as the 3 NP columns of the B operand (P stored
+//     position-major, no swizzle), so 4 MMAs per tile accumulate three
+//     partial O^T blocks; the epilogue adds them and divides by 2^cv.  A
+//     tile whose v_scale would break the bound lowers cv first, rescaling
+//     the accumulator by the same power of two (with the running-max
+//     rescale, in the same step).
 // Limits: D = 128.
 #include <cuda_fp16.h>
 
@@ -38,32 +54,28 @@ namespace kvattn {
 namespace {
 
 constexpr int kStage = 16384;    // one staged tile: 128 positions x 128 codes
-// Warps 0-5 as in the bf16 kernel; CW more warps widen the V codes.  The
-// widening paces the kernel, so passes with fewer heads (fewer registers a
-// thread) get more converter warps.
-template <int CW>
-constexpr int kQ8Threads = 192 + 32 * CW;
-template <int NP>
-constexpr int kConvWarps = NP <= 16 ? 8 : NP <= 32 ? 4 : 2;
+constexpr int kQWarps = 2;       // warps 6-7 write the q parts
+constexpr int kQ8Threads = 192 + 32 * kQWarps;
+constexpr float kTauQ8 = 2.f;    // rescale once a score passes the running max by 2 (log2 units)
+constexpr float kVHi = 64.f;     // v_scale[j] 2^cv stays <= 64
+constexpr int kCvNone = 1 << 20; // cv not chosen yet (piece start)
 
 template <int NP>
 struct Q8Cfg {
-    static constexpr int D = 128;
     static constexpr int QB = 2 * NP * 128;   // one q buffer: NP hi rows, then NP lo rows (E4M3, swizzled)
-    static constexpr int PB = NP * kT * 2;    // one f16 P^T stage
+    static constexpr int PB = 3 * NP * kT;    // one P stage: 3 NP E4M3 columns x 128 positions
     static constexpr int PST = 2;
-    static constexpr int NB = 2;              // f16 V ring slots
-    static constexpr int NBAR_MAX = 2 * NB + 2 * 8 + 14;
-    static constexpr int FIXED = 2 * QB + PST * PB + 4 * 64 * 4 + 3 * 64 * 4 + 2 * 64 * 4 +
+    static constexpr int NS_MAX = 12;
+    static constexpr int NBAR_MAX = 2 * NS_MAX + 14;
+    static constexpr int FIXED = 2 * QB + PST * PB + 4 * 64 * 4 + 3 * 64 * 4 + 2 * 64 * 4 + 16 +
                                  64 + 1024 + NBAR_MAX * 8;
-    static constexpr int NS_FIT = (kSmemLimit - FIXED - NB * kChunk) / kStage;
-    static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;   // staging slots, both rings
-    static constexpr int NSV = NS / 2;                   // V staging slots
-    static constexpr int NSK = NS - NSV;                 // K staging slots
+    static constexpr int NS_FIT = (kSmemLimit - FIXED) / kStage;
+    static constexpr int NS = NS_FIT > NS_MAX ? NS_MAX : NS_FIT;   // staging slots, both rings
+    static constexpr int NSK = NS / 2;                             // K staging slots
+    static constexpr int NSV = NS - NSK;                           // V staging slots
     static_assert(NSV >= 2 && NSK >= 2, "staging rings must hold two tiles each");
 
-    static constexpr int off_ring = 0;
-    static constexpr int off_kst = NB * kChunk;
+    static constexpr int off_kst = 0;
     static constexpr int off_vst = off_kst + NSK * kStage;
     static constexpr int off_q = off_vst + NSV * kStage;
     static constexpr int off_p = off_q + 2 * QB;
@@ -72,18 +84,24 @@ struct Q8Cfg {
     static constexpr int off_mref = off_ltot + 64 * 4;
     static constexpr int off_alpha = off_mref + 64 * 4;
     static constexpr int off_qinv = off_alpha + 64 * 4;   // float [2][64]: 2^-c per head
-    static constexpr int off_bar = off_qinv + 2 * 64 * 4;
-    static constexpr int nbar = 2 * NB + 2 * NS + 14;
+    static constexpr int off_vred = off_qinv + 2 * 64 * 4;  // float [4]: a tile's largest v_scale
+    static constexpr int off_bar = off_vred + 16;
+    static constexpr int nbar = 2 * NS + 14;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int bytes = off_misc + 64;
     static constexpr int alloc = bytes + 1024;
     static_assert(alloc <= kSmemLimit, "shared memory");
     static_assert(off_q % 1024 == 0 && off_p % 1024 == 0 && QB % 1024 == 0, "swizzle atoms");
 
-    // TMEM: S0, S1 (NP columns each), then the O^T accumulator (NP columns)
-    static constexpr int TMEM_COLS = pow2_at_least(3 * NP);
-    static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, NP);
-    static constexpr uint32_t IDESC_PV = idesc_f16_f32(128, NP, true, true);
+    // TMEM: S0, S1 (side by side: 2 NP columns each, hi part then lo part;
+    // else NP columns), then the O^T accumulator (3 NP columns: hi, mid, lo
+    // parts of P)
+    static constexpr bool SBS = NP <= 32;
+    static constexpr int SW = SBS ? 2 * NP : NP;
+    static constexpr int OA = 2 * SW;
+    static constexpr int TMEM_COLS = pow2_at_least(OA + 3 * NP);
+    static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, SW, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, 3 * NP, true, true);
 };
 
 // Two E4M3 codes (low byte first) -> f16x2 (low half first); exact.
@@ -106,21 +124,21 @@ __device__ __forceinline__ float2 e4m3x2_value(uint16_t two) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
-template <int NP, int CW>
-__global__ void __launch_bounds__(kQ8Threads<CW>, 1)
+// 2^e as a binary32 value, e in [-126, 127].
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+template <int NP>
+__global__ void __launch_bounds__(kQ8Threads, 1)
     decode_q8_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
     using C = Q8Cfg<NP>;
-    constexpr int kConvThreads = 32 * CW;
     constexpr int D = 128;
-    constexpr int NB = C::NB;
     constexpr int NSK = C::NSK;
     constexpr int NSV = C::NSV;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *ring = smem + C::off_ring;
     uint8_t *kst = smem + C::off_kst;
     uint8_t *vst = smem + C::off_vst;
     uint8_t *qbuf = smem + C::off_q;
@@ -130,16 +148,15 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
     float *mref_s = reinterpret_cast<float *>(smem + C::off_mref);
     float *alpha_s = reinterpret_cast<float *>(smem + C::off_alpha);
     float *qinv_s = reinterpret_cast<float *>(smem + C::off_qinv);
+    float *vred_s = reinterpret_cast<float *>(smem + C::off_vred);
     uint64_t *bar_base = reinterpret_cast<uint64_t *>(smem + C::off_bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::off_misc + 16);
 
-    // vf_full/vf_empty: the f16 V ring (filled by the converters);
-    // kst_*: the K staging ring (TMA -> MMA); vst_*: the V staging ring
-    // (TMA -> converters); q_full/q_empty: the q parts and 2^-c (filled by
-    // the converters, freed by the last Q K^T of the piece and the softmax)
-    uint64_t *vf_full = bar_base, *vf_empty = bar_base + NB;
-    uint64_t *kst_full = bar_base + 2 * NB, *kst_empty = kst_full + NSK;
+    // kst_*: the K staging ring (TMA -> Q K^T); vst_*: the V staging ring
+    // (TMA -> P V); q_full/q_empty: the q parts and 2^-c (written by warps
+    // 6-7, freed by the last Q K^T of the piece and the 4 softmax warps)
+    uint64_t *kst_full = bar_base, *kst_empty = kst_full + NSK;
     uint64_t *vst_full = kst_empty + NSK, *vst_empty = vst_full + NSV;
     uint64_t *q_full = vst_empty + NSV, *q_empty = q_full + 2;
     uint64_t *s_full = q_empty + 2, *s_empty = s_full + 2;
@@ -151,20 +168,16 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
     const int segs_per_b = p.Hkv * p.head_groups;
 
     if (tid == 0) {
-        for (int s = 0; s < NB; ++s) {
-            mbar_init(&vf_full[s], CW);  // one arrival per converter warp
-            mbar_init(&vf_empty[s], 1);
-        }
         for (int s = 0; s < NSK; ++s) {
             mbar_init(&kst_full[s], 1);
             mbar_init(&kst_empty[s], 1);
         }
         for (int s = 0; s < NSV; ++s) {
             mbar_init(&vst_full[s], 1);
-            mbar_init(&vst_empty[s], CW);
+            mbar_init(&vst_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&q_full[s], CW);
+            mbar_init(&q_full[s], kQWarps);
             mbar_init(&q_empty[s], 1 + 4);  // the MMA commit and the 4 softmax warps
             mbar_init(&s_full[s], 1);
             mbar_init(&s_empty[s], 4);
@@ -199,8 +212,8 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
         return;
     }
     const long long ntiles = st.g_end - st.g_begin;
-    const uint32_t ring_s = smem_u32(ring);
     const uint32_t kst_s = smem_u32(kst);
+    const uint32_t vst_s = smem_u32(vst);
     const uint32_t qbuf_s = smem_u32(qbuf);
     const uint32_t pbuf_s = smem_u32(pbuf);
 
@@ -250,113 +263,62 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
         return;
     }
 
-    // ============================================================ converters
+    // ======================================================== q parts (6, 7)
     if (warp >= 6) {
-        const int ct = tid - 192;  // 0 .. 32 CW - 1
-        const int cw = warp - 6;
+        const int qw = warp - 6;
         TileIter itq;
         itq.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
-        long long n = 0;
         int piece = 0;
         bool ok = true;
-        // wait on a barrier with lane 0, the whole warp learning the outcome
-        auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
-            bool w = true;
-            if (lane == 0) w = wait_bar(bar, parity, abort_flag);
-            return __shfl_sync(0xffffffffu, w, 0);
-        };
-        // staged V tile n -> f16 ring slot n % NB
-        auto convert = [&]() -> bool {
-            const int ss = (int)(n % NSV), fs = (int)(n % NB);
-            if (!wwait(&vst_full[ss], (uint32_t)((n / NSV) & 1))) return false;
-            if (n >= NB && !wwait(&vf_empty[fs], (uint32_t)(((n / NB) - 1) & 1))) return false;
-            // thread ct converts column block k = ct mod 8 of rows ct / 8 + 4 CW i:
-            // the swizzle (row mod 8 is the same for all its rows) fixes its
-            // offsets, and its rows are 512 CW bytes apart in both layouts
-            const int k = ct & 7, rr = (ct >> 3) & 7;
-            const uint8_t *srcp = vst + ss * kStage + (ct >> 3) * 128 + ((k ^ rr) << 4);
-            // codes 16k .. 16k+15 -> f16 columns 16k .. 16k+15: 64-column half
-            // k / 4, 16-byte pieces 2 (k mod 4) and 2 (k mod 4) + 1
-            uint8_t *dstp = ring + fs * kChunk + (k >> 2) * 16384 + (ct >> 3) * 128;
-            const int o0 = ((2 * (k & 3)) ^ rr) << 4, o1 = ((2 * (k & 3) + 1) ^ rr) << 4;
-#pragma unroll
-            for (int i = 0; i < kStage / 16 / kConvThreads; ++i) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(srcp + i * (kConvThreads / 8) * 128);
-                uint4 a, c;
-                a.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xFFFF));
-                a.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
-                a.z = e4m3x2_to_f16x2((uint16_t)(w.y & 0xFFFF));
-                a.w = e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
-                c.x = e4m3x2_to_f16x2((uint16_t)(w.z & 0xFFFF));
-                c.y = e4m3x2_to_f16x2((uint16_t)(w.z >> 16));
-                c.z = e4m3x2_to_f16x2((uint16_t)(w.w & 0xFFFF));
-                c.w = e4m3x2_to_f16x2((uint16_t)(w.w >> 16));
-                *reinterpret_cast<uint4 *>(dstp + i * (kConvThreads / 8) * 128 + o0) = a;
-                *reinterpret_cast<uint4 *>(dstp + i * (kConvThreads / 8) * 128 + o1) = c;
-            }
-            // the MMA reads the ring through the async proxy; TMA then
-            // refills the staging slot
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&vf_full[fs]);
-                mbar_arrive(&vst_empty[ss]);
-            }
-            ++n;
-            return true;
-        };
         // the piece's q rows as E4M3 hi / lo parts, swizzled K-major rows
         // (hi of head g in row g, lo in row NP + g), and 2^-c per head
-        auto load_q = [&](const TileIter &it) -> bool {
-            const int qs = piece & 1;
-            if (piece >= 2 && !wwait(&q_empty[qs], (uint32_t)(((piece >> 1) - 1) & 1)))
-                return false;
-            const int kvh = it.seg / p.head_groups, hg = it.seg % p.head_groups;
-            const int h0 = kvh * p.G + hg * p.heads_per_seg;
-            const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
-            uint8_t *qb = qbuf + qs * C::QB;
-            for (int g = cw; g < NP; g += CW) {
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
-                if (g < gvalid) {  // lane l holds columns 4l .. 4l + 3
-                    const uint2 raw = reinterpret_cast<const uint2 *>(
-                        p.q)[((size_t)it.b * p.Hq + h0 + g) * (D / 4) + lane];
-                    x[0] = __uint_as_float(raw.x << 16);
-                    x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-                    x[2] = __uint_as_float(raw.y << 16);
-                    x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+        for (long long r = 0; r < ntiles && ok; ++r) {
+            if (r == 0 || itq.t == 0) {
+                const int qs = piece & 1;
+                if (piece >= 2) {
+                    bool w = true;
+                    if (lane == 0) w = wait_bar(&q_empty[qs], (uint32_t)(((piece >> 1) - 1) & 1), abort_flag);
+                    ok = __shfl_sync(0xffffffffu, w, 0);
+                    if (!ok) break;
                 }
-                float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+                const int kvh = itq.seg / p.head_groups, hg = itq.seg % p.head_groups;
+                const int h0 = kvh * p.G + hg * p.heads_per_seg;
+                const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
+                uint8_t *qb = qbuf + qs * C::QB;
+                for (int g = qw; g < NP; g += kQWarps) {
+                    float x[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (g < gvalid) {  // lane l holds columns 4l .. 4l + 3
+                        const uint2 raw = reinterpret_cast<const uint2 *>(
+                            p.q)[((size_t)itq.b * p.Hq + h0 + g) * (D / 4) + lane];
+                        x[0] = __uint_as_float(raw.x << 16);
+                        x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+                        x[2] = __uint_as_float(raw.y << 16);
+                        x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+                    }
+                    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+                    amax = warp_max(amax);
+                    // c = 7 - floor(log2 amax), kept where 2^c and 2^-c are normal
+                    int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+                    e = max(-119, min(e, 120));
+                    const float sc = pow2i(7 - e);
+                    float y[4];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                // c = 7 - floor(log2 amax), kept where 2^c and 2^-c are normal
-                int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-                e = max(-119, min(e, 120));
-                const float sc = __uint_as_float((uint32_t)(127 + 7 - e) << 23);
-                float y[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) y[u] = x[u] * sc;  // exact: a power of two
-                const uint16_t h01 = e4m3x2_of(y[0], y[1]), h23 = e4m3x2_of(y[2], y[3]);
-                const float2 v01 = e4m3x2_value(h01), v23 = e4m3x2_value(h23);
-                const uint16_t l01 = e4m3x2_of(y[0] - v01.x, y[1] - v01.y);
-                const uint16_t l23 = e4m3x2_of(y[2] - v23.x, y[3] - v23.y);
-                const int off = (((lane >> 2) ^ (g & 7)) << 4) + 4 * (lane & 3);
-                *reinterpret_cast<uint32_t *>(qb + g * 128 + off) = (uint32_t)h01 | ((uint32_t)h23 << 16);
-                *reinterpret_cast<uint32_t *>(qb + (NP + g) * 128 + off) = (uint32_t)l01 | ((uint32_t)l23 << 16);
-                if (lane == 0)
-                    qinv_s[qs * 64 + g] = (g < gvalid) ? __uint_as_float((uint32_t)(127 - 7 + e) << 23) : 0.f;
+                    for (int u = 0; u < 4; ++u) y[u] = x[u] * sc;  // exact: a power of two
+                    const uint16_t h01 = e4m3x2_of(y[0], y[1]), h23 = e4m3x2_of(y[2], y[3]);
+                    const float2 v01 = e4m3x2_value(h01), v23 = e4m3x2_value(h23);
+                    const uint16_t l01 = e4m3x2_of(y[0] - v01.x, y[1] - v01.y);
+                    const uint16_t l23 = e4m3x2_of(y[2] - v23.x, y[3] - v23.y);
+                    const int off = (((lane >> 2) ^ (g & 7)) << 4) + 4 * (lane & 3);
+                    *reinterpret_cast<uint32_t *>(qb + g * 128 + off) = (uint32_t)h01 | ((uint32_t)h23 << 16);
+                    *reinterpret_cast<uint32_t *>(qb + (NP + g) * 128 + off) = (uint32_t)l01 | ((uint32_t)l23 << 16);
+                    if (lane == 0) qinv_s[qs * 64 + g] = (g < gvalid) ? pow2i(e - 7) : 0.f;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[qs]);
+                ++piece;
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&q_full[qs]);
-            ++piece;
-            return true;
-        };
-        for (long long r = 0; r <= ntiles && ok; ++r) {
-            if (r < ntiles) {
-                if (r == 0 || itq.t == 0) ok = load_q(itq);
-                itq.next();
-            }
-            if (r >= 1 && ok) ok = convert();
+            itq.next();
         }
         if (!ok && lane == 0) {
             set_error(p.err, DEV_ERR_TIMEOUT);
@@ -377,34 +339,36 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
             bool ok = true;
             while (ip < ntiles) {
                 bool did = false;
-                if (ip < iq) {  // P V of tile ip
+                if (ip < iq) {  // P V of tile ip: 32 positions per MMA, the 3 P parts side by side
                     const long long j = ip;
                     const int pb = (int)(j & 1);
                     const bool first_pv = (j == 0) || (itp.t == 0);
                     bool ready = mbar_test(&p_full[pb], (uint32_t)((j >> 1) & 1));
                     if (ready && first_pv && piece_pv > 0)
                         ready = mbar_test(o_free, (uint32_t)((piece_pv - 1) & 1));
-                    const int slot = (int)(j % NB);
-                    if (ready) ready = mbar_test(&vf_full[slot], (uint32_t)((j / NB) & 1));
+                    const int slot = (int)(j % NSV);
+                    if (ready) ready = mbar_test(&vst_full[slot], (uint32_t)((j / NSV) & 1));
                     if (ready) {
                         if (first_pv) ++piece_pv;
                         tc_fence_after();
                         const uint32_t pstage = pbuf_s + (int)(j % C::PST) * C::PB;
-                        const uint32_t v0 = ring_s + slot * kChunk;
+                        const uint32_t v0 = vst_s + slot * kStage;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t ad = smem_desc(v0 + kk * 2048, 16384, 1024, 2);
-                            const uint64_t bd = smem_desc(pstage + kk * 256, 128, (kT / 8) * 128, 0);
-                            umma_bf16(tmem + 2 * NP, ad, bd, C::IDESC_PV, !(first_pv && kk == 0));
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // A = V^T: the staged tile read position-major (SW128);
+                            // B = P: position-major, no swizzle, 16-column blocks
+                            const uint64_t ad = smem_desc(v0 + kk * 4096, 16384, 1024, 2);
+                            const uint64_t bd = smem_desc(pstage + kk * 512, 128, 2048, 0);
+                            umma_f8(tmem + C::OA, ad, bd, C::IDESC_PV, !(first_pv && kk == 0));
                         }
-                        umma_commit(&vf_empty[slot]);
+                        umma_commit(&vst_empty[slot]);
                         umma_commit(&pv_done[pb]);
                         if (j < ntiles - 1) itp.next();
                         ++ip;
                         did = true;
                     }
                 }
-                if (iq < ntiles) {  // Q K^T of tile iq: hi part, then lo part
+                if (iq < ntiles) {  // Q K^T of tile iq
                     const long long i = iq;
                     const int sb = (int)(i & 1);
                     const bool first_q = (i == 0) || (itq.t == 0);
@@ -422,11 +386,11 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
                         const uint32_t a0 = kst_s + slot * kStage;
                         const uint32_t b0 = qbuf_s + qcur * C::QB;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {  // 32 codes per MMA
+                        for (int kk = 0; kk < (C::SBS ? 4 : 8); ++kk) {  // 32 codes per MMA
                             const uint64_t ad = smem_desc(a0 + (kk & 3) * 32, 16, 1024, 2);
                             const uint64_t bd =
                                 smem_desc(b0 + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024, 2);
-                            umma_f8(tmem + sb * NP, ad, bd, C::IDESC_QK, kk != 0);
+                            umma_f8(tmem + sb * C::SW, ad, bd, C::IDESC_QK, kk != 0);
                         }
                         umma_commit(&kst_empty[slot]);
                         umma_commit(&s_full[sb]);
@@ -495,10 +459,12 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
         const long long i0 = i;
         const int qs = spiece & 1;
         const float *qinv = qinv_s + qs * 64;
+        int cv = kCvNone;  // the piece's V weights run in units of 2^-cv (same in every thread)
+        float vsf = 0.f;   // 2^cv
 #pragma unroll
         for (int g = 0; g < NP; ++g) l[g] = 0.f;
         if (row < NP) mref_s[row] = -INFINITY;
-        // the piece's 2^-c (written by the converters)
+        // the piece's 2^-c (written by warps 6-7)
         carry_fail = carry_fail || !wait_bar(&q_full[qs], (uint32_t)((spiece >> 1) & 1), abort_flag);
         named_bar_sync(kBarSoftmax, 128);
 
@@ -517,19 +483,27 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
             tc_fence_after();
             float s[NP];
 #pragma unroll
-            for (int c = 0; c < NP / 16; ++c) {
+            for (int c = 0; c < NP / 16; ++c) {  // hi-part scores (all of it when not side by side)
                 float v[16];
-                tmem_ld16(lane_base + sb * NP + c * 16, v);
+                tmem_ld16(lane_base + sb * C::SW + c * 16, v);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) s[c * 16 + k] = v[k];
             }
             tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < (C::SBS ? NP / 16 : 0); ++c) {  // plus the lo-part scores
+                float v[16];
+                tmem_ld16(lane_base + sb * C::SW + NP + c * 16, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) s[c * 16 + k] += v[k];
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[sb]);
 
             const float sl = p.scale_log2 * ksc;
-            bool over = false;
+            bool over = vsc * vsf > kVHi;
 #pragma unroll
             for (int g = 0; g < NP; g += 4) {
                 const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g);
@@ -538,8 +512,8 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
                 s[g + 1] = valid ? s[g + 1] * (c4.y * sl) : -INFINITY;
                 s[g + 2] = valid ? s[g + 2] * (c4.z * sl) : -INFINITY;
                 s[g + 3] = valid ? s[g + 3] * (c4.w * sl) : -INFINITY;
-                over |= (s[g] > m4.x + kTau) | (s[g + 1] > m4.y + kTau) |
-                        (s[g + 2] > m4.z + kTau) | (s[g + 3] > m4.w + kTau);
+                over |= (s[g] > m4.x + kTauQ8) | (s[g + 1] > m4.y + kTauQ8) |
+                        (s[g + 2] > m4.z + kTauQ8) | (s[g + 3] > m4.w + kTauQ8);
             }
             if (named_bar_sync_or(kBarSoftmax, 128, over || fail)) {
                 if (named_bar_sync_or(kBarSoftmax, 128, fail || *abort_flag != 0)) {
@@ -547,6 +521,8 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
                     break;
                 }
                 warp_cols_np<NP>(s, red + q4 * 64, lane, OpMax());
+                const float vm = warp_max(vsc);  // 0 on rows past the length
+                if (lane == 0) vred_s[q4] = vm;
                 named_bar_sync(kBarSoftmax, 128);
                 if (row < NP) {
                     const int g = row;
@@ -558,6 +534,24 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
                                                                          : fast_exp2(m_old - m_new);
                     mref_s[g] = m_new;
                 }
+                // the V unit: the tile's largest v_scale times 2^cv in [32, 64),
+                // lowered only (the accumulator follows by the same power of two)
+                const float tv = fmaxf(fmaxf(vred_s[0], vred_s[1]), fmaxf(vred_s[2], vred_s[3]));
+                float fv = 1.f;
+                if (tv > 0.f) {
+                    int e = (int)((__float_as_uint(tv) >> 23) & 0xFF) - 127;
+                    e = max(-120, min(e, 127));
+                    const int cn = 5 - e;
+                    if (cv == kCvNone) {
+                        cv = cn;
+                    } else if (cn < cv) {
+                        fv = ldexpf(1.f, cn - cv);
+                        cv = cn;
+                    }
+                } else if (cv == kCvNone) {
+                    cv = 0;
+                }
+                vsf = pow2i(cv);
                 named_bar_sync(kBarSoftmax, 128);
 #pragma unroll
                 for (int g = 0; g < NP; ++g) l[g] *= alpha_s[g];
@@ -567,21 +561,23 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
                         fail = true;
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < NP / 16; ++c) {
+                    for (int c = 0; c < 3 * NP / 16; ++c) {
                         float v[16];
-                        const uint32_t a = lane_base + 2 * NP + c * 16;
+                        const uint32_t a = lane_base + C::OA + c * 16;
                         tmem_ld16(a, v);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) v[k] *= alpha_s[c * 16 + k];
+                        for (int k = 0; k < 16; ++k) v[k] *= alpha_s[(c * 16 + k) % NP] * fv;
                         tmem_st16(a, v);
                     }
                     tmem_st_wait();
                 }
             }
 
-            // probabilities p (summed into l) times the row's V scale, as f16
-            uint32_t pk[NP / 2];
+            // probabilities p (summed into l); the weights p v_scale 2^cv as
+            // three E4M3 parts, each the rounded remainder of the previous
+            const float vs2 = vsc * vsf;
+            uint32_t ph[NP / 4], pm[NP / 4], pl[NP / 4];
 #pragma unroll
             for (int g4 = 0; g4 < NP; g4 += 4) {
                 const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g4);
@@ -593,8 +589,22 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
                     const float p1 = (s[g + 1] == -INFINITY) ? 0.f : fast_exp2(s[g + 1] - mm[h + 1]);
                     l[g] += p0;
                     l[g + 1] += p1;
-                    const __half2 h2 = __floats2half2_rn(p0 * vsc, p1 * vsc);
-                    pk[g / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+                    const float w0 = p0 * vs2, w1 = p1 * vs2;
+                    const uint16_t c1 = e4m3x2_of(w0, w1);
+                    const float2 d1 = e4m3x2_value(c1);
+                    const float r0 = w0 - d1.x, r1 = w1 - d1.y;
+                    const uint16_t c2 = e4m3x2_of(r0, r1);
+                    const float2 d2 = e4m3x2_value(c2);
+                    const uint16_t c3 = e4m3x2_of(r0 - d2.x, r1 - d2.y);
+                    if (h == 0) {
+                        ph[g4 / 4] = c1;
+                        pm[g4 / 4] = c2;
+                        pl[g4 / 4] = c3;
+                    } else {
+                        ph[g4 / 4] |= (uint32_t)c1 << 16;
+                        pm[g4 / 4] |= (uint32_t)c2 << 16;
+                        pl[g4 / 4] |= (uint32_t)c3 << 16;
+                    }
                 }
             }
             if (i >= C::PST) {
@@ -602,11 +612,18 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
                 if (!wait_bar(&pv_done[jp & 1], (uint32_t)((jp >> 1) & 1), abort_flag))
                     fail = true;
             }
+            // P stage: column block n / 16 at 2048 n / 16, position row at
+            // 128 (row / 8) + 16 (row mod 8); columns hi 0..NP-1, mid, lo
             uint8_t *pdst = pbuf + (int)(i % C::PST) * C::PB + (row >> 3) * 128 + (row & 7) * 16;
 #pragma unroll
-            for (int c = 0; c < NP / 8; ++c)
-                *reinterpret_cast<uint4 *>(pdst + c * (kT / 8) * 128) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            for (int c = 0; c < NP / 16; ++c) {
+                *reinterpret_cast<uint4 *>(pdst + c * 2048) =
+                    make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+                *reinterpret_cast<uint4 *>(pdst + (NP / 16 + c) * 2048) =
+                    make_uint4(pm[4 * c], pm[4 * c + 1], pm[4 * c + 2], pm[4 * c + 3]);
+                *reinterpret_cast<uint4 *>(pdst + (2 * NP / 16 + c) * 2048) =
+                    make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -634,14 +651,17 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
         named_bar_sync(kBarSoftmax, 128);
         const bool complete = (t0 == 0) && it.last_tile_of_segment();
         const size_t slot = 2 * (size_t)blockIdx.x + (first_piece ? 0 : 1);
+        const float vinv = (cv == kCvNone) ? 1.f : ldexpf(1.f, -cv);
         float o[NP];
 #pragma unroll
-        for (int c = 0; c < NP / 16; ++c) {
-            float v[16];
-            tmem_ld16(lane_base + 2 * NP + c * 16, v);
+        for (int c = 0; c < NP / 16; ++c) {  // O^T = (hi + mid + lo parts) 2^-cv
+            float v[16], w[16], x[16];
+            tmem_ld16(lane_base + C::OA + c * 16, v);
+            tmem_ld16(lane_base + C::OA + NP + c * 16, w);
+            tmem_ld16(lane_base + C::OA + 2 * NP + c * 16, x);
             tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[c * 16 + k] = v[k];
+            for (int k = 0; k < 16; ++k) o[c * 16 + k] = (v[k] + w[k] + x[k]) * vinv;
         }
         const int d = row;
         if (complete) {
@@ -680,20 +700,19 @@ __global__ void __launch_bounds__(kQ8Threads<CW>, 1)
 template <int NP>
 cudaError_t launch_q8(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeParams &p,
                       int num_ctas, cudaStream_t stream) {
-    constexpr int CW = kConvWarps<NP>;
     static int done_for_device[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (!(dev >= 0 && dev < 64 && done_for_device[dev])) {
-        e = cudaFuncSetAttribute(decode_q8_kernel<NP, CW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_q8_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Q8Cfg<NP>::alloc);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) done_for_device[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_ctas);
-    cfg.blockDim = dim3(kQ8Threads<CW>);
+    cfg.blockDim = dim3(kQ8Threads);
     cfg.dynamicSmemBytes = Q8Cfg<NP>::alloc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -701,7 +720,7 @@ cudaError_t launch_q8(const CUtensorMap &tmk, const CUtensorMap &tmv, const Deco
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_q8_kernel<NP, CW>, tmk, tmv, p);
+    return cudaLaunchKernelEx(&cfg, decode_q8_kernel<NP>, tmk, tmv, p);
 }
 
 }  // namespace

@@ -267,8 +267,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 
 // Instruction descriptor for kind::f8f6f4 with E4M3 A/B (format code 0 in
 // both fields) and fp32 D: the same bits as f16 A/B under kind::f16.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major,
+                                                      bool b_mn_major) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor for kind::f16 with f16 A/B and fp32 D.

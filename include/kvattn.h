@@ -321,8 +321,9 @@ KVATTN_API int kv_append_fp8(void *k_codes, void *v_codes, float *k_scale, float
 /* gqa_decode_attn_fp8 -- gqa_decode_attn over an 8-bit cache: K[b,kvh,j,:] =
  * E4M3(k_codes[b,kvh,j,:]) * k_scale[b,kvh,j], V likewise.  The cache read
  * per position and K/V head is 2 (D + 4) bytes instead of 4 D.  q bf16
- * [B, Hq, D] (entries beyond +-65504 saturate: the products run in f16),
- * out fp32 [B, Hq, D]; lengths, errors and ownership as gqa_decode_attn.
+ * [B, Hq, D] (any finite value: each head enters the 8-bit products as two
+ * E4M3 parts under a power-of-two scale, exact for a bf16 value), out fp32
+ * [B, Hq, D]; lengths, errors and ownership as gqa_decode_attn.
  * Needs D = 128 (KVATTN_ERR_UNSUPPORTED otherwise).  Rows at and past
  * seq_lens[b], codes and scales, are never read. */
 KVATTN_API int gqa_decode_attn_fp8(const void *q, const void *k_codes, const void *v_codes,
