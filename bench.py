@@ -59,6 +59,27 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(seed, rank):
+    """Each rank draws its own batch: the ranks run independent problems
+    (weak scaling, no data-path exchange)."""
+    return seed + 1000 * rank
+
+
+def over_ranks(ms_total, units, world, device):
+    """Whole-job timing over the ranks: the slowest rank's elapsed time and
+    the units (KV bytes of the timed steps) that all ranks processed.  With
+    one rank, the inputs unchanged."""
+    if world <= 1:
+        return float(ms_total), float(units)
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(ms_total)], dtype=torch.float64, device=device)
+    uu = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    dist.all_reduce(uu, op=dist.ReduceOp.SUM)
+    return float(tt.item()), float(uu.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -320,15 +341,15 @@ def gpu_arm(a, w):
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     cache_bytes = 2 * w.B * w.Hkv * w.Lmax * w.D * 2
-    read_bytes = accounting.kv_bytes_read(wl.attn_lens(w, a.seed + 1000 * rank).tolist(),
+    read_bytes = accounting.kv_bytes_read(wl.attn_lens(w, rank_seed(a.seed, rank)).tolist(),
                                           w.Hkv, w.D, window=w.window)
     ncopies = max(1, int(math.ceil(4 * l2 / read_bytes)))
     ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
-    x = wl.make_inputs(w, seed=a.seed + 1000 * rank, device=dev)
+    x = wl.make_inputs(w, seed=rank_seed(a.seed, rank), device=dev)
     table = None
     if w.block_size:
         # paged: the pools hold only the blocks the sequences use, scattered
-        pg = wl.make_paged(w, x, seed=a.seed + 1000 * rank)
+        pg = wl.make_paged(w, x, seed=rank_seed(a.seed, rank))
         del x["k_cache"], x["v_cache"]
         x["k_cache"], x["v_cache"], table = pg["k_pool"], pg["v_pool"], pg["block_table"]
         cache_bytes = 2 * x["k_cache"].numel() * 2
@@ -444,12 +465,9 @@ def gpu_arm(a, w):
     g.check_device_error(stream)
     ms_total = t0.elapsed_time(t1)
     local_ms_step = ms_total / a.steps
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total, job_bytes = over_ranks(ms_total, kv_bytes * a.steps, world, dev)
     ms_step = ms_total / a.steps
-    value = world * kv_bytes * a.steps / (ms_total / 1e3) / 1e9
+    value = job_bytes / (ms_total / 1e3) / 1e9
     # average duration of one step's launch over the timed region
     achieved = kv_bytes / (local_ms_step / 1e3) / 1e9
 
@@ -519,7 +537,8 @@ def gpu_arm(a, w):
         e1.record(stream)
     stream.synchronize()
     e2e_ms = e0.elapsed_time(e1) / n_e2e
-    e2e_val = world * kv_bytes / (e2e_ms / 1e3) / 1e9
+    e2e_ms, e2e_bytes = over_ranks(e2e_ms, kv_bytes, world, dev)
+    e2e_val = e2e_bytes / (e2e_ms / 1e3) / 1e9
     g.check_device_error(stream)
 
     traffic = stored_traffic(w.name)
