@@ -471,71 +471,97 @@ def gpu_arm(a, w):
     # average duration of one step's launch over the timed region
     achieved = kv_bytes / (local_ms_step / 1e3) / 1e9
 
-    # ---- end to end through the public Python API with host buffers
-    hq = x["q"].cpu().pin_memory()
-    hkn = x["k_new"].cpu().pin_memory()
-    hvn = x["v_new"].cpu().pin_memory()
-    hpos = pos.cpu().pin_memory()
-    hout = torch.empty_like(out, device="cpu").pin_memory()
-    dq, dkn, dvn = torch.empty_like(x["q"]), torch.empty_like(x["k_new"]), torch.empty_like(x["v_new"])
-    dpos = torch.empty_like(pos)
-    n_e2e = max(1, a.e2e_steps)
-    hlens = lens.cpu().pin_memory()
-    dlens = torch.empty_like(lens)
-    # bytes each e2e step moves, counted from the tensors it copies
-    inputs_h = (hq, hlens) if w.T > 1 else (hq, hkn, hvn, hpos)
-    if fp8:
-        inputs_h = (hq, hkn, hvn, hpos, hlens)
+    # ---- spread of the step time, outside the timed region: events around
+    # each replay of the ncopies-step chain
+    reps = max(20, min(400, 4000 // ncopies))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for k in range(reps):
+            chain.replay()
+            evs[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    per = sorted(1e3 * evs[k].elapsed_time(evs[k + 1]) / ncopies for k in range(reps))
+    spread = {"p10": per[reps // 10], "p50": per[reps // 2], "p90": per[(9 * reps) // 10],
+              "over": "%d replays of the %d-step chain (us per step)" % (reps, ncopies)}
+
+    # ---- end to end through the public Python API with host buffers.  A
+    # step's inputs go up from pinned host memory in ONE copy (the tensors
+    # packed side by side at 256-byte offsets) and its output comes back in
+    # one copy.  Uploads and downloads run on streams of their own with two
+    # buffer sets, so step i's upload and step i-1's download overlap the
+    # kernels of the steps around them, as a serving loop would run them.
+    if w.T > 1:
+        send = [("q", x["q"]), ("lens", lens)]
+    elif fp8:
+        send = [("q", x["q"]), ("k_new", x["k_new"]), ("v_new", x["v_new"]),
+                ("pos", pos), ("lens", lens)]
+    else:
+        send = [("q", x["q"]), ("k_new", x["k_new"]), ("v_new", x["v_new"]), ("pos", pos)]
     if table is not None:
-        # a paged server sends the block table with every step
-        htable = table.cpu().pin_memory()
-        dtable = torch.empty_like(table)
-        inputs_h = inputs_h + (htable,)
-    io = {"h2d": sum(t.numel() * t.element_size() for t in inputs_h),
-          "d2h": hout.numel() * hout.element_size()}
+        send.append(("table", table))  # a paged server sends the block table with every step
+    layout, nbuf = [], 0
+    for name, t in send:
+        nb = t.numel() * t.element_size()
+        layout.append((name, nbuf, nb, t.dtype, tuple(t.shape)))
+        nbuf += (nb + 255) // 256 * 256
+    hbuf = torch.empty(nbuf, dtype=torch.uint8).pin_memory()
+    for (name, o, nb, _, _), (_, t) in zip(layout, send):
+        hbuf[o:o + nb].copy_(t.detach().cpu().contiguous().reshape(-1).view(torch.uint8))
+    dbufs = [torch.empty(nbuf, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dviews = [{name: db[o:o + nb].view(dt).view(shp) for name, o, nb, dt, shp in layout}
+              for db in dbufs]
+    outs = [out, torch.empty_like(out)]
+    houts = [torch.empty_like(out, device="cpu").pin_memory() for _ in range(2)]
+    io = {"h2d": sum(nb for _, _, nb, _, _ in layout),
+          "d2h": houts[0].numel() * houts[0].element_size()}
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)]
+          for k in ("in_ready", "in_free", "out_ready", "out_free")}
+    n_e2e = max(1, a.e2e_steps)
 
     def e2e_step(i):
+        s = i % 2
+        v, o = dviews[s], outs[s]
+        up.wait_event(ev["in_free"][s])          # step i-2's kernels are done with this set
+        with torch.cuda.stream(up):
+            dbufs[s].copy_(hbuf, non_blocking=True)
+            ev["in_ready"][s].record(up)
+        stream.wait_event(ev["in_ready"][s])
+        stream.wait_event(ev["out_free"][s])     # step i-2's output has been read back
         r = i % ncopies
-        dq.copy_(hq, non_blocking=True)
+        c = caches[r]
         if w.T > 1:
-            dlens.copy_(hlens, non_blocking=True)
-            g.gqa_decode_attn_multi(dq, caches[r][0], caches[r][1], dlens, w.scale, out=out,
-                                    stream=stream)
+            g.gqa_decode_attn_multi(v["q"], c[0], c[1], v["lens"], w.scale, out=o, stream=stream)
         elif fp8:
-            dkn.copy_(hkn, non_blocking=True)
-            dvn.copy_(hvn, non_blocking=True)
-            dpos.copy_(hpos, non_blocking=True)
-            dlens.copy_(hlens, non_blocking=True)
-            c = caches[r]
-            g.kv_append_fp8(c[0], c[1], c[2], c[3], dkn, dvn, dpos, stream=stream)
-            g.gqa_decode_attn_fp8(dq, c[0], c[1], c[2], c[3], dlens, w.scale, out=out,
+            g.kv_append_fp8(c[0], c[1], c[2], c[3], v["k_new"], v["v_new"], v["pos"],
+                            stream=stream)
+            g.gqa_decode_attn_fp8(v["q"], c[0], c[1], c[2], c[3], v["lens"], w.scale, out=o,
                                   stream=stream)
         elif table is not None:
-            dkn.copy_(hkn, non_blocking=True)
-            dvn.copy_(hvn, non_blocking=True)
-            dpos.copy_(hpos, non_blocking=True)
-            dtable.copy_(htable, non_blocking=True)
-            g.gqa_decode_step_paged(dq, dkn, dvn, caches[r][0], caches[r][1], dtable, dpos,
-                                    w.scale, out=out, stream=stream)
+            g.gqa_decode_step_paged(v["q"], v["k_new"], v["v_new"], c[0], c[1], v["table"],
+                                    v["pos"], w.scale, out=o, stream=stream)
         else:
-            dkn.copy_(hkn, non_blocking=True)
-            dvn.copy_(hvn, non_blocking=True)
-            dpos.copy_(hpos, non_blocking=True)
-            g.gqa_decode_step(dq, dkn, dvn, caches[r][0], caches[r][1], dpos, w.scale, out=out,
-                              stream=stream, window=w.window)
-        hout.copy_(out, non_blocking=True)
+            g.gqa_decode_step(v["q"], v["k_new"], v["v_new"], c[0], c[1], v["pos"], w.scale,
+                              out=o, stream=stream, window=w.window)
+        ev["in_free"][s].record(stream)
+        ev["out_ready"][s].record(stream)
+        down.wait_event(ev["out_ready"][s])
+        with torch.cuda.stream(down):
+            houts[s].copy_(o, non_blocking=True)
+            ev["out_free"][s].record(down)
 
-    with torch.cuda.stream(stream):
-        for i in range(5):
-            e2e_step(i)
-    stream.synchronize()
+    for i in range(6):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(n_e2e):
-            e2e_step(i)
-        e1.record(stream)
-    stream.synchronize()
+    e0.record(up)
+    h0 = time.perf_counter()
+    for i in range(n_e2e):
+        e2e_step(i)
+    host_us = 1e6 * (time.perf_counter() - h0) / n_e2e  # host time to issue one step
+    e1.record(down)
+    torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / n_e2e
     e2e_ms, e2e_bytes = over_ranks(e2e_ms, kv_bytes, world, dev)
     e2e_val = e2e_bytes / (e2e_ms / 1e3) / 1e9
@@ -566,6 +592,7 @@ def gpu_arm(a, w):
                             "steps chained in CUDA graphs"),
                    "numerics": "bf16 in, fp32 accumulate and out",
                    "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
+        "us_per_step_spread": spread,
         "seq_steps_per_s": world * w.B * a.steps / (ms_total / 1e3),
         "tokens_scored_per_s": world * w.B * w.T * a.steps / (ms_total / 1e3),
         "bf16_equivalent_gbs": world * kv_bytes_bf16 * a.steps / (ms_total / 1e3) / 1e9,
@@ -587,7 +614,8 @@ def gpu_arm(a, w):
                      if peak_kind == "measured" else "fallback 6800 GB/s"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
                 "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms,
-                "api": "grouped_query_kv_gb300.%s (eager)"
+                "host_issue_us_per_step": host_us,
+                "api": "grouped_query_kv_gb300.%s (eager; one packed upload and one download per step on their own streams, double-buffered)"
                        % ("kv_append_fp8 + gqa_decode_attn_fp8" if fp8 else
                           "gqa_decode_step_paged" if table is not None else
                           "gqa_decode_attn_multi" if w.T > 1 else "gqa_decode_step")},

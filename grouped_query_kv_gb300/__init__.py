@@ -97,6 +97,9 @@ def library_path() -> str:
 def lib():
     """The loaded C library (raises if it has not been built)."""
     global _lib
+    h = _lib
+    if h is not None:  # per-call fast path: no lock once loaded
+        return h
     with _lock:
         if _lib is None:
             if not os.path.exists(_LIB_PATH):
@@ -125,27 +128,29 @@ def _check(status: int):
 
 
 def _stream_ptr(stream):
-    import torch
     if stream is None:
+        import torch
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream  # a plain int: ctypes converts it for the c_void_p argument
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _need(t, name, dtype, shape=None):
+    # the checks run on every call of a decode loop, so they use the cheapest
+    # torch attributes (is_cuda, dtype identity, torch.Size == tuple)
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor (got %s)" % (name, t.device))
-    if t.dtype != dtype:
+    if t.dtype is not dtype:
         raise TypeError("%s must be %s (got %s)" % (name, dtype, t.dtype))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != tuple(shape):
         raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
 
 
