@@ -512,7 +512,7 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         if ((rc = encode_cache_map(&tmv, v_cache, D, Lmax, B * Hkv, P.tile_positions))) return rc;
     }
 
-    DecodeParams p;
+    DecodeParams p = {};
     p.q = static_cast<const uint16_t *>(q);
     p.seq_lens = seq_lens;
     p.len_add = fused ? 1 : 0;
@@ -601,7 +601,7 @@ int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, cons
     if ((rc = encode_fp8_map(&tmk, k_codes, D, Lmax, B * Hkv, P.tile_positions))) return rc;
     if ((rc = encode_fp8_map(&tmv, v_codes, D, Lmax, B * Hkv, P.tile_positions))) return rc;
 
-    DecodeParams p;
+    DecodeParams p = {};
     memset(&p, 0, sizeof p);
     p.q = static_cast<const uint16_t *>(q);
     p.seq_lens = seq_lens;

@@ -110,7 +110,7 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
     if ((rc = api_encode_cache_maps(&tmk, &tmv, k_cache, v_cache, D, Lmax, B * Hkv, tile)))
         return rc;
 
-    DecodeParams p;
+    DecodeParams p = {};
     p.q = static_cast<const uint16_t *>(q);
     p.seq_lens = seq_lens;
     p.len_add = 0;
