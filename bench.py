@@ -197,18 +197,18 @@ class Clocks:
 
 # --------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, seed, target_s, max_seqs=None):
-    """Time the oracle (all host cores) on whole sequences of the workload:
-    as many sequences as fit in target_s (at most the whole batch), repeated
-    until target_s of CPU work has run.  Returns (seconds, sequences,
-    kv_bytes, threads, repetitions)."""
+def oracle_sample(w, seed, target_s, max_seqs=None, threads=None):
+    """Time the oracle (all host cores, or `threads` of them) on whole
+    sequences of the workload: as many sequences as fit in target_s (at most
+    the whole batch), repeated until target_s of CPU work has run.  Returns
+    (seconds, sequences, kv_bytes, threads, repetitions)."""
     import dataclasses
 
     import oracle
     from grouped_query_kv_gb300 import accounting
     from grouped_query_kv_gb300 import workloads as wl
 
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     lens_all = wl.attn_lens(w, seed)
 
     def inputs(nb):
@@ -628,6 +628,10 @@ def gpu_arm(a, w):
             "value": by / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": "%d of %d sequences (all heads) x %d repetitions, %.1f s, "
                       "double precision; %s" % (nb, w.B, reps, dt, cpu_model())}
+        dt1, nb1, by1, _, reps1 = oracle_sample(w, a.seed, a.cpu_seconds / 4, threads=1)
+        line["cpu_baseline"]["single_thread"] = {
+            "value": by1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+            "sample": "%d sequences x %d repetitions, %.1f s" % (nb1, reps1, dt1)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
