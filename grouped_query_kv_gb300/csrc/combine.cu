@@ -2,20 +2,22 @@
 // grid cut into several pieces (flash-decoding's cross-split log-sum-exp
 // combine):  m* = max_s m_s,  w_s = 2^(m_s - m*),
 //            out = sum_s w_s o_s / sum_s w_s l_s.
-// The split-KV kernel leaves one record per CTA; CTA c's record names a
-// segment when c is the first cut inside it.  Block (x, y) merges the
-// segment of record x, or of the x-th record that names one (found with a
-// block-wide ballot over the records), y picks a slice of 4 x kThreads of the segment's heads x D
-// outputs (four consecutive d per thread, as float4).  Each thread loads its
-// head's (m_s, l_s) and its own o_s for a batch of pieces at once -- all
-// independent loads, one round trip -- and forms the weights itself (the
-// (m, l) loads of a warp hit one or two addresses).  Batches after the first
-// fold in with an online rescale.  The grid has at most min(CTAs, segments)
-// rows, and few blocks: a large grid takes microseconds just to be placed.  Launched with programmatic
-// serialisation: it waits on the split-KV kernel with griddepcontrol.wait
-// instead of a full launch gap.
+// Block (x, y) merges one split segment: with fewer segments than CTAs, row
+// x is segment x, located from the lengths by the split-KV kernel's own cost
+// arithmetic before the wait on that kernel; otherwise row x reads CTA x's
+// record, which names a segment when x is the first cut inside it.  y picks
+// a slice of 4 x kThreads of the segment's heads x D outputs (four
+// consecutive d per thread, as float4).  Each thread loads its head's
+// (m_s, l_s) and its own o_s for a batch of pieces at once -- all independent
+// loads, one round trip -- and forms the weights itself (the (m, l) loads of
+// a warp hit one or two addresses).  Batches after the first fold in with an
+// online rescale.  The grid has at most min(CTAs, segments) rows, and few
+// blocks: a large grid takes microseconds just to be placed.  Launched with
+// programmatic serialisation: it waits on the split-KV kernel with
+// griddepcontrol.wait instead of a full launch gap.
 #include "internal.h"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 namespace kvattn {
 
@@ -30,49 +32,73 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// direct: block row c merges the segment CTA c's record names (rows whose
-// record names none exit at once); else block row x finds the x-th record
-// that names a segment.  The host takes direct rows unless they would mean
-// many more blocks (few long segments): placing blocks costs microseconds.
+// Where the split-KV kernel put segment s's pieces, from the lengths alone,
+// with the same cost arithmetic as its schedule (schedule.cuh): the first
+// contributing CTA c0, the number of pieces n (1: the segment was not split)
+// and the workspace slot of piece 0 -- 2 c0 when c0's range starts at the
+// segment's first tile, else 2 c0 + 1 (its last piece).  Called by a whole
+// warp; every lane gets the results.
+__device__ inline void segment_pieces(const DecodeParams &p, int s, int grid, int *c0, int *n,
+                                      int *first_slot) {
+    const int lane = threadIdx.x & 31;
+    const LenView lens{p.seq_lens, p.len_add, p.window};
+    const int segs_per_b = p.Hkv * p.head_groups;
+    const SchedCost w{p.cost_piece};
+    long long total, cost;
+    int ctas_eff;
+    sched_totals(lens, p.B, p.Lmax, p.tile, segs_per_b, w, grid, &total, &cost, &ctas_eff);
+    const int b = s / segs_per_b, sg = s % segs_per_b;
+    int before = 0;  // tiles of one segment of every sequence before b
+    for (int bb = lane; bb < b; bb += 32) before += seq_ntiles(lens[bb], p.Lmax, p.tile, lens.window);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    const int nt = seq_ntiles(lens[b], p.Lmax, p.tile, lens.window);
+    const long long cost0 = (long long)segs_per_b * ((long long)before * kCostTile + (long long)w.P * b) +
+                            (long long)sg * ((long long)nt * kCostTile + w.P);
+    const long long last = cost0 + (nt == 1 ? 0 : w.P + (long long)kCostTile * (nt - 1));
+    const int c = sched_owner(cost0, cost, ctas_eff);
+    bool starts = true;  // c's range starts at this segment's first tile
+    if (s > 0) {
+        // the tile before: the last of the previous segment
+        const int ntp = sg > 0 ? nt : seq_ntiles(lens[b - 1], p.Lmax, p.tile, lens.window);
+        const long long prev = cost0 - kCostTile - (ntp == 1 ? w.P : 0);
+        starts = prev < sched_bound(cost, ctas_eff, c);
+    }
+    *c0 = c;
+    *n = sched_owner(last, cost, ctas_eff) - c + 1;
+    *first_slot = 2 * c + (starts ? 0 : 1);
+}
+
+// by_segment: block row s merges segment s, whose pieces it locates from the
+// lengths before waiting on the split-KV kernel (the lengths are an input of
+// the call, written before that kernel started, so only the partials are
+// waited for); else block row c merges the segment CTA c's record names
+// (rows whose record names none exit at once).  The host takes rows by
+// segment when there are fewer segments than CTAs: few rows, and no record
+// load between the wait and the partials' loads.
 __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p, int num_ctas,
-                                                           int direct) {
-    __shared__ int s_wcount[kThreads / 32];
-    __shared__ int s_owner;
+                                                           int by_segment) {
     // the next kernel in the stream may start its prologue while this one
     // runs; it waits for these writes with its own griddepcontrol.wait
     pdl_launch_dependents();
-    pdl_wait_prior();  // partials and records come from the split-KV kernel just before
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int4 *recs = reinterpret_cast<const int4 *>(p.split);
 
     int c = (int)blockIdx.x;
-    if (direct) {
-        if (recs[c].x < 0) return;
+    int4 rec;
+    if (by_segment) {
+        int c0, n, fs;
+        segment_pieces(p, (int)blockIdx.x, num_ctas, &c0, &n, &fs);
+        if (n <= 1) return;  // not split: the split-KV kernel wrote this segment's rows
+        const int segs_per_b = p.Hkv * p.head_groups;
+        rec = make_int4((int)blockIdx.x / segs_per_b, (int)blockIdx.x % segs_per_b, fs, n);
+        c = c0 + 1;
+        pdl_wait_prior();  // the partials come from the split-KV kernel just before
     } else {
-        // the blockIdx.x-th CTA whose record names a segment
-        if (tid == 0) s_owner = -1;
-        int seen = 0;
-        for (int base = 0; base < num_ctas; base += kThreads) {
-            const int cc = base + tid;
-            const bool own = cc < num_ctas && recs[cc].x >= 0;
-            const unsigned m = __ballot_sync(0xffffffffu, own);
-            if (lane == 0) s_wcount[warp] = __popc(m);
-            __syncthreads();
-            int before = seen, total = 0;
-            for (int w = 0; w < kThreads / 32; ++w) {
-                if (w < warp) before += s_wcount[w];
-                total += s_wcount[w];
-            }
-            if (own && before + __popc(m & ((1u << lane) - 1u)) == (int)blockIdx.x) s_owner = cc;
-            __syncthreads();
-            seen += total;
-            if (seen > (int)blockIdx.x) break;
-        }
-        c = s_owner;
-        if (c < 0) return;
+        pdl_wait_prior();  // partials and records come from the split-KV kernel just before
+        if (recs[c].x < 0) return;  // CTA c is not the first cut inside a segment
+        rec = recs[c];
     }
-
-    const int4 rec = recs[c];
     const int b = rec.x, seg = rec.y, first_slot = rec.z, npieces = rec.w;
     const int kvh = seg / p.head_groups;
     const int hg = seg % p.head_groups;
@@ -137,11 +163,12 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
 }  // namespace
 
 cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream) {
-    // at most one owner per segment, and at most one per CTA
+    // rows: one per segment when segments are fewer than CTAs, else one per
+    // CTA record (at most one owner per segment, and at most one per CTA)
     const long long segs = (long long)p.B * p.Hkv * p.head_groups;
     const int ycount = (p.heads_per_seg * p.D / 4 + kThreads - 1) / kThreads;
-    const int direct = (segs >= num_ctas || (long long)num_ctas * ycount <= 1024) ? 1 : 0;
-    const int rows = direct ? num_ctas : (int)(segs < num_ctas ? segs : num_ctas);
+    const int by_segment = segs < num_ctas ? 1 : 0;
+    const int rows = by_segment ? (int)segs : num_ctas;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(rows, ycount);
     cfg.blockDim = dim3(kThreads);
@@ -152,7 +179,7 @@ cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t str
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, p, num_ctas, direct);
+    return cudaLaunchKernelEx(&cfg, combine_kernel, p, num_ctas, by_segment);
 }
 
 }  // namespace kvattn
