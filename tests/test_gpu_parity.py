@@ -183,6 +183,22 @@ def test_non_finite_padding_is_never_used(path):
     assert_close(out, ref, bits(x["v_cache"]), lens_np)
 
 
+@pytest.mark.parametrize("ctas", [15, 16, 17, 40])
+def test_combine_rows_by_segment_and_by_record(ctas):
+    # 16 segments: with more CTAs than segments the combine locates each
+    # segment's pieces from the lengths (before waiting on the split-KV
+    # kernel), otherwise it reads the CTAs' records; both must merge alike,
+    # with ragged and one-tile sequences among the split ones
+    w = wl.Workload("rows", B=16, Hq=8, Hkv=1, D=128, Lmax=3000, scale=0.1,
+                    lens=(3000, 1, 2, 2999, 128, 129, 1500, 257, 3000, 64, 700, 2048, 5, 1000,
+                          2500, 1777))
+    g.set_tuning(2, ctas)
+    try:
+        run_step(w, seed=ctas)
+    finally:
+        g.set_tuning(0, 0)
+
+
 @pytest.mark.parametrize("ctas", [1, 3, 152, 600])
 def test_tensor_core_split_pieces(ctas):
     w = wl.Workload("tcsplit", B=3, Hq=48, Hkv=1, D=256, Lmax=5000, scale=1 / 16,
