@@ -19,7 +19,7 @@ __all__ = [
     "gqa_decode_attn_multi", "gqa_decode_attn_paged", "gqa_decode_step_paged",
     "kv_quantize_fp8", "kv_append_fp8", "gqa_decode_attn_fp8",
     "check_device_error", "get_plan",
-    "set_tuning", "release", "KvAttnError", "library_path", "lib",
+    "set_tuning", "set_wait_limit", "set_kernel_events", "release", "KvAttnError", "library_path", "lib",
     "KVATTN_OK", "KVATTN_ERR_INVALID_ARG", "KVATTN_ERR_UNSUPPORTED",
     "KVATTN_ERR_CUDA", "KVATTN_ERR_OOM", "KVATTN_ERR_DEVICE_BOUNDS",
     "KVATTN_ERR_TIMEOUT", "EXPORTED_SYMBOLS",
@@ -85,6 +85,8 @@ _SIGS = {
     "kvattn_check_device_error": (_I, [_VP]),
     "kvattn_release": (None, []),
     "kvattn_set_tuning": (_I, [_I, _I]),
+    "kvattn_set_wait_limit": (_I, [ctypes.c_uint]),
+    "kvattn_set_kernel_events": (_I, [_VP, _VP]),
     "kvattn_get_plan": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(kvattn_plan)]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -479,6 +481,25 @@ def get_plan(B, Hq, Hkv, D, Lmax, num_sms=0) -> dict:
 
 def set_tuning(force_path: int = 0, num_ctas: int = 0):
     _check(lib().kvattn_set_tuning(force_path, num_ctas))
+
+
+def set_wait_limit(polls: int = 0):
+    """Test knob: polls before the tensor-core kernel's pipeline waits give
+    up (0 restores the default); see kvattn_set_wait_limit."""
+    _check(lib().kvattn_set_wait_limit(int(polls)))
+
+
+def set_kernel_events(before=None, after=None):
+    """Measurement hook: record these torch.cuda.Event objects just before
+    and just after the split-KV kernel of every later attention call (None,
+    None stops).  The events must have been created (recorded once) first."""
+    if (before is None) != (after is None):
+        raise ValueError("give both events or neither")
+    b = before.cuda_event if before is not None else None
+    a = after.cuda_event if after is not None else None
+    if before is not None and (not b or not a):
+        raise ValueError("record each event once before handing it over (torch creates it lazily)")
+    _check(lib().kvattn_set_kernel_events(b, a))
 
 
 def release():

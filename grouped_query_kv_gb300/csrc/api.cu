@@ -40,6 +40,9 @@ int cuda_fail(cudaError_t e, const char *what) {
 std::mutex g_mu;
 int g_force_path = 0;
 int g_force_ctas = 0;
+unsigned int g_wait_limit = 0;           // 0: the kernels' default wait limits
+cudaEvent_t g_ev_before = nullptr;       // measurement hook around the split-KV kernel
+cudaEvent_t g_ev_after = nullptr;
 
 struct DeviceState {
     bool ready = false;
@@ -404,6 +407,21 @@ int kvattn_set_tuning(int force_path, int num_ctas) {
     return KVATTN_OK;
 }
 
+int kvattn_set_wait_limit(unsigned int polls) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_wait_limit = polls;
+    return KVATTN_OK;
+}
+
+int kvattn_set_kernel_events(void *before, void *after) {
+    if ((before == nullptr) != (after == nullptr))
+        return fail(KVATTN_ERR_INVALID_ARG, "kvattn_set_kernel_events: give both events or neither");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_ev_before = static_cast<cudaEvent_t>(before);
+    g_ev_after = static_cast<cudaEvent_t>(after);
+    return KVATTN_OK;
+}
+
 int kvattn_get_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, kvattn_plan *plan) {
     t_last_error[0] = 0;
     if (!plan) return fail(KVATTN_ERR_INVALID_ARG, "plan is null");
@@ -491,8 +509,13 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     DeviceState *ds;
     Plan pl;
     void *ws = nullptr;
+    unsigned int wait_limit = 0;
+    cudaEvent_t ev_before = nullptr, ev_after = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
+        wait_limit = g_wait_limit;
+        ev_before = g_ev_before;
+        ev_after = g_ev_after;
         if ((rc = device_state(dev, &ds))) return rc;
         if ((rc = get_encoder())) return rc;
         if ((rc = make_plan(B, Hq, Hkv, D, Lmax, ds->num_sms, &pl, T))) return rc;
@@ -543,8 +566,11 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     p.num_blocks = pg ? pg->num_blocks : 0;
     p.k_scale = nullptr;
     p.v_scale = nullptr;
+    p.wait_limit = wait_limit;
 
     cudaError_t e;
+    if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess)
+        return cuda_fail(e, "recording the event before the split-KV kernel");
     if (P.path == 2) {
         CUtensorMap tmq;
         if ((rc = encode_q_map(&tmq, q, D, B, T, Hq, p.G, pl.np))) return rc;
@@ -558,6 +584,8 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         e = launch_decode_fma(tmk, tmv, p, P.num_ctas, P.smem_bytes, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    if (ev_after && (e = cudaEventRecord(ev_after, stream)) != cudaSuccess)
+        return cuda_fail(e, "recording the event after the split-KV kernel");
     e = launch_combine(p, P.num_ctas, stream);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     return KVATTN_OK;
@@ -585,8 +613,11 @@ int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, cons
     DeviceState *ds;
     Plan pl;
     void *ws = nullptr;
+    cudaEvent_t ev_before = nullptr, ev_after = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
+        ev_before = g_ev_before;
+        ev_after = g_ev_after;
         if ((rc = device_state(dev, &ds))) return rc;
         if ((rc = get_encoder())) return rc;
         const int saved = g_force_path;
@@ -624,8 +655,13 @@ int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, cons
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.k_scale = k_scale;
     p.v_scale = v_scale;
-    cudaError_t e = launch_decode_q8(tmk, tmv, p, pl.np, P.num_ctas, stream);
+    cudaError_t e;
+    if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess)
+        return cuda_fail(e, "recording the event before the split-KV kernel");
+    e = launch_decode_q8(tmk, tmv, p, pl.np, P.num_ctas, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fp8 decode kernel launch");
+    if (ev_after && (e = cudaEventRecord(ev_after, stream)) != cudaSuccess)
+        return cuda_fail(e, "recording the event after the split-KV kernel");
     e = launch_combine(p, P.num_ctas, stream);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     return KVATTN_OK;

@@ -56,6 +56,7 @@ namespace {
 constexpr int kStage = 16384;    // one staged tile: 128 positions x 128 codes
 constexpr int kQWarps = 2;       // warps 6-7 write the q parts
 constexpr int kQ8Threads = 192 + 32 * kQWarps;
+constexpr int kQ8EndThreads = 192;  // warps 0-5 meet before tensor memory is freed
 constexpr float kTauQ8 = 2.f;    // rescale once a score passes the running max by 2 (log2 units)
 constexpr float kVHi = 64.f;     // v_scale[j] 2^cv stays <= 64
 constexpr int kCvNone = 1 << 20; // cv not chosen yet (piece start)
@@ -220,12 +221,12 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     // ================================================================ producer
     // Issue order K_0, K_1, V_0, K_2, V_1, ... (each ring in its own order)
     if (warp == 0) {
+        long long nk = 0, nv = 0;  // K and V stage copies issued (lane 0)
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             TileIter itk, itv;
             itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
             itv.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
-            long long nk = 0, nv = 0;
             bool ok = true;
             auto issue = [&](const void *tm, const TileIter &it, uint8_t *base, uint64_t *full,
                              uint64_t *empty, int ns, long long &n) -> bool {
@@ -251,15 +252,20 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             if (!ok) {
                 set_error(p.err, DEV_ERR_TIMEOUT);
                 *abort_flag = 1;
-                volatile int never = 0;
-                for (long long k = nk > NSK ? nk - NSK : 0; k < nk; ++k)
-                    wait_bar(&kst_full[k % NSK], (uint32_t)((k / NSK) & 1), &never);
-                for (long long k = nv > NSV ? nv - NSV : 0; k < nv; ++k)
-                    wait_bar(&vst_full[k % NSV], (uint32_t)((k / NSV) & 1), &never);
             }
         }
         __syncwarp();
         pdl_launch_dependents();
+        named_bar_sync(kBarEnd, kQ8EndThreads);
+        if (*abort_flag && lane == 0) {
+            // a role gave up, so copies may still be in flight that no one
+            // consumed: let them land before the CTA exits
+            volatile int never = 0;
+            for (long long k = nk > NSK ? nk - NSK : 0; k < nk; ++k)
+                wait_bar(&kst_full[k % NSK], (uint32_t)((k / NSK) & 1), &never);
+            for (long long k = nv > NSV ? nv - NSV : 0; k < nv; ++k)
+                wait_bar(&vst_full[k % NSV], (uint32_t)((k / NSV) & 1), &never);
+        }
         return;
     }
 
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             wait_bar(drain, 0, &never);
         }
         __syncwarp();
-        named_bar_sync(kBarEnd, 160);
+        named_bar_sync(kBarEnd, kQ8EndThreads);
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
         return;
@@ -694,7 +700,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     }
     if (aborted) set_error(p.err, DEV_ERR_TIMEOUT);
     tc_fence_before();
-    named_bar_sync(kBarEnd, 160);
+    named_bar_sync(kBarEnd, kQ8EndThreads);
 }
 
 template <int NP>

@@ -46,7 +46,7 @@ constexpr int kChunk = 32768;       // one ring chunk: 2 boxes of 64 columns x 1
 constexpr int kSmemLimit = 232448;  // 227 KB per CTA
 constexpr float kTau = 8.0f;        // log2 headroom before the running max must move
 constexpr int kBarSoftmax = 1;      // named barrier: the 128 softmax threads
-constexpr int kBarEnd = 2;          // named barrier: warps 1-5 before TMEM is freed
+constexpr int kBarEnd = 2;          // named barrier: all warps before TMEM is freed
 constexpr uint32_t kMmaIdleLimit = 1u << 23;  // ~seconds of polling with nothing ready
 
 __host__ __device__ constexpr int pow2_at_least(int x) {
@@ -103,8 +103,9 @@ __device__ __forceinline__ void set_error(unsigned int *err, unsigned int code) 
 }
 
 // Bounded wait that also gives up early once another role has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    for (uint32_t it = 0; it < KVATTN_SPIN_LIMIT; ++it) {
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         uint32_t limit = KVATTN_SPIN_LIMIT) {
+    for (uint32_t it = 0; it < limit; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 255u && *abort_flag) return false;
     }
@@ -449,17 +450,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) {
             set_error(p.err, DEV_ERR_TIMEOUT);
             *abort_flag = 1;
-            // let copies already issued land before the CTA can exit
-            const long long first = n > NCH ? n - NCH : 0;
-            for (long long k = first; k < n; ++k) {
-                volatile int never = 0;
-                wait_bar(&bs.chunk_full[k % NCH], (uint32_t)((k / NCH) & 1), &never);
-            }
         }
         // every load of this CTA is issued: the next kernel (the combine) may
         // be scheduled now -- late enough that its waiting blocks do not sit
         // beside this kernel for long, early enough to hide its launch
         pdl_launch_dependents();
+        named_bar_sync(kBarEnd, kThreads);
+        if (*abort_flag && lane == 0) {
+            // a role gave up, so copies may still be in flight that no one
+            // consumed: let them land before the CTA exits -- the last NCH
+            // ring chunks and the last two q loads (earlier ones were waited
+            // for before their slots were reused)
+            volatile int never = 0;
+            const long long first = n > NCH ? n - NCH : 0;
+            for (long long k = first; k < n; ++k)
+                wait_bar(&bs.chunk_full[k % NCH], (uint32_t)((k / NCH) & 1), &never);
+            for (int q = piece > 2 ? piece - 2 : 0; q < piece; ++q)
+                wait_bar(&bs.q_full[q & 1], (uint32_t)((q >> 1) & 1), &never);
+        }
         return;
     }
 
@@ -583,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (idle >= kMmaIdleLimit) {
+                if (idle >= (p.wait_limit ? p.wait_limit : kMmaIdleLimit)) {
                     ok = false;
                     *abort_flag = 1;
                     break;
@@ -600,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_bar(bs.drain, 0, &never);
         }
         __syncwarp();
-        named_bar_sync(kBarEnd, 160);
+        named_bar_sync(kBarEnd, kThreads);
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
         return;
@@ -616,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long i = 0;
     bool first_piece = true;
     bool aborted = false;
+    const uint32_t wlim = p.wait_limit ? p.wait_limit : KVATTN_SPIN_LIMIT;
     bool carry_fail = false;  // a failed wait late in a tile is voted on at the next barrier
     float l[NP];
 
@@ -638,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         while (true) {
             const int sb = (int)(i & 1);
-            bool fail = carry_fail || !wait_bar(&bs.s_full[sb], (uint32_t)((i >> 1) & 1), abort_flag);
+            bool fail = carry_fail || !wait_bar(&bs.s_full[sb], (uint32_t)((i >> 1) & 1), abort_flag, wlim);
             tc_fence_after();
             float s[NP];
 #pragma unroll
@@ -718,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i > i0) {
                     // O^T holds this piece's earlier tiles: scale column g by alpha[g]
                     const long long j = i - 1;
-                    if (!wait_bar(&bs.pv_done[j & 1], (uint32_t)((j >> 1) & 1), abort_flag))
+                    if (!wait_bar(&bs.pv_done[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, wlim))
                         fail = true;
                     tc_fence_after();
 #pragma unroll
@@ -763,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the P stage written now was last read by PV of tile i - PST
             if (i >= C::PST) {
                 const long long jp = i - C::PST;
-                if (!wait_bar(&bs.pv_done[jp & 1], (uint32_t)((jp >> 1) & 1), abort_flag))
+                if (!wait_bar(&bs.pv_done[jp & 1], (uint32_t)((jp >> 1) & 1), abort_flag, wlim))
                     fail = true;
             }
             uint8_t *pdst = pbuf + 2 * (int)(i % C::PST) * C::PB + (row >> 3) * 128 + (row & 7) * 16;
@@ -788,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- piece end: O^T is complete once the last PV has finished
         const long long e = i - 1;
-        bool fail = carry_fail || !wait_bar(&bs.pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag);
+        bool fail = carry_fail || !wait_bar(&bs.pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag, wlim);
         carry_fail = false;
         tc_fence_after();
         warp_cols_np<NP>(l, red + q4 * 64, lane, OpSum());
@@ -856,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (aborted) set_error(p.err, DEV_ERR_TIMEOUT);
     tc_fence_before();
-    named_bar_sync(kBarEnd, 160);
+    named_bar_sync(kBarEnd, kThreads);
 }
 
 template <int D, int NP, bool MT, bool PG>

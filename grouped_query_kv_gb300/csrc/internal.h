@@ -60,6 +60,10 @@ struct DecodeParams {
     // [B, Hkv, Lmax] for K and for V; null otherwise
     const float *k_scale;
     const float *v_scale;
+    // tensor-core kernel: polls before a pipeline wait gives up (the softmax
+    // threads' waits and the MMA thread's idle polling); 0 = the default.
+    // Waits for copies and MMAs already issued always keep the default.
+    unsigned int wait_limit;
 };
 
 // Host launchers (return cudaError_t of the launch).

@@ -385,6 +385,33 @@ KVATTN_API void kvattn_release(void);
  */
 KVATTN_API int kvattn_set_tuning(int force_path, int num_ctas);
 
+/*
+ * Test knob for the failure handling (process-wide; 0 restores the default).
+ * Every wait inside the tensor-core split-KV kernel is bounded; this sets
+ * how many polls its pipeline waits make before giving up -- the softmax
+ * threads' waits for scores and for finished P.V products, and the MMA
+ * thread's polling while nothing is ready.  A kernel that gives up sets the
+ * device error word to KVATTN_ERR_TIMEOUT (read by kvattn_check_device_error),
+ * lets every copy and MMA it already issued finish, frees its tensor memory
+ * and returns; the output of that call is undefined.  Waits for work already
+ * issued keep their default limit.  With a very small value (1) a call is
+ * sure to give up, which is how the tests exercise this path.  Always
+ * returns KVATTN_OK.
+ */
+KVATTN_API int kvattn_set_wait_limit(unsigned int polls);
+
+/*
+ * Measurement hook (process-wide).  With two events given (cudaEvent_t
+ * handles, owned by the caller), every later attention call records
+ * `before` on its stream just before its split-KV kernel and `after` just
+ * after it, so that cudaEventElapsedTime(before, after) is that kernel's
+ * duration alone.  The records sit between the kernel and its neighbours on
+ * the stream, so they also end the programmatic overlap with them: use it to
+ * time, not in production.  Pass (NULL, NULL) to stop; one NULL alone is
+ * KVATTN_ERR_INVALID_ARG.
+ */
+KVATTN_API int kvattn_set_kernel_events(void *before, void *after);
+
 /* How a call with these sizes would run (host-side planning only; no GPU
  * work).  num_sms <= 0 queries the current device. */
 typedef struct {

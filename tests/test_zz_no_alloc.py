@@ -4,20 +4,36 @@ own pool at start-up, or a loop that cannot take the synchronisation a
 cudaFree brings).  Its partial results live in a fixed array inside the
 library instead of a cudaMalloc'd workspace.
 
-The GPU test calls it through the C ABI twice in a row, on two different
-problems that both split sequences across CTAs (so the fixed array is used,
-and the second call runs on whatever the first left in it), and checks each
-result against the regular gqa_decode_attn within the tolerance the parity
-tests use.  This file is named so that pytest collects it last."""
+The GPU test calls it through the C ABI on several problems in a row, so the
+fixed array is used by each call after the previous one left its contents
+there, and checks every output against the double-precision oracle within
+the tolerance the parity tests use.  The sequence covers the CUDA-core path
+at D = 64, 128 and 256, and a call on a small grid right after a call on a
+large one: the second call reads fewer partial slots than the first wrote,
+so reading a stale slot would show.  This file is named so that pytest
+collects it last."""
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import grouped_query_kv_gb300 as g
+import oracle
 from grouped_query_kv_gb300 import workloads as wl
 
-from helpers import ATOL, VREL
+from helpers import assert_close, bits
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from grouped_query_kv_gb300 import build
+    build.build()
+    oracle.build()
+    h = g.lib()
+    assert h.kvattn_set_tuning(0, 0) == 0
+    yield h
+    assert h.kvattn_set_tuning(0, 0) == 0
 
 
 def _call(fn, x, w, lens, out, stream):
@@ -28,42 +44,48 @@ def _call(fn, x, w, lens, out, stream):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_regular_entry_point_on_two_calls_in_a_row():
-    from grouped_query_kv_gb300 import build
-    build.build()
-    lib = g.lib()
-    assert lib.kvattn_set_tuning(0, 0) == 0
+def test_noalloc_matches_the_oracle_on_calls_in_a_row(lib):
     dev = torch.device("cuda")
     stream = torch.cuda.current_stream()
     cases = [
+        # (workload, forced grid: 0 = one CTA per SM)
         # one long sequence: every CTA gets a piece of it
-        wl.Workload("noalloc_a", B=1, Hq=16, Hkv=2, D=128, Lmax=3000, scale=0.088,
-                    lens=(3000,)),
+        (wl.Workload("noalloc_a", B=1, Hq=16, Hkv=2, D=128, Lmax=3000, scale=0.088,
+                     lens=(3000,)), 0),
         # ragged multi-query batch with wide heads
-        wl.Workload("noalloc_b", B=6, Hq=16, Hkv=1, D=256, Lmax=2048, scale=1 / 16,
-                    lens=(2048, 1, 900, 1500, 64, 2047)),
+        (wl.Workload("noalloc_b", B=6, Hq=16, Hkv=1, D=256, Lmax=2048, scale=1 / 16,
+                     lens=(2048, 1, 900, 1500, 64, 2047)), 0),
+        # D = 64 (the CUDA-core kernel's own head size), grouped heads
+        (wl.Workload("noalloc_c", B=3, Hq=8, Hkv=2, D=64, Lmax=4000, scale=0.125,
+                     lens=(4000, 17, 2500)), 0),
+        # a large forced grid (many split pieces, slots up to 2 x 400) ...
+        (wl.Workload("noalloc_d", B=2, Hq=8, Hkv=1, D=128, Lmax=6000, scale=0.088,
+                     lens=(6000, 5999)), 400),
+        # ... then a small one on a problem of its own: it reads only the
+        # first slots, which the previous call also wrote
+        (wl.Workload("noalloc_e", B=4, Hq=4, Hkv=4, D=64, Lmax=900, scale=0.125,
+                     lens=(900, 3, 450, 77)), 6),
     ]
-    for seed, w in enumerate(cases):
-        x = wl.make_inputs(w, seed=40 + seed, device=dev)
-        lens = x["attn_lens"]
-        got = torch.full((w.B, w.Hq, w.D), float("nan"), device=dev)
-        want = torch.empty((w.B, w.Hq, w.D), device=dev)
-        assert _call(lib.gqa_decode_attn_noalloc, x, w, lens, got, stream) == 0, \
-            lib.kvattn_last_error()
-        assert _call(lib.gqa_decode_attn, x, w, lens, want, stream) == 0, \
-            lib.kvattn_last_error()
-        assert lib.kvattn_check_device_error(ctypes.c_void_p(stream.cuda_stream)) == 0
-        vmax = max(float(x["v_cache"][b, :, :int(n)].abs().max())
-                   for b, n in enumerate(lens.tolist()))
-        err = float((got - want).abs().max())
-        assert torch.isfinite(got).all()
-        assert err <= min(ATOL, VREL * vmax), (w.name, err)
+    try:
+        for seed, (w, ctas) in enumerate(cases):
+            assert lib.kvattn_set_tuning(0, ctas) == 0
+            x = wl.make_inputs(w, seed=40 + seed, device=dev)
+            lens = x["attn_lens"]
+            got = torch.full((w.B, w.Hq, w.D), float("nan"), device=dev)
+            assert _call(lib.gqa_decode_attn_noalloc, x, w, lens, got, stream) == 0, \
+                lib.kvattn_last_error()
+            assert lib.kvattn_check_device_error(ctypes.c_void_p(stream.cuda_stream)) == 0
+            lens_np = lens.cpu().numpy()
+            ref = oracle.gqa_decode(bits(x["q"]), bits(x["k_cache"]), bits(x["v_cache"]),
+                                    lens_np, w.scale)
+            assert_close(got, ref, bits(x["v_cache"]), lens_np)
+    finally:
+        assert lib.kvattn_set_tuning(0, 0) == 0
 
 
-def test_noalloc_rejects_a_grid_whose_partials_do_not_fit():
+def test_noalloc_rejects_a_grid_whose_partials_do_not_fit(lib):
     # a forced grid of 2000 CTAs needs 2*2000*8*(256+2)*4 bytes > 4 MiB; the
     # check comes before any device work, so this runs without a GPU
-    lib = g.lib()
     assert lib.kvattn_set_tuning(0, 2000) == 0
     try:
         fake = ctypes.c_void_p(0x10000)
