@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the headline workload")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -320,186 +322,240 @@ def _oracle_fixed(w, seed, nb, threads):
 
 # ------------------------------------------------------------------ GPU arm
 
-def gpu_arm(a, w):
-    import torch
-    import torch.distributed as dist
+CHAIN_MAX = 1000          # steps per captured CUDA graph
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+# the other target shapes (and the built extensions), timed in the same run
+PER_CONFIG = ["palm8b_mqa", "llama70b_gqa_ragged", "palm540b_long_mqa", "sweep_hkv32_b256",
+              "sweep_hkv8_b256", "sweep_hkv1_b256", "local_gqa_w4096", "llama70b_spec4",
+              "palm540b_spec4", "llama70b_paged64", "llama70b_paged16", "llama70b_fp8",
+              "palm8b_fp8", "palm540b_fp8"]
 
-    import grouped_query_kv_gb300 as g
-    from grouped_query_kv_gb300 import accounting
-    from grouped_query_kv_gb300 import workloads as wl
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-    lib = g.lib()
-    peak, peak_kind = measured_peaks()
+class Setup:
+    """One workload's device inputs, its rotation of cache copies (so that
+    consecutive steps never hit in L2) and the step call."""
 
-    # ---- inputs: `ncopies` caches so consecutive steps never hit in L2 (the
-    # steps of one round read at least 4x L2 between them)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    cache_bytes = 2 * w.B * w.Hkv * w.Lmax * w.D * 2
-    read_bytes = accounting.kv_bytes_read(wl.attn_lens(w, rank_seed(a.seed, rank)).tolist(),
-                                          w.Hkv, w.D, window=w.window)
-    ncopies = max(1, int(math.ceil(4 * l2 / read_bytes)))
-    ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
-    x = wl.make_inputs(w, seed=rank_seed(a.seed, rank), device=dev)
-    table = None
-    if w.block_size:
-        # paged: the pools hold only the blocks the sequences use, scattered
-        pg = wl.make_paged(w, x, seed=rank_seed(a.seed, rank))
-        del x["k_cache"], x["v_cache"]
-        x["k_cache"], x["v_cache"], table = pg["k_pool"], pg["v_pool"], pg["block_table"]
-        cache_bytes = 2 * x["k_cache"].numel() * 2
-        ncopies = max(1, int(math.ceil(4 * l2 / read_bytes)))
-        ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
-        nblk, _, bs, _ = x["k_cache"].shape
-        maxb = table.shape[1]
-    fp8 = w.kv_dtype == "fp8"
-    if fp8:
-        # the 8-bit cache: codes and per-row scales quantized on the GPU
-        kc, ks = g.kv_quantize_fp8(x["k_cache"])
-        vc, vs = g.kv_quantize_fp8(x["v_cache"])
-        del x["k_cache"], x["v_cache"]
-        x["k_cache"], x["v_cache"] = kc, vc
-        cache_bytes = 2 * (kc.numel() + 4 * ks.numel())
-        ncopies = max(1, int(math.ceil(4 * l2 / (read_bytes * (w.D + 4) / (2 * w.D)))))
-        ncopies = min(ncopies, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // cache_bytes)))
-        caches = [(kc, vc, ks, vs)]
-        for r in range(1, ncopies):
-            caches.append((kc.clone(), vc.clone(), ks.clone(), vs.clone()))
-    else:
-        caches = [(x["k_cache"], x["v_cache"])]
-        for r in range(1, ncopies):
-            caches.append((x["k_cache"].clone(), x["v_cache"].clone()))
-    lens = x["attn_lens"]
-    pos = x["append_pos"]
-    out = torch.empty(tuple(x["q"].shape), dtype=torch.float32, device=dev)
-    kv_bytes = accounting.kv_bytes_read(lens.cpu().tolist(), w.Hkv, w.D, window=w.window)
-    # bf16-equivalent bytes: what the same attention reads from a bf16 cache
-    kv_bytes_bf16 = kv_bytes
-    if fp8:
-        kv_bytes = accounting.kv_bytes_read_fp8(lens.cpu().tolist(), w.Hkv, w.D)
+    def __init__(self, w, seed, dev, lib, stream):
+        import torch
 
-    stream = torch.cuda.Stream(device=dev)
-    sp = ctypes_void(stream.cuda_stream)
-    P = lambda t: ctypes_void(t.data_ptr())  # noqa: E731
-    q_p, kn_p, vn_p, pos_p, out_p = map(P, (x["q"], x["k_new"], x["v_new"], pos, out))
+        import grouped_query_kv_gb300 as g
+        from grouped_query_kv_gb300 import accounting
+        from grouped_query_kv_gb300 import workloads as wl
 
-    lens_p = P(lens)
-    table_p = P(table) if table is not None else None
-
-    def call_step(r):
-        # one decode step: append this token's K/V and attend (fused kernel);
-        # for T drafted tokens, their scoring pass over the cache
-        if fp8:
-            c = caches[r]
-            rc = lib.kv_append_fp8(P(c[0]), P(c[1]), P(c[2]), P(c[3]), kn_p, vn_p, pos_p, w.B,
-                                   w.Hkv, w.D, w.Lmax, sp)
-            assert rc == 0, lib.kvattn_last_error()
-            rc = lib.gqa_decode_attn_fp8(q_p, P(c[0]), P(c[1]), P(c[2]), P(c[3]), lens_p, out_p,
-                                         w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
-        elif table is not None:
-            rc = lib.gqa_decode_step_paged(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]),
-                                           table_p, pos_p, out_p, w.B, w.Hq, w.Hkv, w.D, nblk,
-                                           bs, maxb, float(w.scale), sp)
-        elif w.T > 1:
-            rc = lib.gqa_decode_attn_multi(q_p, P(caches[r][0]), P(caches[r][1]), lens_p, out_p,
-                                           w.B, w.T, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
-        elif w.window is None:
-            rc = lib.gqa_decode_step(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]), pos_p,
-                                     out_p, w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+        self.w, self.dev, self.lib, self.stream = w, dev, lib, stream
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+        lens_host = wl.attn_lens(w, seed).tolist()
+        read_bytes = accounting.kv_bytes_read(lens_host, w.Hkv, w.D, window=w.window)
+        x = wl.make_inputs(w, seed=seed, device=dev)
+        self.table = None
+        self.fp8 = w.kv_dtype == "fp8"
+        if w.block_size:
+            # paged: the pools hold only the blocks the sequences use, scattered
+            pg = wl.make_paged(w, x, seed=seed)
+            del x["k_cache"], x["v_cache"]
+            x["k_cache"], x["v_cache"], self.table = pg["k_pool"], pg["v_pool"], pg["block_table"]
+            self.nblk, _, self.bs, _ = x["k_cache"].shape
+            self.maxb = self.table.shape[1]
+        if self.fp8:
+            # the 8-bit cache: codes and per-row scales quantized on the GPU
+            kc, ks = g.kv_quantize_fp8(x["k_cache"])
+            vc, vs = g.kv_quantize_fp8(x["v_cache"])
+            del x["k_cache"], x["v_cache"]
+            x["k_cache"], x["v_cache"], x["k_scale"], x["v_scale"] = kc, vc, ks, vs
+            self.cache_bytes = 2 * (kc.numel() + 4 * ks.numel())
+            step_read = read_bytes * (w.D + 4) / (2 * w.D)
+            names = ("k_cache", "v_cache", "k_scale", "v_scale")
         else:
-            rc = lib.gqa_decode_step_window(q_p, kn_p, vn_p, P(caches[r][0]), P(caches[r][1]),
-                                            pos_p, out_p, w.B, w.Hq, w.Hkv, w.D, w.Lmax,
-                                            float(w.scale), int(w.window), sp)
+            self.cache_bytes = 2 * x["k_cache"].numel() * 2
+            step_read = read_bytes
+            names = ("k_cache", "v_cache")
+        free = torch.cuda.mem_get_info(dev)[0]
+        self.ncopies = max(1, min(int(math.ceil(4 * l2 / step_read)),
+                                  int(0.5 * free // self.cache_bytes)))
+        self.caches = [tuple(x[n] for n in names)]
+        for _ in range(1, self.ncopies):
+            self.caches.append(tuple(x[n].clone() for n in names))
+        self.x = x
+        self.lens = x["attn_lens"]
+        self.pos = x["append_pos"]
+        self.out = torch.empty(tuple(x["q"].shape), dtype=torch.float32, device=dev)
+        lh = self.lens.cpu().tolist()
+        self.kv_bytes_bf16 = accounting.kv_bytes_read(lh, w.Hkv, w.D, window=w.window)
+        self.kv_bytes = (accounting.kv_bytes_read_fp8(lh, w.Hkv, w.D) if self.fp8
+                         else self.kv_bytes_bf16)
+        self.sp = ctypes_void(stream.cuda_stream)
+
+    def call(self, r, q=None, kn=None, vn=None, pos=None, lens=None, out=None, table=None):
+        """One step on cache copy r through the C ABI: append this token's K/V
+        and attend (fused kernel); T drafted tokens: their scoring pass; the
+        8-bit cache: append, then attend.  Tensors default to the setup's own."""
+        w, lib, c = self.w, self.lib, self.caches[r]
+        P = lambda t: ctypes_void(t.data_ptr())  # noqa: E731
+        q = P(self.x["q"] if q is None else q)
+        kn = P(self.x["k_new"] if kn is None else kn)
+        vn = P(self.x["v_new"] if vn is None else vn)
+        pos = P(self.pos if pos is None else pos)
+        lens = P(self.lens if lens is None else lens)
+        out = P(self.out if out is None else out)
+        sp = self.sp
+        if self.fp8:
+            rc = lib.kv_append_fp8(P(c[0]), P(c[1]), P(c[2]), P(c[3]), kn, vn, pos, w.B, w.Hkv,
+                                   w.D, w.Lmax, sp)
+            assert rc == 0, lib.kvattn_last_error()
+            rc = lib.gqa_decode_attn_fp8(q, P(c[0]), P(c[1]), P(c[2]), P(c[3]), lens, out, w.B,
+                                         w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+        elif self.table is not None:
+            tp = P(self.table if table is None else table)
+            rc = lib.gqa_decode_step_paged(q, kn, vn, P(c[0]), P(c[1]), tp, pos, out, w.B, w.Hq,
+                                           w.Hkv, w.D, self.nblk, self.bs, self.maxb,
+                                           float(w.scale), sp)
+        elif w.T > 1:
+            rc = lib.gqa_decode_attn_multi(q, P(c[0]), P(c[1]), lens, out, w.B, w.T, w.Hq, w.Hkv,
+                                           w.D, w.Lmax, float(w.scale), sp)
+        elif w.window is None:
+            rc = lib.gqa_decode_step(q, kn, vn, P(c[0]), P(c[1]), pos, out, w.B, w.Hq, w.Hkv,
+                                     w.D, w.Lmax, float(w.scale), sp)
+        else:
+            rc = lib.gqa_decode_step_window(q, kn, vn, P(c[0]), P(c[1]), pos, out, w.B, w.Hq,
+                                            w.Hkv, w.D, w.Lmax, float(w.scale), int(w.window), sp)
         assert rc == 0, lib.kvattn_last_error()
 
-    with torch.cuda.stream(stream):
-        for r in range(ncopies):           # first calls allocate the workspace
-            call_step(r)
-    stream.synchronize()
-    g.check_device_error(stream)
+    def launches_per_step(self):
+        return 3 if self.fp8 else 2
 
-    # one graph runs the ncopies steps back to back (programmatic edges between
-    # their kernels, so a step's launch overlaps the previous step's tail);
-    # single-step graphs make up the remainder, so exactly K steps are timed
-    chain = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(chain, stream=stream):
-        for r in range(ncopies):
-            call_step(r)
-    singles = []
-    for r in range(ncopies):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=stream):
-            call_step(r)
-        singles.append(gr)
-    torch.cuda.synchronize(dev)
+    def describe(self):
+        w = self.w
+        if self.fp8:
+            return ("kv_append_fp8 then gqa_decode_attn_fp8 (8-bit cache: E4M3 codes and one "
+                    "fp32 scale per row; kv_bytes_per_step counts codes and scales)")
+        if self.table is not None:
+            return ("gqa_decode_step_paged (kv_append fused into the attention kernel, K/V "
+                    "reached through the block table)")
+        if w.T > 1:
+            return ("gqa_decode_attn_multi (T new tokens scored in one pass over the cache, "
+                    "which already holds their rows)")
+        return "gqa_decode_step (kv_append fused into the attention kernel)"
 
-    def run_steps(k):
-        for _ in range(k // ncopies):
-            chain.replay()
-        for r in range(k % ncopies):
-            singles[r].replay()
+    def free(self):
+        import torch
+        self.caches = self.x = self.out = self.lens = self.pos = self.table = None
+        torch.cuda.synchronize(self.dev)
+        torch.cuda.empty_cache()
 
-    # ---- warm-up, then exactly K timed steps
-    with torch.cuda.stream(stream):
-        run_steps(a.warmup)
-    stream.synchronize()
+
+def time_chained(S, steps, warmup):
+    """Exactly `steps` steps, W untimed before them, chained in CUDA graphs of
+    up to CHAIN_MAX steps (programmatic edges between their kernels, so a
+    step's launch overlaps the previous step's tail).  Returns the elapsed
+    milliseconds of the timed steps and the graph used most (for replays)."""
+    import torch
+    graphs = {}
+
+    def graph_for(n):
+        if n not in graphs:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=S.stream):
+                for i in range(n):
+                    S.call(i % S.ncopies)
+            graphs[n] = gr
+        return graphs[n]
+
+    L = max(1, min(steps, CHAIN_MAX))
+
+    def run(k):
+        for _ in range(k // L):
+            graph_for(L).replay()
+        if k % L:
+            graph_for(k % L).replay()
+
+    with torch.cuda.stream(S.stream):
+        for r in range(S.ncopies):  # first calls allocate the workspace
+            S.call(r)
+    S.stream.synchronize()
+    for n in {L, steps % L, min(warmup, L), warmup % L} - {0}:
+        graph_for(n)
+    torch.cuda.synchronize(S.dev)
+    with torch.cuda.stream(S.stream):
+        run(warmup)
+    S.stream.synchronize()
+    return run, graphs
+
+
+def time_run(S, run, steps, before=None, after=None):
+    """Events around exactly `steps` steps, with a barrier and a device
+    synchronisation on both sides.  A short GPU sleep is queued ahead of the
+    start event, so that the host has submitted the steps' graphs by the time
+    the GPU reaches it: the timed region holds the steps' GPU work, not the
+    submission latency of the first graph."""
+    import torch
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = Clocks(local)
-    clocks.start()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        run_steps(a.steps)
-        t1.record(stream)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    g.check_device_error(stream)
-    ms_total = t0.elapsed_time(t1)
-    local_ms_step = ms_total / a.steps
-    ms_total, job_bytes = over_ranks(ms_total, kv_bytes * a.steps, world, dev)
-    ms_step = ms_total / a.steps
-    value = job_bytes / (ms_total / 1e3) / 1e9
-    # average duration of one step's launch over the timed region
-    achieved = kv_bytes / (local_ms_step / 1e3) / 1e9
+    if before:
+        before()
+    torch.cuda.synchronize(S.dev)
+    with torch.cuda.stream(S.stream):
+        torch.cuda._sleep(200000)  # ~0.1 ms at 2 GHz
+        t0.record(S.stream)
+        run(steps)
+        t1.record(S.stream)
+    torch.cuda.synchronize(S.dev)
+    if after:
+        after()
+    return t0.elapsed_time(t1)
 
-    # ---- spread of the step time, outside the timed region: events around
-    # each replay of the ncopies-step chain
-    reps = max(20, min(400, 4000 // ncopies))
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-    with torch.cuda.stream(stream):
-        evs[0].record(stream)
-        for k in range(reps):
-            chain.replay()
-            evs[k + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    per = sorted(1e3 * evs[k].elapsed_time(evs[k + 1]) / ncopies for k in range(reps))
-    spread = {"p10": per[reps // 10], "p50": per[reps // 2], "p90": per[(9 * reps) // 10],
-              "over": "%d replays of the %d-step chain (us per step)" % (reps, ncopies)}
 
-    # ---- end to end through the public Python API with host buffers.  A
-    # step's inputs go up from pinned host memory in ONE copy (the tensors
-    # packed side by side at 256-byte offsets) and its output comes back in
-    # one copy.  Uploads and downloads run on streams of their own with two
-    # buffer sets, so step i's upload and step i-1's download overlap the
-    # kernels of the steps around them, as a serving loop would run them.
+def kernel_alone(S, n):
+    """The split-KV kernel timed by itself: events recorded just before and
+    just after it inside each call (kvattn_set_kernel_events), steps issued
+    one by one over the same cache rotation.  The records end the kernel's
+    overlap with its neighbours, so this runs outside the timed region."""
+    import torch
+
+    import grouped_query_kv_gb300 as g
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    with torch.cuda.stream(S.stream):
+        for b, a in evs:  # torch creates events on first record
+            b.record(S.stream)
+            a.record(S.stream)
+        for r in range(3):
+            S.call(r % S.ncopies)
+    torch.cuda.synchronize(S.dev)
+    try:
+        with torch.cuda.stream(S.stream):
+            for i, (b, a) in enumerate(evs):
+                g.set_kernel_events(b, a)
+                S.call(i % S.ncopies)
+    finally:
+        g.set_kernel_events(None, None)
+    torch.cuda.synchronize(S.dev)
+    us = sorted(1e3 * b.elapsed_time(a) for b, a in evs)
+    return {"mean_us": sum(us) / len(us), "p10_us": us[len(us) // 10], "p50_us": us[len(us) // 2],
+            "p90_us": us[(9 * len(us)) // 10], "launches": n}
+
+
+def e2e_graphs(S, steps):
+    """End to end through the public Python API with host buffers, the steps
+    captured in CUDA graphs as a serving loop would run them: every step
+    uploads its inputs from pinned host memory (one packed copy) and reads its
+    output back into pinned host memory.  Uploads and downloads run on
+    streams of their own with two buffer sets, so step i's upload and step
+    i-1's download overlap the kernels around them.  Returns the timing and
+    the bytes moved per step."""
+    import torch
+
+    import grouped_query_kv_gb300 as g
+    w, dev, stream = S.w, S.dev, S.stream
+    x = S.x
     if w.T > 1:
-        send = [("q", x["q"]), ("lens", lens)]
-    elif fp8:
+        send = [("q", x["q"]), ("lens", S.lens)]
+    elif S.fp8:
         send = [("q", x["q"]), ("k_new", x["k_new"]), ("v_new", x["v_new"]),
-                ("pos", pos), ("lens", lens)]
+                ("pos", S.pos), ("lens", S.lens)]
     else:
-        send = [("q", x["q"]), ("k_new", x["k_new"]), ("v_new", x["v_new"]), ("pos", pos)]
-    if table is not None:
-        send.append(("table", table))  # a paged server sends the block table with every step
+        send = [("q", x["q"]), ("k_new", x["k_new"]), ("v_new", x["v_new"]), ("pos", S.pos)]
+    if S.table is not None:
+        send.append(("table", S.table))  # a paged server sends the block table with every step
     layout, nbuf = [], 0
     for name, t in send:
         nb = t.numel() * t.element_size()
@@ -511,16 +567,15 @@ def gpu_arm(a, w):
     dbufs = [torch.empty(nbuf, dtype=torch.uint8, device=dev) for _ in range(2)]
     dviews = [{name: db[o:o + nb].view(dt).view(shp) for name, o, nb, dt, shp in layout}
               for db in dbufs]
-    outs = [out, torch.empty_like(out)]
-    houts = [torch.empty_like(out, device="cpu").pin_memory() for _ in range(2)]
+    outs = [S.out, torch.empty_like(S.out)]
+    houts = [torch.empty_like(S.out, device="cpu").pin_memory() for _ in range(2)]
     io = {"h2d": sum(nb for _, _, nb, _, _ in layout),
           "d2h": houts[0].numel() * houts[0].element_size()}
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = {k: [torch.cuda.Event() for _ in range(2)]
           for k in ("in_ready", "in_free", "out_ready", "out_free")}
-    n_e2e = max(1, a.e2e_steps)
 
-    def e2e_step(i):
+    def step(i):
         s = i % 2
         v, o = dviews[s], outs[s]
         up.wait_event(ev["in_free"][s])          # step i-2's kernels are done with this set
@@ -529,16 +584,15 @@ def gpu_arm(a, w):
             ev["in_ready"][s].record(up)
         stream.wait_event(ev["in_ready"][s])
         stream.wait_event(ev["out_free"][s])     # step i-2's output has been read back
-        r = i % ncopies
-        c = caches[r]
+        c = S.caches[i % S.ncopies]
         if w.T > 1:
             g.gqa_decode_attn_multi(v["q"], c[0], c[1], v["lens"], w.scale, out=o, stream=stream)
-        elif fp8:
+        elif S.fp8:
             g.kv_append_fp8(c[0], c[1], c[2], c[3], v["k_new"], v["v_new"], v["pos"],
                             stream=stream)
             g.gqa_decode_attn_fp8(v["q"], c[0], c[1], c[2], c[3], v["lens"], w.scale, out=o,
                                   stream=stream)
-        elif table is not None:
+        elif S.table is not None:
             g.gqa_decode_step_paged(v["q"], v["k_new"], v["v_new"], c[0], c[1], v["table"],
                                     v["pos"], w.scale, out=o, stream=stream)
         else:
@@ -551,77 +605,213 @@ def gpu_arm(a, w):
             houts[s].copy_(o, non_blocking=True)
             ev["out_free"][s].record(down)
 
+    # eager: the host issues every copy and call (its issue time is reported)
     for i in range(6):
-        e2e_step(i)
+        step(i)
     torch.cuda.synchronize(dev)
+    n_e = max(1, min(steps, 200))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(up)
     h0 = time.perf_counter()
-    for i in range(n_e2e):
-        e2e_step(i)
-    host_us = 1e6 * (time.perf_counter() - h0) / n_e2e  # host time to issue one step
+    for i in range(n_e):
+        step(i)
+    host_us = 1e6 * (time.perf_counter() - h0) / n_e
     e1.record(down)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
-    e2e_ms, e2e_bytes = over_ranks(e2e_ms, kv_bytes, world, dev)
-    e2e_val = e2e_bytes / (e2e_ms / 1e3) / 1e9
+    eager_ms = e0.elapsed_time(e1) / n_e
+
+    # graphs: the same steps captured (both side streams join the capture
+    # through events recorded on the capturing stream)
+    L = max(2, min(steps, 200))
+    L += L % 2  # whole buffer-set pairs per graph
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for s in range(2):
+            ev["in_free"][s].record(stream)
+            ev["out_free"][s].record(stream)
+        for i in range(L):
+            step(i)
+        for s in range(2):
+            stream.wait_event(ev["out_free"][s])
+            stream.wait_event(ev["in_free"][s])
+    torch.cuda.synchronize(dev)
+    gr.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(1, int(math.ceil(steps / L)))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        h0 = time.perf_counter()
+        for _ in range(reps):
+            gr.replay()
+        ghost_us = 1e6 * (time.perf_counter() - h0) / (reps * L)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    graph_ms = e0.elapsed_time(e1) / (reps * L)
+    return {"graph_ms": graph_ms, "graph_steps": reps * L, "graph_host_us": ghost_us,
+            "eager_ms": eager_ms, "eager_steps": n_e, "eager_host_us": host_us, "io": io}
+
+
+def config_line(S, ms_step, kern, peak):
+    kv = S.kv_bytes
+    d = {"us_per_step": 1e3 * ms_step, "gbs": kv / (ms_step / 1e3) / 1e9,
+         "frac": kv / (ms_step / 1e3) / 1e9 / peak,
+         "kernel_alone_us": kern["mean_us"],
+         "kernel_alone_frac": kv / (kern["mean_us"] / 1e6) / 1e9 / peak,
+         "kv_bytes_per_step": kv, "seq_steps_per_s": S.w.B / (ms_step / 1e3),
+         "tokens_scored_per_s": S.w.B * S.w.T / (ms_step / 1e3),
+         "rotating_copies": S.ncopies}
+    if S.fp8:
+        d["bf16_equivalent_gbs"] = S.kv_bytes_bf16 / (ms_step / 1e3) / 1e9
+    return d
+
+
+def gpu_arm(a, w):
+    import torch
+    import torch.distributed as dist
+
+    import grouped_query_kv_gb300 as g
+    from grouped_query_kv_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    lib = g.lib()
+    peak, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    S = Setup(w, rank_seed(a.seed, rank), dev, lib, stream)
     g.check_device_error(stream)
 
+    # ---- warm-up, then exactly K timed steps (max over ranks)
+    run, graphs = time_chained(S, a.steps, a.warmup)
+    clocks = Clocks(local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+    clocks.start()
+    ms_total = time_run(S, run, a.steps, before=barrier, after=barrier)
+    clk = clocks.stop()
+    g.check_device_error(stream)
+    local_ms_step = ms_total / a.steps
+    ms_total, job_bytes = over_ranks(ms_total, S.kv_bytes * a.steps, world, dev)
+    ms_step = ms_total / a.steps
+    value = job_bytes / (ms_total / 1e3) / 1e9
+
+    # ---- spread of the step time, outside the timed region: events around
+    # each replay of a chain of steps
+    gsp = graphs[max(graphs)]
+    reps = max(10, min(200, 4000 // max(graphs)))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for k in range(reps):
+            gsp.replay()
+            evs[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    per = sorted(1e3 * evs[k].elapsed_time(evs[k + 1]) / max(graphs) for k in range(reps))
+    spread = {"p10": per[reps // 10], "p50": per[reps // 2], "p90": per[(9 * reps) // 10],
+              "over": "%d replays of the %d-step chain (us per step)" % (reps, max(graphs))}
+
+    # ---- the split-KV kernel alone (the dominant kernel of the step)
+    kern = kernel_alone(S, 100)
+    kern_gbs = S.kv_bytes / (kern["mean_us"] / 1e6) / 1e9
+    step_gbs = S.kv_bytes / (local_ms_step / 1e3) / 1e9
+    g.check_device_error(stream)
+
+    # ---- end to end with host buffers
+    e2e = e2e_graphs(S, a.e2e_steps)
+    g.check_device_error(stream)
+    e2e_ms, e2e_bytes = over_ranks(e2e["graph_ms"], S.kv_bytes, world, dev)
+    e2e_val = e2e_bytes / (e2e_ms / 1e3) / 1e9
+    eager_ms, _ = over_ranks(e2e["eager_ms"], S.kv_bytes, world, dev)
+
     traffic = stored_traffic(w.name)
+    step_desc = S.describe()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                   "Lmax": w.Lmax, "window": w.window, "seq_len": int(lens.max().item()),
-                   "kv_bytes_per_step": kv_bytes,
+                   "Lmax": w.Lmax, "window": w.window, "seq_len": int(S.lens.max().item()),
+                   "kv_bytes_per_step": S.kv_bytes,
                    "l2": "inputs larger than L2: %d rotating cache copies, %.0f MB (%.1fx L2)"
-                         % (ncopies, ncopies * cache_bytes / 1e6, ncopies * cache_bytes / l2),
+                         % (S.ncopies, S.ncopies * S.cache_bytes / 1e6,
+                            S.ncopies * S.cache_bytes / S.l2),
                    "T": w.T, "block_size": w.block_size, "kv_dtype": w.kv_dtype,
-                   "step": ("kv_append_fp8 then gqa_decode_attn_fp8 (8-bit cache: E4M3 codes and "
-                            "one fp32 scale per row; kv_bytes_per_step counts codes and scales), "
-                            "steps chained in CUDA graphs" if fp8 else
-                            "gqa_decode_step_paged (kv_append fused into the attention kernel, "
-                            "K/V reached through the block table), steps chained in CUDA graphs"
-                            if table is not None else
-                            "gqa_decode_attn_multi (T new tokens scored in one pass over the "
-                            "cache, which already holds their rows), steps chained in CUDA graphs"
-                            if w.T > 1 else
-                            "gqa_decode_step (kv_append fused into the attention kernel), "
-                            "steps chained in CUDA graphs"),
+                   "step": step_desc + ", steps chained in CUDA graphs of up to %d steps"
+                           % CHAIN_MAX,
                    "numerics": "bf16 in, fp32 accumulate and out",
                    "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
         "us_per_step_spread": spread,
         "seq_steps_per_s": world * w.B * a.steps / (ms_total / 1e3),
         "tokens_scored_per_s": world * w.B * w.T * a.steps / (ms_total / 1e3),
-        "bf16_equivalent_gbs": world * kv_bytes_bf16 * a.steps / (ms_total / 1e3) / 1e9,
+        "bf16_equivalent_gbs": world * S.kv_bytes_bf16 * a.steps / (ms_total / 1e3) / 1e9,
         "us_per_step": 1e3 * ms_step,
-        "hbm_fraction": achieved / peak,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak,
-                     "traffic": sum(traffic.values()) if traffic else None,
+        "hbm_fraction": (S.kv_bytes / (local_ms_step / 1e3) / 1e9) / peak,
+        "roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": step_gbs / peak,
+                     "frac_of_nominal": step_gbs / NOMINAL_HBM_GBS,
+                     "traffic": traffic.get(_decode_kernel_name(traffic)) if traffic else None,
                      "traffic_by_kernel": traffic,
-                     "kernel": ("kv_append_fp8 + gqa_decode_attn_fp8 (append, 8-bit split-KV "
-                                "kernel, combine), " if fp8 else
-                                "gqa_decode_step_paged (fused append + split-KV kernel over "
-                                "the block table + combine), " if table is not None else
-                                "gqa_decode_attn_multi (split-KV kernel + combine), " if w.T > 1
-                                else "gqa_decode_step (fused append + split-KV kernel + combine), ")
-                               +
-                               "average over the timed steps",
+                     "kernel": "the split-KV attention kernel of %s: one launch per step, "
+                               "back to back in the timed region, so its average launch "
+                               "interval there is the step time (the combine runs beside its "
+                               "tail and the next launch's prologue beside the combine)"
+                               % step_desc.split(" (")[0],
+                     "alone": {"achieved": kern_gbs, "frac": kern_gbs / peak,
+                               "frac_of_nominal": kern_gbs / NOMINAL_HBM_GBS, "duration": kern,
+                               "source": "CUDA events recorded just before and after the "
+                                         "split-KV kernel inside each of %d steps issued one by "
+                                         "one after the timed region (kvattn_set_kernel_events)"
+                                         "; without a neighbour to overlap, its launch and "
+                                         "prologue show in full" % kern["launches"]},
+                     "nominal_peak": NOMINAL_HBM_GBS,
                      "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind
                      if peak_kind == "measured" else "fallback 6800 GB/s"},
-        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
-                "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms,
-                "host_issue_us_per_step": host_us,
-                "api": "grouped_query_kv_gb300.%s (eager; one packed upload and one download per step on their own streams, double-buffered)"
-                       % ("kv_append_fp8 + gqa_decode_attn_fp8" if fp8 else
-                          "gqa_decode_step_paged" if table is not None else
-                          "gqa_decode_attn_multi" if w.T > 1 else "gqa_decode_step")},
-        "gpu_launches": (3 if fp8 else 2) * a.steps,
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": e2e["io"]["h2d"],
+                "d2h_bytes_per_step": e2e["io"]["d2h"], "ms_per_step": e2e_ms,
+                "steps": e2e["graph_steps"], "host_issue_us_per_step": e2e["graph_host_us"],
+                "api": "grouped_query_kv_gb300.%s per step, with its upload (one packed copy "
+                       "from pinned memory) and download on their own streams, double-buffered, "
+                       "the steps captured in CUDA graphs" % step_desc.split(" (")[0],
+                "eager": {"value": S.kv_bytes / (eager_ms / 1e3) / 1e9, "unit": "GB/s",
+                          "ms_per_step": eager_ms, "steps": e2e["eager_steps"],
+                          "host_issue_us_per_step": e2e["eager_host_us"],
+                          "api": "the same steps issued one by one from Python"}},
+        "gpu_launches": S.launches_per_step() * a.steps,
         "clocks": clk,
     }
+    S.free()
+    del S
+
+    # ---- the other target shapes, each timed the same way in this run
+    if not a.no_per_config and rank == 0 and world == 1:
+        pcs = {}
+        clocks_pc = Clocks(local)
+        clocks_pc.start()
+        for name in PER_CONFIG:
+            if name == w.name or name not in wl.WORKLOADS:
+                continue
+            wp = wl.WORKLOADS[name]
+            Sp = Setup(wp, a.seed, dev, lib, stream)
+            est_ms = max(0.01, Sp.kv_bytes / 6.0e9)
+            k = int(max(20, min(2000, 250.0 / est_ms)))
+            runp, _ = time_chained(Sp, k, 5)
+            msp = time_run(Sp, runp, k) / k
+            kp = kernel_alone(Sp, 20)
+            g.check_device_error(stream)
+            pcs[name] = config_line(Sp, msp, kp, peak)
+            pcs[name]["steps"] = k
+            pcs[name]["step"] = Sp.describe()
+            Sp.free()
+            del Sp, runp
+        line["per_config"] = pcs
+        line["per_config_clocks"] = clocks_pc.stop()
+
     if rank == 0 and not a.no_cpu_baseline:
         dt, nb, by, threads, reps = oracle_sample(w, a.seed, a.cpu_seconds)
         line["cpu_baseline"] = {
@@ -637,6 +827,13 @@ def gpu_arm(a, w):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _decode_kernel_name(traffic):
+    for k in traffic:
+        if k.startswith("decode"):
+            return k
+    return next(iter(traffic))
 
 
 def ctypes_void(v):

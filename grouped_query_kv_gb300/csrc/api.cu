@@ -180,7 +180,8 @@ int encode_fp8_map(CUtensorMap *m, const void *base, int D, int Lmax, int BH, in
 
 struct Plan {
     kvattn_plan pub;
-    int heads_per_seg;
+    int heads_per_seg;  // query rows per pass (heads, or hpg heads x T tokens)
+    int hpg;            // query heads per pass
     int np;  // tensor-core path: heads per pass rounded up to 16
     int cost_piece;  // schedule weight of a piece (a tile weighs 32)
 };
@@ -208,26 +209,31 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl, in
         return fail(KVATTN_ERR_UNSUPPORTED, "several new tokens need the tensor-core path");
     p.path = path;
     if (T > 1) {
-        // one pass takes the group's heads of all T tokens
-        if (tc_heads_per_seg(G * T, D) != G * T)
-            return fail(KVATTN_ERR_UNSUPPORTED,
-                        "G * T = %d query rows per K/V head exceed one pass (%d at D=%d)", G * T,
-                        tc_heads_per_seg(1 << 20, D), D);
-        pl->heads_per_seg = G * T;
-        pl->np = tc_np(G * T, D);
+        // one pass takes hpg of the group's heads for all T tokens as its
+        // columns; a group whose G x T query rows exceed one pass is split
+        // into passes of (nearly) equal head counts, each re-reading the K/V
+        const int maxcols = tc_heads_per_seg(1 << 20, D);  // columns one pass holds
+        if (T > maxcols)
+            return fail(KVATTN_ERR_UNSUPPORTED, "T = %d new tokens exceed one pass (%d at D=%d)",
+                        T, maxcols, D);
+        const int hmax = maxcols / T;
+        const int passes = (G + hmax - 1) / hmax;
+        pl->hpg = (G + passes - 1) / passes;
+        pl->heads_per_seg = pl->hpg * T;
+        pl->np = (pl->heads_per_seg + 15) / 16 * 16;
         p.tile_positions = tc_tile();
         p.stages = tc_stages(D, pl->np);
         p.threads = tc_threads();
         p.smem_bytes = tc_smem_bytes(D, pl->np);
     } else if (path == 2) {
-        pl->heads_per_seg = tc_heads_per_seg(G, D);
+        pl->heads_per_seg = pl->hpg = tc_heads_per_seg(G, D);
         pl->np = tc_np(G, D);
         p.tile_positions = tc_tile();
         p.stages = tc_stages(D, pl->np);
         p.threads = tc_threads();
         p.smem_bytes = tc_smem_bytes(D, pl->np);
     } else {
-        pl->heads_per_seg = fma_heads_per_seg(G);
+        pl->heads_per_seg = pl->hpg = fma_heads_per_seg(G);
         pl->np = 0;
         p.tile_positions = fma_tile(D);
         p.stages = fma_stages(D);
@@ -235,7 +241,7 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl, in
         p.smem_bytes = fma_smem_bytes(D, pl->heads_per_seg);
     }
     p.heads_per_cta = pl->heads_per_seg;
-    p.head_groups = T > 1 ? 1 : (G + pl->heads_per_seg - 1) / pl->heads_per_seg;
+    p.head_groups = (G + pl->hpg - 1) / pl->hpg;
     // CTA ranges balance cost: a tile costs W and a piece (q load, the first
     // tile's exact max, the output's read-out and stores) costs P more.
     // Measured on GB300 with the tensor-core kernel, a piece takes about
@@ -251,12 +257,12 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl, in
 
 // 3-D map over q, 128-byte swizzle.  One token per sequence: q viewed as
 // (D, B*Hq, 1) with box (64, np, 1).  T tokens: q [B, T, Hq, D] viewed as
-// (D, Hq, B*T) with box (64, G, T) -- the group's heads of every token.
-int encode_q_map(CUtensorMap *m, const void *base, int D, int B, int T, int Hq, int G, int np) {
+// (D, Hq, B*T) with box (64, hpg, T) -- one pass's heads of every token.
+int encode_q_map(CUtensorMap *m, const void *base, int D, int B, int T, int Hq, int hpg, int np) {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(T == 1 ? B * Hq : Hq),
                           (cuuint64_t)(T == 1 ? 1 : B * T)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)(T == 1 ? B * Hq : Hq) * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)(T == 1 ? np : G), (cuuint32_t)T};
+    cuuint32_t box[3] = {64, (cuuint32_t)(T == 1 ? np : hpg), (cuuint32_t)T};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -552,13 +558,14 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.Lmax = Lmax;
     p.G = Hq / Hkv;
     p.heads_per_seg = pl.heads_per_seg;
+    p.hpg = pl.hpg;
     p.head_groups = P.head_groups;
     p.tile = P.tile_positions;
     p.cost_piece = pl.cost_piece;
     p.window = window < Lmax ? window : Lmax;
     p.T = T;
     // bytes of one piece's q box: (64 columns x rows) per 64-column slab
-    p.q_bytes = (D / 64) * (T == 1 ? pl.np : p.G * T) * 128;
+    p.q_bytes = (D / 64) * (T == 1 ? pl.np : pl.hpg * T) * 128;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.block_table = pg ? pg->table : nullptr;
     p.block_lg = lg;
@@ -573,7 +580,7 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
         return cuda_fail(e, "recording the event before the split-KV kernel");
     if (P.path == 2) {
         CUtensorMap tmq;
-        if ((rc = encode_q_map(&tmq, q, D, B, T, Hq, p.G, pl.np))) return rc;
+        if ((rc = encode_q_map(&tmq, q, D, B, T, Hq, pl.hpg, pl.np))) return rc;
         e = pg ? tc_prepare_paged(D, pl.np, T > 1) : tc_prepare(D, pl.np, T > 1);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         e = pg ? launch_decode_tc_paged(tmk, tmv, tmq, p, pl.np, P.num_ctas, stream)
@@ -645,6 +652,7 @@ int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, cons
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.Lmax = Lmax;
     p.G = Hq / Hkv;
     p.heads_per_seg = pl.heads_per_seg;
+    p.hpg = pl.hpg;
     p.head_groups = P.head_groups;
     p.tile = P.tile_positions;
     // a tile carries half the bytes of a bf16 tile; a piece's fixed work

@@ -102,13 +102,17 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
     const int b = rec.x, seg = rec.y, first_slot = rec.z, npieces = rec.w;
     const int kvh = seg / p.head_groups;
     const int hg = seg % p.head_groups;
-    const int h0 = kvh * p.G + hg * p.heads_per_seg;
+    const int h0 = kvh * p.G + hg * p.hpg;
+    // columns: heads, or (token, head) pairs of the pass's hpg heads for T
+    // new tokens, of which the first hvalid heads exist
     const int gvalid = p.T == 1 ? min(p.heads_per_seg, p.G - hg * p.heads_per_seg)
-                                : p.heads_per_seg;  // (token, head) columns
+                                : p.heads_per_seg;
+    const int hvalid = min(p.hpg, p.G - hg * p.hpg);
     const int D = p.D;
     const int x = (blockIdx.y * kThreads + tid) * 4;
     const int g = x / D, d = x % D;
-    if (g >= gvalid) return;
+    const int t = p.T == 1 ? 0 : g / p.hpg, gg = p.T == 1 ? g : g % p.hpg;
+    if (g >= gvalid || gg >= hvalid) return;
 
     // piece k's workspace slot: the first piece is the last piece of CTA
     // c-1 (or its first), piece k >= 1 is the first piece of CTA c + k - 1
@@ -155,7 +159,6 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const DecodeParams p,
         mrun = mx;
     }
     const float inv = (den > 0.f) ? 1.f / den : 0.f;
-    const int t = p.T == 1 ? 0 : g / p.G, gg = p.T == 1 ? g : g % p.G;
     *reinterpret_cast<float4 *>(p.out + (((size_t)b * p.T + t) * p.Hq + h0 + gg) * D + d) =
         make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
 }

@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // first head; T tokens: q as (D, Hq, B*T), the group's heads
                         // of each of the sequence's T tokens, rows ordered (token, head)
                         mbar_arrive_expect_tx(&bs.q_full[qs], (uint32_t)p.q_bytes);
-                        const int h0 = kvh * p.G + hg * p.heads_per_seg;
+                        const int h0 = kvh * p.G + hg * p.hpg;
                         const int qy = MT ? h0 : itk.b * p.Hq + h0;
                         const int qz = MT ? itk.b * p.T : 0;
 #pragma unroll
@@ -636,9 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t0 = it.t;
         if (row == 0 && q4 == 0 && t0 == 0 && (it.len < 0 || it.len > p.Lmax))
             set_error(p.err, DEV_ERR_BOUNDS);
-        const int h0 = kvh * p.G + hg * p.heads_per_seg;
-        // columns: (token, head) for T new tokens, heads of one group otherwise
+        const int h0 = kvh * p.G + hg * p.hpg;
+        // columns: (token, head) for T new tokens, heads of one group otherwise;
+        // with T tokens a column is valid when its head is one of the pass's
+        // hvalid heads (the last pass of a group may hold fewer)
         const int gvalid = MT ? p.heads_per_seg : min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
+        const int hvalid = min(p.hpg, p.G - hg * p.hpg);
         const long long i0 = i;
 #pragma unroll
         for (int g = 0; g < NP; ++g) l[g] = 0.f;
@@ -697,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int g = 0; g < NP; ++g) {
                     if (pos >= len - (p.T - 1 - t)) s[g] = -INFINITY;
-                    if (++gg == p.G) {
+                    if (++gg == p.hpg) {
                         gg = 0;
                         ++t;
                     }
@@ -824,12 +827,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int t = 0, gg = 0;
 #pragma unroll
                 for (int g = 0; g < NP; ++g) {
-                    if (g < gvalid) {
+                    if (g < gvalid && gg < hvalid) {
                         const float lt = ltot_s[g];
                         p.out[(((size_t)b * p.T + t) * p.Hq + h0 + gg) * D + d] =
                             (lt > 0.f) ? o[g] / lt : 0.f;
                     }
-                    if (++gg == p.G) {
+                    if (++gg == p.hpg) {
                         gg = 0;
                         ++t;
                     }

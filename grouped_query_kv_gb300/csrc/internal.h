@@ -38,8 +38,10 @@ struct DecodeParams {
     int *split;               // [grid, 4] per-CTA combine record (b, seg, first slot, pieces)
     int B, Hq, Hkv, D, Lmax;
     int G;                    // Hq / Hkv
-    int heads_per_seg;        // query heads one segment serves
-    int head_groups;          // ceil(G / heads_per_seg)
+    int heads_per_seg;        // query rows one segment serves: heads, or (token, head) pairs
+                              // for T new tokens (hpg heads x T tokens)
+    int head_groups;          // passes per (b, kvh): ceil(G / hpg)
+    int hpg;                  // query heads per pass (T = 1: heads_per_seg)
     int tile;                 // positions per tile
     int window;               // positions attended at most (>= Lmax: all)
     int T;                    // new tokens (queries) per sequence, >= 1; q and out are

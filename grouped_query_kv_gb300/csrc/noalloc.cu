@@ -124,6 +124,7 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.Lmax = Lmax;
     p.G = G;
     p.heads_per_seg = hps;
+    p.hpg = hps;
     p.head_groups = (G + hps - 1) / hps;
     p.tile = tile;
     p.cost_piece = 16;  // the regular entry point's schedule weight for this path
