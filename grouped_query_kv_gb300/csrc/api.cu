@@ -163,12 +163,12 @@ int check_paged(const Paged &pg, int Hkv, const char *who, int *lg, int *Lmax) {
 }
 
 // 3-D map over an 8-bit cache [B*Hkv, Lmax, D] of one-byte codes: dims
-// (D, Lmax, B*Hkv), box (D, tile, 1), 128-byte swizzle (D = 128: one
-// 128-byte row per position).
+// (D, Lmax, B*Hkv), box (128, tile, 1), 128-byte swizzle: one box is the
+// tile's codes of 128 head dims (D / 128 boxes per tile).
 int encode_fp8_map(CUtensorMap *m, const void *base, int D, int Lmax, int BH, int tile) {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Lmax, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)D * (cuuint64_t)Lmax};
-    cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)tile, 1};
+    cuuint32_t box[3] = {128, (cuuint32_t)tile, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -613,7 +613,10 @@ int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, cons
     if (!std::isfinite(scale)) return fail(KVATTN_ERR_INVALID_ARG, "%s: scale must be finite", who);
     int rc = check_sizes(B, Hq, Hkv, D, Lmax);
     if (rc) return rc;
-    if (D != 128) return fail(KVATTN_ERR_UNSUPPORTED, "%s: an 8-bit cache needs D = 128 (D=%d)", who, D);
+    if (D != 128 && D != 256)
+        return fail(KVATTN_ERR_UNSUPPORTED,
+                    "%s: the 8-bit kernel reads 128-code rows per copy and needs D = 128 or 256 "
+                    "(D=%d)", who, D);
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int dev;
     if ((rc = current_device(&dev))) return rc;

@@ -44,7 +44,11 @@
 //     tile whose v_scale would break the bound lowers cv first, rescaling
 //     the accumulator by the same power of two (with the running-max
 //     rescale, in the same step).
-// Limits: D = 128.
+// D = 128 or 256.  A 128-position tile of codes is D / 128 TMA boxes of 128
+// positions x 128 codes (the 128-byte swizzle's width), side by side in its
+// staging slot; the q parts have one 128-code slab per box; Q K^T runs
+// 4 D / 128 K-steps of 32 codes, and P V runs one M = 128 block of MMAs per
+// 128 head dims, each into its own O^T accumulator.
 #include <cuda_fp16.h>
 
 #include "decode_tc.cuh"
@@ -53,7 +57,7 @@ namespace kvattn {
 
 namespace {
 
-constexpr int kStage = 16384;    // one staged tile: 128 positions x 128 codes
+constexpr int kBox = 16384;      // one TMA box: 128 positions x 128 codes
 constexpr int kQWarps = 2;       // warps 6-7 write the q parts
 constexpr int kQ8Threads = 192 + 32 * kQWarps;
 constexpr int kQ8EndThreads = 192;  // warps 0-5 meet before tensor memory is freed
@@ -61,9 +65,12 @@ constexpr float kTauQ8 = 2.f;    // rescale once a score passes the running max 
 constexpr float kVHi = 64.f;     // v_scale[j] 2^cv stays <= 64
 constexpr int kCvNone = 1 << 20; // cv not chosen yet (piece start)
 
-template <int NP>
+template <int D, int NP>
 struct Q8Cfg {
-    static constexpr int QB = 2 * NP * 128;   // one q buffer: NP hi rows, then NP lo rows (E4M3, swizzled)
+    static constexpr int SL = D / 128;        // 128-code slabs per row
+    static constexpr int kStage = SL * kBox;  // one staged tile: 128 positions x D codes
+    static constexpr int QSL = 2 * NP * 128;  // one slab of a q buffer: NP hi rows, NP lo rows
+    static constexpr int QB = SL * QSL;       // one q buffer (E4M3, swizzled, K-major)
     static constexpr int PB = 3 * NP * kT;    // one P stage: 3 NP E4M3 columns x 128 positions
     static constexpr int PST = 2;
     static constexpr int NS_MAX = 12;
@@ -95,12 +102,12 @@ struct Q8Cfg {
     static_assert(off_q % 1024 == 0 && off_p % 1024 == 0 && QB % 1024 == 0, "swizzle atoms");
 
     // TMEM: S0, S1 (side by side: 2 NP columns each, hi part then lo part;
-    // else NP columns), then the O^T accumulator (3 NP columns: hi, mid, lo
-    // parts of P)
+    // else NP columns), then per 128 head dims an O^T accumulator (3 NP
+    // columns: hi, mid, lo parts of P)
     static constexpr bool SBS = NP <= 32;
     static constexpr int SW = SBS ? 2 * NP : NP;
     static constexpr int OA = 2 * SW;
-    static constexpr int TMEM_COLS = pow2_at_least(OA + 3 * NP);
+    static constexpr int TMEM_COLS = pow2_at_least(OA + SL * 3 * NP);
     static constexpr uint32_t IDESC_QK = idesc_e4m3_f32(128, SW, false, false);
     static constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, 3 * NP, true, true);
 };
@@ -128,12 +135,13 @@ __device__ __forceinline__ float2 e4m3x2_value(uint16_t two) {
 // 2^e as a binary32 value, e in [-126, 127].
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-template <int NP>
+template <int D, int NP>
 __global__ void __launch_bounds__(kQ8Threads, 1)
     decode_q8_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
-    using C = Q8Cfg<NP>;
-    constexpr int D = 128;
+    using C = Q8Cfg<D, NP>;
+    constexpr int SL = C::SL;
+    constexpr int kStage = C::kStage;
     constexpr int NSK = C::NSK;
     constexpr int NSV = C::NSV;
 
@@ -235,7 +243,10 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                     return false;
                 mbar_arrive_expect_tx(&full[slot], kStage);
                 const int z = it.b * p.Hkv + it.seg / p.head_groups;
-                tma_load_3d(base + slot * kStage, tm, &full[slot], 0, it.row0(), z, pol);
+#pragma unroll
+                for (int sl = 0; sl < SL; ++sl)
+                    tma_load_3d(base + slot * kStage + sl * kBox, tm, &full[slot], sl * 128,
+                                it.row0(), z, pol);
                 ++n;
                 return true;
             };
@@ -292,31 +303,44 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
                 uint8_t *qb = qbuf + qs * C::QB;
                 for (int g = qw; g < NP; g += kQWarps) {
-                    float x[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (g < gvalid) {  // lane l holds columns 4l .. 4l + 3
-                        const uint2 raw = reinterpret_cast<const uint2 *>(
-                            p.q)[((size_t)itq.b * p.Hq + h0 + g) * (D / 4) + lane];
-                        x[0] = __uint_as_float(raw.x << 16);
-                        x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-                        x[2] = __uint_as_float(raw.y << 16);
-                        x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+                    // lane l holds columns 128 sl + 4l .. 128 sl + 4l + 3 of each slab sl
+                    float x[SL][4];
+                    float amax = 0.f;
+#pragma unroll
+                    for (int sl = 0; sl < SL; ++sl) {
+                        x[sl][0] = x[sl][1] = x[sl][2] = x[sl][3] = 0.f;
+                        if (g < gvalid) {
+                            const uint2 raw = reinterpret_cast<const uint2 *>(
+                                p.q)[((size_t)itq.b * p.Hq + h0 + g) * (D / 4) + sl * 32 + lane];
+                            x[sl][0] = __uint_as_float(raw.x << 16);
+                            x[sl][1] = __uint_as_float(raw.x & 0xFFFF0000u);
+                            x[sl][2] = __uint_as_float(raw.y << 16);
+                            x[sl][3] = __uint_as_float(raw.y & 0xFFFF0000u);
+                        }
+                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[sl][0]), fabsf(x[sl][1])),
+                                                 fmaxf(fabsf(x[sl][2]), fabsf(x[sl][3]))));
                     }
-                    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
                     amax = warp_max(amax);
                     // c = 7 - floor(log2 amax), kept where 2^c and 2^-c are normal
                     int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
                     e = max(-119, min(e, 120));
                     const float sc = pow2i(7 - e);
-                    float y[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) y[u] = x[u] * sc;  // exact: a power of two
-                    const uint16_t h01 = e4m3x2_of(y[0], y[1]), h23 = e4m3x2_of(y[2], y[3]);
-                    const float2 v01 = e4m3x2_value(h01), v23 = e4m3x2_value(h23);
-                    const uint16_t l01 = e4m3x2_of(y[0] - v01.x, y[1] - v01.y);
-                    const uint16_t l23 = e4m3x2_of(y[2] - v23.x, y[3] - v23.y);
                     const int off = (((lane >> 2) ^ (g & 7)) << 4) + 4 * (lane & 3);
-                    *reinterpret_cast<uint32_t *>(qb + g * 128 + off) = (uint32_t)h01 | ((uint32_t)h23 << 16);
-                    *reinterpret_cast<uint32_t *>(qb + (NP + g) * 128 + off) = (uint32_t)l01 | ((uint32_t)l23 << 16);
+#pragma unroll
+                    for (int sl = 0; sl < SL; ++sl) {
+                        float y[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) y[u] = x[sl][u] * sc;  // exact: a power of two
+                        const uint16_t h01 = e4m3x2_of(y[0], y[1]), h23 = e4m3x2_of(y[2], y[3]);
+                        const float2 v01 = e4m3x2_value(h01), v23 = e4m3x2_value(h23);
+                        const uint16_t l01 = e4m3x2_of(y[0] - v01.x, y[1] - v01.y);
+                        const uint16_t l23 = e4m3x2_of(y[2] - v23.x, y[3] - v23.y);
+                        uint8_t *qs_b = qb + sl * C::QSL;
+                        *reinterpret_cast<uint32_t *>(qs_b + g * 128 + off) =
+                            (uint32_t)h01 | ((uint32_t)h23 << 16);
+                        *reinterpret_cast<uint32_t *>(qs_b + (NP + g) * 128 + off) =
+                            (uint32_t)l01 | ((uint32_t)l23 << 16);
+                    }
                     if (lane == 0) qinv_s[qs * 64 + g] = (g < gvalid) ? pow2i(e - 7) : 0.f;
                 }
                 fence_proxy_async_smem();
@@ -360,12 +384,16 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                         const uint32_t pstage = pbuf_s + (int)(j % C::PST) * C::PB;
                         const uint32_t v0 = vst_s + slot * kStage;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            // A = V^T: the staged tile read position-major (SW128);
-                            // B = P: position-major, no swizzle, 16-column blocks
-                            const uint64_t ad = smem_desc(v0 + kk * 4096, 16384, 1024, 2);
-                            const uint64_t bd = smem_desc(pstage + kk * 512, 128, 2048, 0);
-                            umma_f8(tmem + C::OA, ad, bd, C::IDESC_PV, !(first_pv && kk == 0));
+                        for (int sl = 0; sl < SL; ++sl) {  // head dims 128 sl .. 128 sl + 127
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                // A = V^T: the staged box read position-major (SW128);
+                                // B = P: position-major, no swizzle, 16-column blocks
+                                const uint64_t ad = smem_desc(v0 + sl * kBox + kk * 4096, 16384, 1024, 2);
+                                const uint64_t bd = smem_desc(pstage + kk * 512, 128, 2048, 0);
+                                umma_f8(tmem + C::OA + sl * 3 * NP, ad, bd, C::IDESC_PV,
+                                        !(first_pv && kk == 0));
+                            }
                         }
                         umma_commit(&vst_empty[slot]);
                         umma_commit(&pv_done[pb]);
@@ -391,13 +419,20 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                         tc_fence_after();
                         const uint32_t a0 = kst_s + slot * kStage;
                         const uint32_t b0 = qbuf_s + qcur * C::QB;
+                        // 32 codes per MMA; side by side the hi and lo rows are one
+                        // operand of 2 NP rows, else the lo part follows the hi part
 #pragma unroll
-                        for (int kk = 0; kk < (C::SBS ? 4 : 8); ++kk) {  // 32 codes per MMA
-                            const uint64_t ad = smem_desc(a0 + (kk & 3) * 32, 16, 1024, 2);
-                            const uint64_t bd =
-                                smem_desc(b0 + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024, 2);
-                            umma_f8(tmem + sb * C::SW, ad, bd, C::IDESC_QK, kk != 0);
-                        }
+                        for (int part = 0; part < (C::SBS ? 1 : 2); ++part)
+#pragma unroll
+                            for (int sl = 0; sl < SL; ++sl)
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t ad = smem_desc(a0 + sl * kBox + kk * 32, 16, 1024, 2);
+                                    const uint64_t bd = smem_desc(
+                                        b0 + sl * C::QSL + part * (NP * 128) + kk * 32, 16, 1024, 2);
+                                    umma_f8(tmem + sb * C::SW, ad, bd, C::IDESC_QK,
+                                            part != 0 || sl != 0 || kk != 0);
+                                }
                         umma_commit(&kst_empty[slot]);
                         umma_commit(&s_full[sb]);
                         if (itq.last_tile_of_segment() || i == ntiles - 1) umma_commit(&q_empty[qcur]);
@@ -567,7 +602,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                         fail = true;
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < 3 * NP / 16; ++c) {
+                    for (int c = 0; c < SL * 3 * NP / 16; ++c) {
                         float v[16];
                         const uint32_t a = lane_base + C::OA + c * 16;
                         tmem_ld16(a, v);
@@ -658,30 +693,34 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         const bool complete = (t0 == 0) && it.last_tile_of_segment();
         const size_t slot = 2 * (size_t)blockIdx.x + (first_piece ? 0 : 1);
         const float vinv = (cv == kCvNone) ? 1.f : ldexpf(1.f, -cv);
-        float o[NP];
 #pragma unroll
-        for (int c = 0; c < NP / 16; ++c) {  // O^T = (hi + mid + lo parts) 2^-cv
-            float v[16], w[16], x[16];
-            tmem_ld16(lane_base + C::OA + c * 16, v);
-            tmem_ld16(lane_base + C::OA + NP + c * 16, w);
-            tmem_ld16(lane_base + C::OA + 2 * NP + c * 16, x);
-            tmem_ld_wait();
+        for (int sl = 0; sl < SL; ++sl) {  // head dims 128 sl + row
+            const uint32_t oa = lane_base + C::OA + sl * 3 * NP;
+            float o[NP];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[c * 16 + k] = (v[k] + w[k] + x[k]) * vinv;
-        }
-        const int d = row;
-        if (complete) {
+            for (int c = 0; c < NP / 16; ++c) {  // O^T = (hi + mid + lo parts) 2^-cv
+                float v[16], w[16], x[16];
+                tmem_ld16(oa + c * 16, v);
+                tmem_ld16(oa + NP + c * 16, w);
+                tmem_ld16(oa + 2 * NP + c * 16, x);
+                tmem_ld_wait();
 #pragma unroll
-            for (int g = 0; g < NP; ++g) {
-                if (g < gvalid) {
-                    const float lt = ltot_s[g];
-                    p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (lt > 0.f) ? o[g] / lt : 0.f;
-                }
+                for (int k = 0; k < 16; ++k) o[c * 16 + k] = (v[k] + w[k] + x[k]) * vinv;
             }
-        } else {
+            const int d = sl * 128 + row;
+            if (complete) {
 #pragma unroll
-            for (int g = 0; g < NP; ++g)
-                if (g < gvalid) p.ws_o[(slot * p.heads_per_seg + g) * D + d] = o[g];
+                for (int g = 0; g < NP; ++g) {
+                    if (g < gvalid) {
+                        const float lt = ltot_s[g];
+                        p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (lt > 0.f) ? o[g] / lt : 0.f;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < NP; ++g)
+                    if (g < gvalid) p.ws_o[(slot * p.heads_per_seg + g) * D + d] = o[g];
+            }
         }
         tc_fence_before();
         __syncwarp();
@@ -703,7 +742,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     named_bar_sync(kBarEnd, kQ8EndThreads);
 }
 
-template <int NP>
+template <int D, int NP>
 cudaError_t launch_q8(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeParams &p,
                       int num_ctas, cudaStream_t stream) {
     static int done_for_device[64] = {0};
@@ -711,43 +750,49 @@ cudaError_t launch_q8(const CUtensorMap &tmk, const CUtensorMap &tmv, const Deco
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (!(dev >= 0 && dev < 64 && done_for_device[dev])) {
-        e = cudaFuncSetAttribute(decode_q8_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Q8Cfg<NP>::alloc);
+        e = cudaFuncSetAttribute(decode_q8_kernel<D, NP>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Q8Cfg<D, NP>::alloc);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) done_for_device[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_ctas);
     cfg.blockDim = dim3(kQ8Threads);
-    cfg.dynamicSmemBytes = Q8Cfg<NP>::alloc;
+    cfg.dynamicSmemBytes = Q8Cfg<D, NP>::alloc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_q8_kernel<NP>, tmk, tmv, p);
+    return cudaLaunchKernelEx(&cfg, decode_q8_kernel<D, NP>, tmk, tmv, p);
 }
 
 }  // namespace
 
-int q8_smem_bytes(int np) {
-    switch (np) {
-        case 16: return Q8Cfg<16>::alloc;
-        case 32: return Q8Cfg<32>::alloc;
-        case 48: return Q8Cfg<48>::alloc;
-        case 64: return Q8Cfg<64>::alloc;
+int q8_smem_bytes(int D, int np) {
+    switch (D * 1000 + np) {
+        case 128016: return Q8Cfg<128, 16>::alloc;
+        case 128032: return Q8Cfg<128, 32>::alloc;
+        case 128048: return Q8Cfg<128, 48>::alloc;
+        case 128064: return Q8Cfg<128, 64>::alloc;
+        case 256016: return Q8Cfg<256, 16>::alloc;
+        case 256032: return Q8Cfg<256, 32>::alloc;
+        case 256048: return Q8Cfg<256, 48>::alloc;
         default: return -1;
     }
 }
 
 cudaError_t launch_decode_q8(const CUtensorMap &tmk, const CUtensorMap &tmv,
                              const DecodeParams &p, int np, int num_ctas, cudaStream_t stream) {
-    switch (np) {
-        case 16: return launch_q8<16>(tmk, tmv, p, num_ctas, stream);
-        case 32: return launch_q8<32>(tmk, tmv, p, num_ctas, stream);
-        case 48: return launch_q8<48>(tmk, tmv, p, num_ctas, stream);
-        case 64: return launch_q8<64>(tmk, tmv, p, num_ctas, stream);
+    switch (p.D * 1000 + np) {
+        case 128016: return launch_q8<128, 16>(tmk, tmv, p, num_ctas, stream);
+        case 128032: return launch_q8<128, 32>(tmk, tmv, p, num_ctas, stream);
+        case 128048: return launch_q8<128, 48>(tmk, tmv, p, num_ctas, stream);
+        case 128064: return launch_q8<128, 64>(tmk, tmv, p, num_ctas, stream);
+        case 256016: return launch_q8<256, 16>(tmk, tmv, p, num_ctas, stream);
+        case 256032: return launch_q8<256, 32>(tmk, tmv, p, num_ctas, stream);
+        case 256048: return launch_q8<256, 48>(tmk, tmv, p, num_ctas, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -108,9 +108,9 @@ cudaError_t launch_decode_tc_paged(const CUtensorMap &tmk, const CUtensorMap &tm
 
 cudaError_t launch_combine(const DecodeParams &p, int num_ctas, cudaStream_t stream);
 
-// 8-bit (FP8 E4M3) cache: the attention kernel (D = 128; np as tc_np), the
-// row quantizer and the append.
-int q8_smem_bytes(int np);
+// 8-bit (FP8 E4M3) cache: the attention kernel (D = 128 or 256; np as
+// tc_np), the row quantizer and the append.
+int q8_smem_bytes(int D, int np);
 cudaError_t launch_decode_q8(const CUtensorMap &tmk, const CUtensorMap &tmv,
                              const DecodeParams &p, int np, int num_ctas, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(const void *src, void *codes, float *scales, long long rows,

@@ -104,6 +104,12 @@ WORKLOADS = {w.name: w for w in [
              scale=1.0 / math.sqrt(128), ragged=True, kv_dtype="fp8",
              note="Llama-70B-shaped GQA decode over an 8-bit (E4M3 + per-row scale) "
                   "cache, lengths uniform in [1, 8192]"),
+    Workload("palm8b_fp8", B=64, Hq=16, Hkv=1, D=256, Lmax=2048,
+             scale=1.0 / 16.0, lens=(2048,), kv_dtype="fp8",
+             note="the PaLM-8B-shaped MQA decode over an 8-bit (E4M3 + per-row scale) cache"),
+    Workload("palm540b_fp8", B=8, Hq=48, Hkv=1, D=256, Lmax=32768,
+             scale=1.0 / 16.0, lens=(32768,), k_scale=0.5, kv_dtype="fp8",
+             note="the PaLM-540B-shaped long-context MQA decode over an 8-bit cache"),
     Workload("llama70b_paged64", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
              scale=1.0 / math.sqrt(128), ragged=True, block_size=64,
              note="the same over 64-position blocks"),

@@ -330,8 +330,11 @@ KVATTN_API int kv_append_fp8(void *k_codes, void *v_codes, float *k_scale, float
  * [B, Hq, D] (any finite value: each head enters the 8-bit products as two
  * E4M3 parts under a power-of-two scale, exact for a bf16 value), out fp32
  * [B, Hq, D]; lengths, errors and ownership as gqa_decode_attn.
- * Needs D = 128 (KVATTN_ERR_UNSUPPORTED otherwise).  Rows at and past
- * seq_lens[b], codes and scales, are never read. */
+ * Needs D = 128 or 256: the kernel copies each position's codes in rows of
+ * 128 (one 128-byte swizzled TMA box per 128 head dims); D = 64 is
+ * KVATTN_ERR_UNSUPPORTED (not built: its 64-byte rows would need a layout
+ * of their own).  Rows at and past seq_lens[b], codes and scales, are never
+ * read. */
 KVATTN_API int gqa_decode_attn_fp8(const void *q, const void *k_codes, const void *v_codes,
                                    const float *k_scale, const float *v_scale,
                                    const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,

@@ -73,11 +73,10 @@ def test_fp8_append_is_bit_exact():
         g.check_device_error()
 
 
-def _fp8_case(B, Hq, Hkv, Lmax, lens, seed, v_mul=1.0, k_mul=1.0, poison=True):
+def _fp8_case(B, Hq, Hkv, Lmax, lens, seed, v_mul=1.0, k_mul=1.0, poison=True, D=128):
     """bf16 draws quantized on the GPU (the quantizer is bit-exact), rows
     past each length poisoned with NaN codes and scales."""
     dev = torch.device("cuda")
-    D = 128
     gen = torch.Generator(device=dev).manual_seed(seed)
     q = torch.randn((B, Hq, D), generator=gen, device=dev).to(torch.bfloat16)
     k = torch.randn((B, Hkv, Lmax, D), generator=gen, device=dev)
@@ -122,30 +121,35 @@ def _check(q, kc, vc, ks, vs, lens, scale, sel=None):
     return out
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (32, 4), (64, 8), (16, 1), (48, 1), (64, 1), (24, 2)])
-def test_fp8_attention_matches_oracle(Hq, Hkv):
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 8, 8), (128, 32, 4), (128, 64, 8), (128, 16, 1),
+                                      (128, 48, 1), (128, 64, 1), (128, 24, 2), (256, 8, 8),
+                                      (256, 16, 1), (256, 32, 2), (256, 48, 1), (256, 96, 2),
+                                      (256, 24, 3)])
+def test_fp8_attention_matches_oracle(D, Hq, Hkv):
     lens = [1, 2, 63, 127, 128, 129, 255, 256, 300, 511, 600]
-    q, kc, vc, ks, vs, lt = _fp8_case(len(lens), Hq, Hkv, 600, lens, seed=Hq + Hkv)
-    _check(q, kc, vc, ks, vs, lt, 1.0 / np.sqrt(128))
+    q, kc, vc, ks, vs, lt = _fp8_case(len(lens), Hq, Hkv, 600, lens, seed=Hq + Hkv + D, D=D)
+    _check(q, kc, vc, ks, vs, lt, 1.0 / np.sqrt(D))
 
 
+@pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("ctas", [1, 3, 17, 152, 500])
-def test_fp8_split_pieces_merge(ctas):
+def test_fp8_split_pieces_merge(ctas, D):
     g.set_tuning(0, ctas)
     try:
-        q, kc, vc, ks, vs, lt = _fp8_case(4, 32, 4, 3000, [3000, 1, 1709, 130], seed=ctas)
+        q, kc, vc, ks, vs, lt = _fp8_case(4, 32, 4, 3000, [3000, 1, 1709, 130], seed=ctas, D=D)
         _check(q, kc, vc, ks, vs, lt, 0.09)
     finally:
         g.set_tuning(0, 0)
 
 
-def test_fp8_scales_across_magnitudes():
+@pytest.mark.parametrize("D", [128, 256])
+def test_fp8_scales_across_magnitudes(D):
     # key rows spread over e^-5 .. e^2 and value rows over e^-3 .. e^0.5: the
-    # per-row scales carry them (P is f16 in the kernel, so its error is
-    # relative to |V|, about 2^-12; values of order one keep it inside the
-    # absolute bound)
-    q, kc, vc, ks, vs, lt = _fp8_case(3, 16, 2, 400, [400, 250, 77], seed=9, k_mul="rows")
-    _check(q, kc, vc, ks, vs, lt, 1.0)
+    # per-row scales carry them (the weights enter as three E4M3 parts, so
+    # their error is relative to |V|, about 2^-12; values of order one keep
+    # it inside the absolute bound)
+    q, kc, vc, ks, vs, lt = _fp8_case(3, 16, 2, 400, [400, 250, 77], seed=9, k_mul="rows", D=D)
+    _check(q, kc, vc, ks, vs, lt, 1.0 / np.sqrt(D / 128))
 
 
 def test_fp8_empty_sequences_and_bad_lengths():
@@ -163,7 +167,7 @@ def test_fp8_empty_sequences_and_bad_lengths():
 
 def test_fp8_rejects_other_head_dims():
     dev = torch.device("cuda")
-    for D in (64, 256):
+    for D in (64,):
         q = torch.zeros((1, 8, D), dtype=torch.bfloat16, device=dev)
         c = torch.zeros((1, 1, 64, D), dtype=torch.uint8, device=dev)
         s = torch.ones((1, 1, 64), dtype=torch.float32, device=dev)
@@ -178,3 +182,16 @@ def test_llama70b_fp8_workload_sampled():
     q, kc, vc, ks, vs, lt = _fp8_case(w.B, w.Hq, w.Hkv, w.Lmax, lens, seed=0, poison=False)
     rng = np.random.default_rng(2)
     _check(q, kc, vc, ks, vs, lt, w.scale, sel=sorted(rng.choice(w.B, 4, replace=False).tolist()))
+
+
+@pytest.mark.parametrize("name,nsel", [("palm8b_mqa", 6), ("palm540b_long_mqa", 2)])
+def test_palm_fp8_workloads_sampled(name, nsel):
+    # the pages' multi-query shapes at D = 256 over an 8-bit cache, with the
+    # workloads' own lengths and key scaling; sampled sequences against the
+    # oracle
+    w = wl.WORKLOADS[name]
+    lens = wl.attn_lens(w, 0).tolist()
+    q, kc, vc, ks, vs, lt = _fp8_case(w.B, w.Hq, w.Hkv, w.Lmax, lens, seed=1, poison=False,
+                                      k_mul=w.k_scale, D=w.D)
+    rng = np.random.default_rng(3)
+    _check(q, kc, vc, ks, vs, lt, w.scale, sel=sorted(rng.choice(w.B, nsel, replace=False).tolist()))
