@@ -400,11 +400,8 @@ class Setup:
         out = P(self.out if out is None else out)
         sp = self.sp
         if self.fp8:
-            rc = lib.kv_append_fp8(P(c[0]), P(c[1]), P(c[2]), P(c[3]), kn, vn, pos, w.B, w.Hkv,
-                                   w.D, w.Lmax, sp)
-            assert rc == 0, lib.kvattn_last_error()
-            rc = lib.gqa_decode_attn_fp8(q, P(c[0]), P(c[1]), P(c[2]), P(c[3]), lens, out, w.B,
-                                         w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
+            rc = lib.gqa_decode_step_fp8(q, kn, vn, P(c[0]), P(c[1]), P(c[2]), P(c[3]), pos, out,
+                                         w.B, w.Hq, w.Hkv, w.D, w.Lmax, float(w.scale), sp)
         elif self.table is not None:
             tp = P(self.table if table is None else table)
             rc = lib.gqa_decode_step_paged(q, kn, vn, P(c[0]), P(c[1]), tp, pos, out, w.B, w.Hq,
@@ -422,13 +419,14 @@ class Setup:
         assert rc == 0, lib.kvattn_last_error()
 
     def launches_per_step(self):
-        return 3 if self.fp8 else 2
+        return 2
 
     def describe(self):
         w = self.w
         if self.fp8:
-            return ("kv_append_fp8 then gqa_decode_attn_fp8 (8-bit cache: E4M3 codes and one "
-                    "fp32 scale per row; kv_bytes_per_step counts codes and scales)")
+            return ("gqa_decode_step_fp8 (8-bit cache: E4M3 codes and one fp32 scale per row; "
+                    "the quantized append fused into the attention kernel; kv_bytes_per_step "
+                    "counts codes and scales)")
         if self.table is not None:
             return ("gqa_decode_step_paged (kv_append fused into the attention kernel, K/V "
                     "reached through the block table)")
@@ -549,9 +547,6 @@ def e2e_graphs(S, steps):
     x = S.x
     if w.T > 1:
         send = [("q", x["q"]), ("lens", S.lens)]
-    elif S.fp8:
-        send = [("q", x["q"]), ("k_new", x["k_new"]), ("v_new", x["v_new"]),
-                ("pos", S.pos), ("lens", S.lens)]
     else:
         send = [("q", x["q"]), ("k_new", x["k_new"]), ("v_new", x["v_new"]), ("pos", S.pos)]
     if S.table is not None:
@@ -588,10 +583,8 @@ def e2e_graphs(S, steps):
         if w.T > 1:
             g.gqa_decode_attn_multi(v["q"], c[0], c[1], v["lens"], w.scale, out=o, stream=stream)
         elif S.fp8:
-            g.kv_append_fp8(c[0], c[1], c[2], c[3], v["k_new"], v["v_new"], v["pos"],
-                            stream=stream)
-            g.gqa_decode_attn_fp8(v["q"], c[0], c[1], c[2], c[3], v["lens"], w.scale, out=o,
-                                  stream=stream)
+            g.gqa_decode_step_fp8(v["q"], v["k_new"], v["v_new"], c[0], c[1], c[2], c[3],
+                                  v["pos"], w.scale, out=o, stream=stream)
         elif S.table is not None:
             g.gqa_decode_step_paged(v["q"], v["k_new"], v["v_new"], c[0], c[1], v["table"],
                                     v["pos"], w.scale, out=o, stream=stream)

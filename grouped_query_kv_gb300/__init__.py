@@ -17,7 +17,7 @@ import threading
 __all__ = [
     "kv_append", "kv_append_multi", "kv_append_paged", "gqa_decode_attn", "gqa_decode_step",
     "gqa_decode_attn_multi", "gqa_decode_attn_paged", "gqa_decode_step_paged",
-    "kv_quantize_fp8", "kv_append_fp8", "gqa_decode_attn_fp8",
+    "kv_quantize_fp8", "kv_append_fp8", "gqa_decode_attn_fp8", "gqa_decode_step_fp8",
     "check_device_error", "get_plan",
     "set_tuning", "set_wait_limit", "set_kernel_events", "release", "KvAttnError", "library_path", "lib",
     "KVATTN_OK", "KVATTN_ERR_INVALID_ARG", "KVATTN_ERR_UNSUPPORTED",
@@ -76,6 +76,8 @@ _SIGS = {
     "kv_append_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "gqa_decode_attn_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                  ctypes.c_float, _VP]),
+    "gqa_decode_step_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
+                                 _I, ctypes.c_float, _VP]),
     "gqa_decode_attn_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
                                    _I, ctypes.c_float, _VP]),
     "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
@@ -465,6 +467,39 @@ def gqa_decode_attn_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale, 
     _check(lib().gqa_decode_attn_fp8(_ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
                                      _ptr(v_scale), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D,
                                      Lmax, float(scale), _stream_ptr(stream)))
+    return out
+
+
+def gqa_decode_step_fp8(q, k_new, v_new, k_codes, v_codes, k_scale, v_scale, seq_lens, scale,
+                        out=None, stream=None):
+    """kv_append_fp8 then gqa_decode_attn_fp8 over seq_lens[b] + 1 positions,
+    in one pass (the attention kernel writes the quantized rows first).
+    q bf16 [B, Hq, D]; k_new, v_new bf16 [B, Hkv, D]; codes uint8
+    [B, Hkv, Lmax, D] and scales fp32 [B, Hkv, Lmax], updated in place;
+    seq_lens int32 [B] (tokens cached before this step, not modified);
+    out optional fp32 [B, Hq, D].  Returns out."""
+    import torch
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    B, Hq, D = q.shape
+    _need(k_codes, "k_codes", torch.uint8)
+    if k_codes.dim() != 4 or k_codes.shape[0] != B or k_codes.shape[3] != D:
+        raise ValueError("k_codes must be [B, Hkv, Lmax, D] matching q")
+    Hkv, Lmax = k_codes.shape[1], k_codes.shape[2]
+    _need(v_codes, "v_codes", torch.uint8, (B, Hkv, Lmax, D))
+    _need(k_scale, "k_scale", torch.float32, (B, Hkv, Lmax))
+    _need(v_scale, "v_scale", torch.float32, (B, Hkv, Lmax))
+    _need(k_new, "k_new", torch.bfloat16, (B, Hkv, D))
+    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, D))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, (B, Hq, D))
+    _check(lib().gqa_decode_step_fp8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_codes),
+                                     _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+                                     _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, Lmax,
+                                     float(scale), _stream_ptr(stream)))
     return out
 
 

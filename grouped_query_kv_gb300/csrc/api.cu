@@ -598,15 +598,21 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     return KVATTN_OK;
 }
 
-// gqa_decode_attn over an 8-bit cache (decode_fp8.cu), D = 128.
+// gqa_decode_attn over an 8-bit cache (decode_fp8.cu), D = 128 or 256;
+// with k_new / v_new (gqa_decode_step_fp8) the kernel first writes this
+// step's rows, quantized, at seq_lens[b] and attends over one more position.
 int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, const float *k_scale,
                    const float *v_scale, const int32_t *seq_lens, float *out, int B, int Hq,
-                   int Hkv, int D, int Lmax, float scale, kvattn_stream_t stream_) {
-    const char *who = "gqa_decode_attn_fp8";
+                   int Hkv, int D, int Lmax, float scale, kvattn_stream_t stream_,
+                   const void *k_new = nullptr, const void *v_new = nullptr) {
+    const bool fused = k_new != nullptr || v_new != nullptr;
+    const char *who = fused ? "gqa_decode_step_fp8" : "gqa_decode_attn_fp8";
     t_last_error[0] = 0;
-    if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !seq_lens || !out)
+    if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !seq_lens || !out ||
+        (fused && (!k_new || !v_new)))
         return fail(KVATTN_ERR_INVALID_ARG, "%s: null pointer", who);
     if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(out) ||
+        (fused && (!aligned16(k_new) || !aligned16(v_new))) ||
         (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u) ||
         (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return fail(KVATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned (scales 4)", who);
@@ -646,7 +652,12 @@ int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, cons
     memset(&p, 0, sizeof p);
     p.q = static_cast<const uint16_t *>(q);
     p.seq_lens = seq_lens;
-    p.len_add = 0;
+    p.len_add = fused ? 1 : 0;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    // the codes (one byte each), written only by the fused append
+    p.k_cache = const_cast<uint16_t *>(static_cast<const uint16_t *>(k_codes));
+    p.v_cache = const_cast<uint16_t *>(static_cast<const uint16_t *>(v_codes));
     p.out = out;
     p.ws_o = static_cast<float *>(ws);
     p.ws_ml = p.ws_o + (size_t)2 * P.num_ctas * pl.heads_per_seg * D;
@@ -754,6 +765,18 @@ int gqa_decode_attn_fp8(const void *q, const void *k_codes, const void *v_codes,
                         kvattn_stream_t stream) {
     return run_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, out, B, Hq, Hkv, D,
                           Lmax, scale, stream);
+}
+
+int gqa_decode_step_fp8(const void *q, const void *k_new, const void *v_new, void *k_codes,
+                        void *v_codes, float *k_scale, float *v_scale, const int32_t *seq_lens,
+                        float *out, int B, int Hq, int Hkv, int D, int Lmax, float scale,
+                        kvattn_stream_t stream) {
+    if (!k_new || !v_new) {
+        t_last_error[0] = 0;
+        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_step_fp8: null pointer");
+    }
+    return run_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, out, B, Hq, Hkv, D,
+                          Lmax, scale, stream, k_new, v_new);
 }
 
 int kv_quantize_fp8(const void *src, void *codes, float *scales, long long rows, int D,

@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 
 #include "decode_tc.cuh"
+#include "fp8_codec.cuh"
 
 namespace kvattn {
 
@@ -227,43 +228,62 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     const uint32_t pbuf_s = smem_u32(pbuf);
 
     // ================================================================ producer
-    // Issue order K_0, K_1, V_0, K_2, V_1, ... (each ring in its own order)
+    // Issue order K_0, K_1, V_0, K_2, V_1, ... (each ring in its own order).
+    // The whole warp walks the tiles (the fused append quantizes a row with
+    // all 32 lanes); lane 0 alone waits on staging slots and issues copies.
     if (warp == 0) {
-        long long nk = 0, nv = 0;  // K and V stage copies issued (lane 0)
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            TileIter itk, itv;
-            itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
-            itv.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
-            bool ok = true;
-            auto issue = [&](const void *tm, const TileIter &it, uint8_t *base, uint64_t *full,
-                             uint64_t *empty, int ns, long long &n) -> bool {
-                const int slot = (int)(n % ns);
-                if (n >= ns && !wait_bar(&empty[slot], (uint32_t)(((n / ns) - 1) & 1), abort_flag))
-                    return false;
+        long long nk = 0, nv = 0;  // K and V stage copies issued
+        const uint64_t pol = l2_policy_evict_first();
+        TileIter itk, itv;
+        itk.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+        itv.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
+        bool ok = true;
+        auto issue = [&](const void *tm, const TileIter &it, uint8_t *base, uint64_t *full,
+                         uint64_t *empty, int ns, long long &n) -> bool {
+            const int slot = (int)(n % ns);
+            bool w = true;
+            if (lane == 0 && n >= ns) w = wait_bar(&empty[slot], (uint32_t)(((n / ns) - 1) & 1), abort_flag);
+            if (!__shfl_sync(0xffffffffu, w, 0)) return false;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&full[slot], kStage);
                 const int z = it.b * p.Hkv + it.seg / p.head_groups;
 #pragma unroll
                 for (int sl = 0; sl < SL; ++sl)
                     tma_load_3d(base + slot * kStage + sl * kBox, tm, &full[slot], sl * 128,
                                 it.row0(), z, pol);
-                ++n;
-                return true;
-            };
-            for (long long r = 0; r <= ntiles && ok; ++r) {
-                if (r < ntiles) {
-                    ok = issue(&tmk, itk, kst, kst_full, kst_empty, NSK, nk);
-                    itk.next();
-                }
-                if (r >= 1 && ok) {
-                    ok = issue(&tmv, itv, vst, vst_full, vst_empty, NSV, nv);
-                    itv.next();
-                }
             }
-            if (!ok) {
-                set_error(p.err, DEV_ERR_TIMEOUT);
-                *abort_flag = 1;
+            ++n;
+            return true;
+        };
+        for (long long r = 0; r <= ntiles && ok; ++r) {
+            if (r < ntiles) {
+                // fused append: this tile holds the new token's row -- its
+                // codes and scales are written (and made visible to the
+                // copies and to every SM) before the tile's copies go out
+                if (p.len_add && itk.last_tile_of_segment() && itk.len >= 1 && itk.len <= p.Lmax) {
+                    const int z = itk.b * p.Hkv + itk.seg / p.head_groups;
+                    const size_t dst = (size_t)z * p.Lmax + (itk.len - 1);
+                    uint8_t *kc = reinterpret_cast<uint8_t *>(p.k_cache);
+                    uint8_t *vc = reinterpret_cast<uint8_t *>(p.v_cache);
+                    quantize_row_warp<D / 32>(p.k_new + (size_t)z * D, kc + dst * D,
+                                              const_cast<float *>(p.k_scale) + dst, lane);
+                    quantize_row_warp<D / 32>(p.v_new + (size_t)z * D, vc + dst * D,
+                                              const_cast<float *>(p.v_scale) + dst, lane);
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __threadfence();
+                    __syncwarp();
+                }
+                ok = issue(&tmk, itk, kst, kst_full, kst_empty, NSK, nk);
+                itk.next();
             }
+            if (r >= 1 && ok) {
+                ok = issue(&tmv, itv, vst, vst_full, vst_empty, NSV, nv);
+                itv.next();
+            }
+        }
+        if (!ok && lane == 0) {
+            set_error(p.err, DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
         }
         __syncwarp();
         pdl_launch_dependents();
@@ -514,13 +534,23 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             const int r0 = it.row0();
             const int pos = r0 + row;
             const bool valid = row >= it.first_pos() - r0 && pos < len;
-            // this row's scales, loaded while the scores are made
+            // this row's scales, loaded while the scores are made -- except
+            // in a segment's last tile when this call appends: that tile may
+            // hold the row the copy warp has just written, so its scales are
+            // read once the tile's scores exist (the copy warp fenced its
+            // stores before issuing the tile's copies), past L1 (which may
+            // hold the line from the tile before)
+            const bool late = p.len_add && it.last_tile_of_segment();
             float ksc = 0.f, vsc = 0.f;
-            if (valid) {
+            if (valid && !late) {
                 ksc = p.k_scale[zrow + pos];
                 vsc = p.v_scale[zrow + pos];
             }
             bool fail = carry_fail || !wait_bar(&s_full[sb], (uint32_t)((i >> 1) & 1), abort_flag);
+            if (valid && late) {
+                ksc = __ldcg(p.k_scale + zrow + pos);
+                vsc = __ldcg(p.v_scale + zrow + pos);
+            }
             tc_fence_after();
             float s[NP];
 #pragma unroll

@@ -340,6 +340,24 @@ KVATTN_API int gqa_decode_attn_fp8(const void *q, const void *k_codes, const voi
                                    const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
                                    int D, int Lmax, float scale, kvattn_stream_t stream);
 
+/* gqa_decode_step_fp8 -- kv_append_fp8 followed by gqa_decode_attn_fp8 over
+ * seq_lens[b] + 1 positions, in one pass over the 8-bit cache (the decode
+ * step of "The Basics of Transformer Inference", KV-cache paragraph: write
+ * this token's K/V, then attend, itself included): the attention kernel's
+ * copy warp quantizes the new rows (the rule above, bit for bit the bytes
+ * kv_append_fp8 writes) into position seq_lens[b] just before it copies the
+ * tile that holds that position, so the step is one kernel launch (plus the
+ * combine when a sequence is split) instead of two.  k_new, v_new: bf16
+ * [B, Hkv, D], 16-byte aligned; seq_lens counts the tokens cached before
+ * this step and is not modified.  A sequence with seq_lens[b] outside
+ * [0, Lmax - 1] gets no append and a zero output row, and sets
+ * KVATTN_ERR_DEVICE_BOUNDS.  D = 128 or 256; other arguments, errors and
+ * ownership as gqa_decode_attn_fp8. */
+KVATTN_API int gqa_decode_step_fp8(const void *q, const void *k_new, const void *v_new,
+                                   void *k_codes, void *v_codes, float *k_scale, float *v_scale,
+                                   const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
+                                   int D, int Lmax, float scale, kvattn_stream_t stream);
+
 /*
  * gqa_decode_attn_noalloc -- the same computation as gqa_decode_attn, for
  * callers that must not have the library allocate device memory (for

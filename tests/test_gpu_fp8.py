@@ -195,3 +195,68 @@ def test_palm_fp8_workloads_sampled(name, nsel):
                                       k_mul=w.k_scale, D=w.D)
     rng = np.random.default_rng(3)
     _check(q, kc, vc, ks, vs, lt, w.scale, sel=sorted(rng.choice(w.B, nsel, replace=False).tolist()))
+
+
+def _step_check(D, Hq, Hkv, Lmax, cached, seed, scale):
+    """gqa_decode_step_fp8 against the oracle's kv_append_fp8 followed by its
+    attention over one more position: the codes and scales bit for bit (the
+    whole caches, so rows the step must not touch are checked too; rows past
+    each sequence's new row stay NaN-poisoned), the output within the bound."""
+    dev = torch.device("cuda")
+    B = len(cached)
+    q, kc, vc, ks, vs, pos = _fp8_case(B, Hq, Hkv, Lmax, cached, seed=seed, D=D)
+    gen = torch.Generator(device=dev).manual_seed(seed + 1)
+    kn = (torch.randn((B, Hkv, D), generator=gen, device=dev) * 3).to(torch.bfloat16)
+    vn = torch.randn((B, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+    refs = [a.cpu().numpy().copy() for a in (kc, vc, ks, vs)]
+    oracle.kv_append_fp8(*refs, bits(kn), bits(vn), np.asarray(cached, dtype=np.int32))
+    out = g.gqa_decode_step_fp8(q, kn, vn, kc, vc, ks, vs, pos, scale)
+    g.check_device_error()
+    assert np.array_equal(kc.cpu().numpy(), refs[0]), "fused append: K codes differ"
+    assert np.array_equal(vc.cpu().numpy(), refs[1]), "fused append: V codes differ"
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), refs[2].view(np.uint32))
+    assert np.array_equal(vs.cpu().numpy().view(np.uint32), refs[3].view(np.uint32))
+    lens = np.asarray(cached, dtype=np.int32) + 1
+    ref = oracle.gqa_decode_fp8(bits(q), refs[0], refs[1], refs[2], refs[3], lens, scale,
+                                nthreads=oracle_threads())
+    o = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(o))
+    vmax = max(float(np.abs(oracle.dequantize_fp8(refs[1][b, :, :n], refs[3][b, :, :n])).max())
+               for b, n in enumerate(lens))
+    err = float(np.abs(o - ref).max())
+    assert err <= min(ATOL, VREL * vmax), "max|err| %.3g" % err
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 16, 1), (128, 32, 4), (128, 64, 8), (256, 16, 1),
+                                      (256, 48, 1), (256, 32, 2)])
+def test_fp8_fused_step_matches_append_then_attend(D, Hq, Hkv):
+    # cached lengths on every tile edge (the new row opens a tile, ends one,
+    # or lands inside the shifted last tile), up to Lmax - 1
+    cached = [0, 1, 126, 127, 128, 129, 255, 299]
+    _step_check(D, Hq, Hkv, 300, cached, seed=D + Hq, scale=1.0 / np.sqrt(D))
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 152, 500])
+def test_fp8_fused_step_split_grids(ctas):
+    g.set_tuning(0, ctas)
+    try:
+        _step_check(256, 16, 1, 2500, [2499, 0, 1300, 700], seed=ctas, scale=1.0 / 16)
+    finally:
+        g.set_tuning(0, 0)
+
+
+def test_fp8_fused_step_full_cache_is_flagged():
+    # seq_lens[b] = Lmax: no room for the new row -- no append, a zero row,
+    # KVATTN_ERR_DEVICE_BOUNDS; the other sequences are served
+    dev = torch.device("cuda")
+    q, kc, vc, ks, vs, pos = _fp8_case(3, 16, 1, 256, [5, 5, 5], seed=8, poison=False)
+    kn = torch.randn((3, 1, 128), device=dev).to(torch.bfloat16)
+    bad = torch.tensor([4, 256, 17], dtype=torch.int32, device=dev)
+    before = kc.clone()
+    out = g.gqa_decode_step_fp8(q, kn, kn, kc, vc, ks, vs, bad, 0.1)
+    with pytest.raises(g.KvAttnError) as ei:
+        g.check_device_error()
+    assert ei.value.status == g.KVATTN_ERR_DEVICE_BOUNDS
+    assert torch.all(out[1] == 0)
+    assert torch.equal(kc[1], before[1])
+    assert not torch.equal(kc[0, :, 4], before[0, :, 4])  # the in-range rows were written
