@@ -24,10 +24,13 @@
 //     bits is a multiple of the bf16 ulp no larger than 8 of them, so
 //     hi + lo is q 2^c exactly for entries within 2^9 of the head's
 //     largest (smaller ones are off by at most 2^-17 of it: the remainder
-//     falls below E4M3's smallest step).  For passes of up to 32 heads the
-//     parts sit side by side as the 2 NP columns of one B operand and the
-//     softmax adds the two partial scores; wider passes, short of registers
-//     for that, run the lo part as 4 more MMAs into the same accumulator.
+//     falls below E4M3's smallest step).  The two parts sit side by side
+//     as the 2 NP columns of one B operand (at most 128, and 480 of the 512
+//     tensor-memory columns with the O accumulators at NP = 48, D = 256),
+//     so Q K^T takes 4 D / 128 MMAs per tile, and the softmax adds the two
+//     partial scores 16 columns at a time.  (Running the lo part as 4 more
+//     MMAs into the same accumulator, as passes of more than 32 heads once
+//     did, took the PaLM-540B-shaped step from 58.0 to 59.4 us.)
 //     Warps 6-7 write the parts; the softmax scales the score by
 //     2^-c k_scale[j].
 //   * P V.  The weight of position j for head g is w = p v_scale[j]
@@ -102,10 +105,10 @@ struct Q8Cfg {
     static_assert(alloc <= kSmemLimit, "shared memory");
     static_assert(off_q % 1024 == 0 && off_p % 1024 == 0 && QB % 1024 == 0, "swizzle atoms");
 
-    // TMEM: S0, S1 (side by side: 2 NP columns each, hi part then lo part;
-    // else NP columns), then per 128 head dims an O^T accumulator (3 NP
-    // columns: hi, mid, lo parts of P)
-    static constexpr bool SBS = NP <= 32;
+    // TMEM: S0, S1 (side by side: 2 NP columns each, hi part then lo part),
+    // then per 128 head dims an O^T accumulator (3 NP columns: hi, mid, lo
+    // parts of P)
+    static constexpr bool SBS = true;
     static constexpr int SW = SBS ? 2 * NP : NP;
     static constexpr int OA = 2 * SW;
     static constexpr int TMEM_COLS = pow2_at_least(OA + SL * 3 * NP);
