@@ -104,14 +104,15 @@ double oracle_e4m3_to_double(uint8_t code)
     return sign ? -v : v;
 }
 
-/* binary32 -> E4M3, round to nearest with ties to even, finite values
- * beyond the largest (448) saturate to +-448, NaN -> 0x7F. */
-uint8_t oracle_e4m3_from_float(float x)
+/* A real value (given in double) -> E4M3, round to nearest with ties to
+ * even, finite values beyond the largest (448) saturate to +-448,
+ * NaN -> 0x7F. */
+static uint8_t oracle_e4m3_from_double(double x)
 {
     if (isnan(x))
         return 0x7F;
     const uint8_t sign = signbit(x) ? 0x80 : 0x00;
-    const double a = fabs((double)x);
+    const double a = fabs(x);
     if (a > 448.0)
         return sign | 0x7E;
     if (a < ldexp(1.0, -6)) {                     /* subnormal range (or zero) */
@@ -131,6 +132,12 @@ uint8_t oracle_e4m3_from_float(float x)
     if (e > 8 || (e == 8 && m > 6.0))             /* past 448: saturate */
         return sign | 0x7E;
     return sign | (uint8_t)(((e + 7) << 3) | (int)m);
+}
+
+/* binary32 -> E4M3 (every binary32 value is exact in double). */
+uint8_t oracle_e4m3_from_float(float x)
+{
+    return oracle_e4m3_from_double((double)x);
 }
 
 /* One row of D bf16 values -> D codes and its scale (see the header). */

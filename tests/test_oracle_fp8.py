@@ -106,6 +106,66 @@ def test_quantized_rows_reproduce_their_values():
     assert np.all(err[~normal] <= 2.0 ** -10 * (1 + 1e-6))
 
 
+def _near_tie_rows():
+    """Rows [amax, x] of bf16 values chosen so that x / (amax / 448) is,
+    exactly, an E4M3 midpoint (1.3125 times a power of two: 448 x / amax =
+    21 / 16 * 2^e with x = 3 amax 2^e / 1024), while amax / 448 is not a
+    binary32 value: the binary32 scale is off by one rounding, the exact
+    quotient x / scale sits within a binary32 ulp of the midpoint, and the
+    quotient rounded to binary32 may land on the midpoint itself.  Whether
+    the code then comes out even (a tie) or from the exact side is what tells
+    a binary32 division from a double one."""
+    rows = []
+    for amax in range(1, 86, 2):
+        if amax % 7 == 0:
+            continue
+        for e in range(-6, 3):
+            x = 3.0 * amax * 2.0 ** e / 1024
+            if x >= amax:
+                continue
+            rows.append([amax, x])
+    r = np.asarray(rows, dtype=np.float64)
+    bits = _bits(r)
+    assert np.array_equal(_unbits(bits), r), "the constructed values are bf16-exact"
+    return bits
+
+
+def _e4m3_nearest_exact(q):
+    """Fractions -> E4M3 codes by exhaustive nearest search, ties to even
+    (exact rational comparison)."""
+    from fractions import Fraction
+    table = [(Fraction(float(v)), int(c)) for c, v in zip(FINITE, oracle.e4m3_decode(FINITE))
+             if v >= 0]
+    out = []
+    for v in q:
+        a = abs(v)
+        best = min(table, key=lambda t: (abs(t[0] - a), t[1] & 1))
+        out.append(best[1] | (0x80 if v < 0 else 0))
+    return np.asarray(out, dtype=np.uint8)
+
+
+def test_quantizer_divides_in_binary32():
+    # The reading: scale = absmax / 448 and code = E4M3(x / scale), both
+    # divisions IEEE binary32.  torch's float32 division and its
+    # float8_e4m3fn conversion restate that rule with library routines; the
+    # codes and scales must match them bit for bit, on rows where dividing
+    # in double (or exactly) instead gives other codes.
+    from fractions import Fraction
+    rows = _near_tie_rows()
+    codes, scales = oracle.quantize_fp8(rows)
+    x = torch.from_numpy(_unbits(rows)).to(torch.float32)
+    s32 = x.abs().amax(dim=1, keepdim=True) / 448.0
+    want_codes = (x / s32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(scales.view(np.uint32), s32[:, 0].numpy().view(np.uint32))
+    assert np.array_equal(codes, want_codes)
+    # the pin has teeth: the exact quotients round to other codes on some rows
+    exact = []
+    for r, s in zip(_unbits(rows), s32[:, 0].numpy()):
+        exact.append(_e4m3_nearest_exact([Fraction(float(v)) / Fraction(float(s)) for v in r]))
+    exact = np.asarray(exact)
+    assert (exact != want_codes).any(axis=1).sum() >= 5
+
+
 def test_zero_row_has_scale_one():
     codes, scales = oracle.quantize_fp8(np.zeros((2, 64), np.uint16))
     assert np.all(codes == 0) and np.all(scales == 1.0)
@@ -203,6 +263,12 @@ def _fp8_pins_pass(orc) -> bool:
         if not np.array_equal(orc.e4m3_encode(x),
                               torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()):
             return False
+        tie_rows = _near_tie_rows()
+        tc, ts = orc.quantize_fp8(tie_rows)
+        xt = torch.from_numpy(_unbits(tie_rows)).to(torch.float32)
+        st = xt.abs().amax(dim=1, keepdim=True) / 448.0
+        if not np.array_equal(tc, (xt / st).to(torch.float8_e4m3fn).view(torch.uint8).numpy()):
+            return False
         rng = np.random.default_rng(21)
         rows = _bits(rng.standard_normal((8, 64)))
         codes, scales = orc.quantize_fp8(rows)
@@ -235,6 +301,10 @@ MUTANTS = {
     "K read with the V scales": ("oracle_cache_at(k_cache, q8->k, q8->k_scale, row0, j, D, d)",
                                  "oracle_cache_at(k_cache, q8->k, q8->v_scale, row0, j, D, d)"),
     "scale of the previous row": ("* (double)scales[row0 + j];", "* (double)scales[row0 + (j > 0 ? j - 1 : 0)];"),
+    "quotient divided in double": ("        codes[d] = oracle_e4m3_from_float(x);\n",
+                                   "        codes[d] = oracle_e4m3_from_double(oracle_bf16_to_double(row[d]) / (double)s);\n"),
+    "quotient by the reciprocal": ("        volatile float x = (float)oracle_bf16_to_double(row[d]) / s;",
+                                   "        volatile float x = (float)oracle_bf16_to_double(row[d]) * (1.0f / s);"),
 }
 
 
