@@ -231,7 +231,7 @@ def test_llama70b_paged_workload_sampled():
                                   pg["block_table"], x["append_pos"], w.scale)
     g.check_device_error()
     rng = np.random.default_rng(3)
-    sel = sorted(rng.choice(w.B, 4, replace=False).tolist())
+    sel = sorted(rng.choice(w.B, 8, replace=False).tolist())
     lens = x["attn_lens"].cpu().numpy()[sel]
     table = pg["block_table"].cpu().numpy()[sel]
     k = oracle.gather_paged(bits(pg["k_pool"]), table, lens, w.block_size)

@@ -61,7 +61,7 @@ def test_sweep_points(name):
     w = wl.WORKLOADS[name]
     if w.B * w.Hkv * w.Lmax * w.D * 2 * 2 > (1 << 30):
         rng = np.random.default_rng(1)
-        run_step(w, sample_b=rng.choice(w.B, 4, replace=False))
+        run_step(w, sample_b=rng.choice(w.B, 8, replace=False))
     else:
         run_step(w)
 
