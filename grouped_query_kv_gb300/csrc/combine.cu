@@ -23,7 +23,7 @@ namespace kvattn {
 
 namespace {
 
-constexpr int kThreads = 256;  // four outputs (head, d..d+3) per thread
+constexpr int kThreads = 128;  // four outputs (head, d..d+3) per thread
 constexpr int kBatch = 8;      // pieces whose loads are in flight together
 
 __device__ __forceinline__ float ex2(float x) {
