@@ -82,6 +82,12 @@ _SIGS = {
                                    _I, ctypes.c_float, _VP]),
     "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
                                    _I, _I, _I, ctypes.c_float, _VP]),
+    "gqa_decode_attn_multi_window": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
+                                          ctypes.c_float, _I, _VP]),
+    "gqa_decode_attn_paged_window": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
+                                          _I, _I, ctypes.c_float, _I, _VP]),
+    "gqa_decode_step_paged_window": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I,
+                                          _I, _I, _I, _I, ctypes.c_float, _I, _VP]),
     "kvattn_status_string": (ctypes.c_char_p, [_I]),
     "kvattn_last_error": (ctypes.c_char_p, []),
     "kvattn_check_device_error": (_I, [_VP]),
@@ -274,13 +280,16 @@ def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out=None
     return out
 
 
-def gqa_decode_attn_multi(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None):
+def gqa_decode_attn_multi(q, k_cache, v_cache, seq_lens, scale, out=None, stream=None,
+                          window=None):
     """Attention for T new tokens per sequence, causal among themselves: token
-    t of sequence b attends positions [0, seq_lens[b] - T + 1 + t).
+    t of sequence b attends positions [0, e) with e = seq_lens[b] - T + 1 + t
+    (only [e - window, e) for a local attention layer).
 
     q: bf16 [B, T, Hq, D]; caches: bf16 [B, Hkv, Lmax, D] already holding the
     new tokens' rows; seq_lens: int32 [B], tokens in the cache including the
-    new ones; out: optional fp32 [B, T, Hq, D].  Returns out.
+    new ones; out: optional fp32 [B, T, Hq, D]; window: None (all positions)
+    or an int >= 1.  Returns out.
     """
     import torch
     _need(q, "q", torch.bfloat16)
@@ -296,9 +305,15 @@ def gqa_decode_attn_multi(q, k_cache, v_cache, seq_lens, scale, out=None, stream
     if out is None:
         out = torch.empty((B, T, Hq, D), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32, (B, T, Hq, D))
-    _check(lib().gqa_decode_attn_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
-                                       _ptr(out), B, T, Hq, Hkv, D, Lmax, float(scale),
-                                       _stream_ptr(stream)))
+    if window is None:
+        _check(lib().gqa_decode_attn_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(seq_lens), _ptr(out), B, T, Hq, Hkv, D, Lmax,
+                                           float(scale), _stream_ptr(stream)))
+    else:
+        _check(lib().gqa_decode_attn_multi_window(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                  _ptr(seq_lens), _ptr(out), B, T, Hq, Hkv, D,
+                                                  Lmax, float(scale), int(window),
+                                                  _stream_ptr(stream)))
     return out
 
 
@@ -344,13 +359,14 @@ def kv_append_paged(k_pool, v_pool, k_new, v_new, block_table, seq_lens, stream=
 
 
 def gqa_decode_attn_paged(q, k_pool, v_pool, block_table, seq_lens, scale, out=None,
-                          stream=None):
+                          stream=None, window=None):
     """gqa_decode_attn (q [B, Hq, D]) or gqa_decode_attn_multi (q [B, T, Hq, D])
     over a paged cache: position j of sequence b is row j % block_size of
     block block_table[b, j // block_size] of the pools.
 
     k_pool, v_pool: bf16 [num_blocks, Hkv, block_size, D]; block_table: int32
-    [B, max_blocks]; seq_lens: int32 [B]; out: optional fp32 shaped like q.
+    [B, max_blocks]; seq_lens: int32 [B]; out: optional fp32 shaped like q;
+    window: None (all positions) or an int >= 1, each query's local window.
     Returns out.
     """
     import torch
@@ -367,16 +383,25 @@ def gqa_decode_attn_paged(q, k_pool, v_pool, block_table, seq_lens, scale, out=N
     if out is None:
         out = torch.empty(tuple(q.shape), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32, tuple(q.shape))
-    _check(lib().gqa_decode_attn_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
-                                       _ptr(seq_lens), _ptr(out), B, T, Hq, Hkv, D, nblk, bs,
-                                       maxb, float(scale), _stream_ptr(stream)))
+    if window is None:
+        _check(lib().gqa_decode_attn_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                           _ptr(block_table), _ptr(seq_lens), _ptr(out), B, T,
+                                           Hq, Hkv, D, nblk, bs, maxb, float(scale),
+                                           _stream_ptr(stream)))
+    else:
+        _check(lib().gqa_decode_attn_paged_window(_ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                                  _ptr(block_table), _ptr(seq_lens), _ptr(out),
+                                                  B, T, Hq, Hkv, D, nblk, bs, maxb,
+                                                  float(scale), int(window),
+                                                  _stream_ptr(stream)))
     return out
 
 
 def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, scale,
-                          out=None, stream=None):
+                          out=None, stream=None, window=None):
     """gqa_decode_step over a paged cache: the new token's rows go to position
-    seq_lens[b] through the block table, then attention over [0, seq_lens[b] + 1).
+    seq_lens[b] through the block table, then attention over [0, seq_lens[b] + 1)
+    (only its last `window` positions for a local attention layer).
 
     q: bf16 [B, Hq, D]; k_new, v_new: bf16 [B, Hkv, D]; pools and table as
     for gqa_decode_attn_paged; seq_lens: tokens cached before this step.
@@ -396,10 +421,17 @@ def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32, (B, Hq, D))
-    _check(lib().gqa_decode_step_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
-                                       _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
-                                       _ptr(out), B, Hq, Hkv, D, nblk, bs, maxb, float(scale),
-                                       _stream_ptr(stream)))
+    if window is None:
+        _check(lib().gqa_decode_step_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                                           _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+                                           _ptr(out), B, Hq, Hkv, D, nblk, bs, maxb,
+                                           float(scale), _stream_ptr(stream)))
+    else:
+        _check(lib().gqa_decode_step_paged_window(_ptr(q), _ptr(k_new), _ptr(v_new),
+                                                  _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                                  _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D,
+                                                  nblk, bs, maxb, float(scale), int(window),
+                                                  _stream_ptr(stream)))
     return out
 
 

@@ -480,6 +480,9 @@ int kv_append_paged(void *k_pool, void *v_pool, const void *k_new, const void *v
 
 namespace {
 
+// A window no sequence reaches: the full attention.
+constexpr int kFullWindow = 0x7fffffff;
+
 // Shared body of gqa_decode_attn and gqa_decode_step (k_new != nullptr:
 // append this step's rows first; seq_lens then count tokens cached before).
 int run_decode(const void *q, const void *k_cache, const void *v_cache, const void *k_new,
@@ -503,7 +506,6 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     int rc, lg = 0;
     if (pg) {
         if ((rc = check_paged(*pg, Hkv, who, &lg, &Lmax))) return rc;
-        window = Lmax;
         if (D != 128 && D != 256)
             return fail(KVATTN_ERR_UNSUPPORTED, "%s: a paged cache needs D in {128, 256} (D=%d)", who, D);
     }
@@ -562,7 +564,13 @@ int run_decode(const void *q, const void *k_cache, const void *v_cache, const vo
     p.head_groups = P.head_groups;
     p.tile = P.tile_positions;
     p.cost_piece = pl.cost_piece;
-    p.window = window < Lmax ? window : Lmax;
+    // each query's window, and the positions the T queries' windows span
+    // together (token t's ends T - 1 - t positions before the last)
+    p.qwin = window < Lmax ? window : Lmax;
+    p.window = (long long)p.qwin + T - 1 < Lmax ? p.qwin + T - 1 : Lmax;
+    // a paged cache's tiles start on block boundaries: a local window's
+    // first tile starts at the tile boundary before it
+    p.walign = (pg && p.qwin < Lmax) ? P.tile_positions - 1 : 0;
     p.T = T;
     // bytes of one piece's q box: (64 columns x rows) per 64-column slab
     p.q_bytes = (D / 64) * (T == 1 ? pl.np : pl.hpg * T) * 128;
@@ -673,6 +681,8 @@ int run_decode_fp8(const void *q, const void *k_codes, const void *v_codes, cons
     // weighs twice as many tiles
     p.cost_piece = 2 * pl.cost_piece;
     p.window = Lmax;
+    p.qwin = Lmax;
+    p.walign = 0;
     p.T = 1;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.k_scale = k_scale;
@@ -743,7 +753,7 @@ int gqa_decode_attn_paged(const void *q, const void *k_pool, const void *v_pool,
                           int max_blocks, float scale, kvattn_stream_t stream) {
     const Paged pg{block_table, block_size, max_blocks, num_blocks};
     return run_decode(q, k_pool, v_pool, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, 0, scale,
-                      1, stream, "gqa_decode_attn_paged", T, &pg);
+                      kFullWindow, stream, "gqa_decode_attn_paged", T, &pg);
 }
 
 int gqa_decode_step_paged(const void *q, const void *k_new, const void *v_new, void *k_pool,
@@ -755,8 +765,40 @@ int gqa_decode_step_paged(const void *q, const void *k_new, const void *v_new, v
         return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_step_paged: null pointer");
     }
     const Paged pg{block_table, block_size, max_blocks, num_blocks};
-    return run_decode(q, k_pool, v_pool, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, 0, scale, 1,
-                      stream, "gqa_decode_step_paged", 1, &pg);
+    return run_decode(q, k_pool, v_pool, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, 0, scale,
+                      kFullWindow, stream, "gqa_decode_step_paged", 1, &pg);
+}
+
+int gqa_decode_attn_multi_window(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *seq_lens, float *out, int B, int T, int Hq,
+                                 int Hkv, int D, int Lmax, float scale, int window,
+                                 kvattn_stream_t stream) {
+    return run_decode(q, k_cache, v_cache, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, Lmax,
+                      scale, window, stream, "gqa_decode_attn_multi_window", T);
+}
+
+int gqa_decode_attn_paged_window(const void *q, const void *k_pool, const void *v_pool,
+                                 const int32_t *block_table, const int32_t *seq_lens, float *out,
+                                 int B, int T, int Hq, int Hkv, int D, int num_blocks,
+                                 int block_size, int max_blocks, float scale, int window,
+                                 kvattn_stream_t stream) {
+    const Paged pg{block_table, block_size, max_blocks, num_blocks};
+    return run_decode(q, k_pool, v_pool, nullptr, nullptr, seq_lens, out, B, Hq, Hkv, D, 0, scale,
+                      window, stream, "gqa_decode_attn_paged_window", T, &pg);
+}
+
+int gqa_decode_step_paged_window(const void *q, const void *k_new, const void *v_new,
+                                 void *k_pool, void *v_pool, const int32_t *block_table,
+                                 const int32_t *seq_lens, float *out, int B, int Hq, int Hkv,
+                                 int D, int num_blocks, int block_size, int max_blocks,
+                                 float scale, int window, kvattn_stream_t stream) {
+    if (!k_new || !v_new) {
+        t_last_error[0] = 0;
+        return fail(KVATTN_ERR_INVALID_ARG, "gqa_decode_step_paged_window: null pointer");
+    }
+    const Paged pg{block_table, block_size, max_blocks, num_blocks};
+    return run_decode(q, k_pool, v_pool, k_new, v_new, seq_lens, out, B, Hq, Hkv, D, 0, scale,
+                      window, stream, "gqa_decode_step_paged_window", 1, &pg);
 }
 
 int gqa_decode_attn_fp8(const void *q, const void *k_codes, const void *v_codes,

@@ -41,7 +41,7 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ inline void segment_pieces(const DecodeParams &p, int s, int grid, int *c0, int *n,
                                       int *first_slot) {
     const int lane = threadIdx.x & 31;
-    const LenView lens{p.seq_lens, p.len_add, p.window};
+    const LenView lens{p.seq_lens, p.len_add, p.window, p.walign};
     const int segs_per_b = p.Hkv * p.head_groups;
     const SchedCost w{p.cost_piece};
     long long total, cost;
@@ -49,10 +49,10 @@ __device__ inline void segment_pieces(const DecodeParams &p, int s, int grid, in
     sched_totals(lens, p.B, p.Lmax, p.tile, segs_per_b, w, grid, &total, &cost, &ctas_eff);
     const int b = s / segs_per_b, sg = s % segs_per_b;
     int before = 0;  // tiles of one segment of every sequence before b
-    for (int bb = lane; bb < b; bb += 32) before += seq_ntiles(lens[bb], p.Lmax, p.tile, lens.window);
+    for (int bb = lane; bb < b; bb += 32) before += seq_ntiles(lens[bb], p.Lmax, p.tile, lens.window, lens.walign);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
-    const int nt = seq_ntiles(lens[b], p.Lmax, p.tile, lens.window);
+    const int nt = seq_ntiles(lens[b], p.Lmax, p.tile, lens.window, lens.walign);
     const long long cost0 = (long long)segs_per_b * ((long long)before * kCostTile + (long long)w.P * b) +
                             (long long)sg * ((long long)nt * kCostTile + w.P);
     const long long last = cost0 + (nt == 1 ? 0 : w.P + (long long)kCostTile * (nt - 1));
@@ -60,7 +60,7 @@ __device__ inline void segment_pieces(const DecodeParams &p, int s, int grid, in
     bool starts = true;  // c's range starts at this segment's first tile
     if (s > 0) {
         // the tile before: the last of the previous segment
-        const int ntp = sg > 0 ? nt : seq_ntiles(lens[b - 1], p.Lmax, p.tile, lens.window);
+        const int ntp = sg > 0 ? nt : seq_ntiles(lens[b - 1], p.Lmax, p.tile, lens.window, lens.walign);
         const long long prev = cost0 - kCostTile - (ntp == 1 ? w.P : 0);
         starts = prev < sched_bound(cost, ctas_eff, c);
     }

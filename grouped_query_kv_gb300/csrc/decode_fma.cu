@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmv);
     }
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
-    const LenView lens{p.seq_lens, p.len_add, p.window};
+    const LenView lens{p.seq_lens, p.len_add, p.window, 0};  // contiguous: no window alignment
     const SchedCost wcost{p.cost_piece};
     const SchedStart st = warp_locate(lens, p.B, p.Lmax, T, segs_per_b, wcost, blockIdx.x, gridDim.x);
     if (warp == 0) sched_split_record(lens, p.B, p.Lmax, T, segs_per_b, wcost, blockIdx.x, st, p.split);

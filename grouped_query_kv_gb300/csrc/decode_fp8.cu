@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_wait_prior();
-    const LenView lens{p.seq_lens, p.len_add, p.window};
+    const LenView lens{p.seq_lens, p.len_add, p.window, 0};  // contiguous: no window alignment
     const SchedCost wcost{p.cost_piece};
     const SchedStart st = warp_locate(lens, p.B, p.Lmax, kT, segs_per_b, wcost, blockIdx.x, gridDim.x);
     if (warp == 2) sched_split_record(lens, p.B, p.Lmax, kT, segs_per_b, wcost, blockIdx.x, st, p.split);

@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait_prior();  // the caches, q and lengths may come from the previous kernel
     // each warp locates the CTA's tile range by itself: no block barrier
     // stands between reading the lengths and the first TMA load
-    const LenView lens{p.seq_lens, p.len_add, p.window};
+    const LenView lens{p.seq_lens, p.len_add, p.window, PG ? p.walign : 0};  // (only a paged cache aligns)
     const SchedCost wcost{p.cost_piece};
     const SchedStart st = warp_locate(lens, p.B, p.Lmax, kT, segs_per_b, wcost, blockIdx.x, gridDim.x);
     // (a softmax warp writes the record: the producer goes straight to its loads)
@@ -682,6 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 valid = row >= it.first_pos() - r0 && r0 + row < len;
             }
+            // paged, one token: the first tile starts at the tile boundary
+            // before the local window
+            if (PG && !MT) valid = valid && pos >= len - p.qwin;
             bool over = false;
 #pragma unroll
             for (int g = 0; g < NP; g += 4) {
@@ -693,13 +696,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 over |= (s[g] > m4.x + kTau) | (s[g + 1] > m4.y + kTau) |
                         (s[g + 2] > m4.z + kTau) | (s[g + 3] > m4.w + kTau);
             }
-            if (MT && r0 + kT - 1 >= len - (p.T - 1)) {
-                // the tile holds new tokens: token t sees positions < len - (T-1-t)
+            if (MT && (r0 + kT - 1 >= len - (p.T - 1) || r0 < len - p.qwin)) {
+                // the tile holds new tokens, or rows before the last token's
+                // window: token t sees positions [e - qwin, e), e = len - (T-1-t)
                 // (a column masked here after voting at most costs an exact max)
                 int t = 0, gg = 0;
 #pragma unroll
                 for (int g = 0; g < NP; ++g) {
-                    if (pos >= len - (p.T - 1 - t)) s[g] = -INFINITY;
+                    const int e = len - (p.T - 1 - t);
+                    if (pos >= e || pos < e - p.qwin) s[g] = -INFINITY;
                     if (++gg == p.hpg) {
                         gg = 0;
                         ++t;

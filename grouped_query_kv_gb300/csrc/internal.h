@@ -43,7 +43,8 @@ struct DecodeParams {
     int head_groups;          // passes per (b, kvh): ceil(G / hpg)
     int hpg;                  // query heads per pass (T = 1: heads_per_seg)
     int tile;                 // positions per tile
-    int window;               // positions attended at most (>= Lmax: all)
+    int window;               // positions the tiles of a sequence span at most (>= Lmax: all):
+                              // the union of its T queries' windows, qwin + T - 1
     int T;                    // new tokens (queries) per sequence, >= 1; q and out are
                               // [B, T, Hq, D] and token t attends [0, len - T + 1 + t)
     int q_bytes;              // tensor-core path: bytes of one piece's q load
@@ -66,6 +67,9 @@ struct DecodeParams {
     // threads' waits and the MMA thread's idle polling); 0 = the default.
     // Waits for copies and MMAs already issued always keep the default.
     unsigned int wait_limit;
+    int qwin;                 // positions one query attends at most (>= Lmax: all)
+    int walign;               // 0, or tile - 1 (paged cache): window spans start on a tile
+                              // boundary and the rows before a query's window are masked
 };
 
 // Host launchers (return cudaError_t of the launch).

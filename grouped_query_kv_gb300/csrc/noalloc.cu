@@ -129,6 +129,8 @@ extern "C" int gqa_decode_attn_noalloc(const void *q, const void *k_cache,
     p.tile = tile;
     p.cost_piece = 16;  // the regular entry point's schedule weight for this path
     p.window = Lmax;    // full attention
+    p.qwin = Lmax;
+    p.walign = 0;
     p.T = 1;
     p.q_bytes = 0;      // (the CUDA-core kernel reads q itself)
     p.block_table = nullptr;  // contiguous cache

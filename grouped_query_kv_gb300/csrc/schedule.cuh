@@ -26,11 +26,15 @@ namespace kvattn {
 // attention covers one more position; a negative entry stays invalid.  A
 // local (sliding-window) layer attends only the last `window` positions
 // ("The Basics of Transformer Inference", item on mixing in local attention
-// layers); window >= Lmax is the full attention.
+// layers); window >= Lmax is the full attention.  A paged cache's tiles
+// must start on block boundaries, so there the window's first tile starts
+// at the tile boundary at or before the window (walign = tile - 1; the
+// rows before the window are masked); elsewhere it starts at the window.
 struct LenView {
     const int32_t *p;
     int add;     // 0: attention lengths as given; 1: cached-before counts (+1)
     int window;  // positions attended at most, >= 1
+    int walign;  // 0, or tile - 1: window starts rounded down to a tile boundary
     __device__ __forceinline__ int operator[](int b) const {
         const int r = p[b];
         return add ? (r < 0 ? -1 : r + 1) : r;
@@ -40,19 +44,23 @@ struct LenView {
 // A sequence whose length is outside [1, Lmax] still owns one tile, with no
 // valid positions (zero output row; out-of-range lengths also raise the
 // device error word).  Otherwise its tiles cover the min(len, window)
-// attended positions.
-__device__ __forceinline__ int seq_ntiles(int len, int Lmax, int tile, int window) {
+// attended positions, and with walign = tile - 1 the positions from the
+// tile boundary before the window's start.
+__device__ __forceinline__ int seq_ntiles(int len, int Lmax, int tile, int window, int walign) {
+    // (len - window) & walign: the rows between that boundary and the window
+    // (a span of at least len when len <= window, so the min stays len)
+    const int span = window + ((len - window) & walign);
     // tiles are a power of two positions (64 or 128): a shift, not a division
-    return (len <= 0 || len > Lmax) ? 1 : ((len < window ? len : window) + tile - 1) >> (__ffs(tile) - 1);
+    return (len <= 0 || len > Lmax) ? 1 : ((len < span ? len : span) + tile - 1) >> (__ffs(tile) - 1);
 }
 
 __device__ __forceinline__ int seq_valid_len(int len, int Lmax) {
     return (len < 0 || len > Lmax) ? 0 : len;
 }
 
-// First attended position of a sequence of (valid) length len.
-__device__ __forceinline__ int seq_window_start(int len, int window) {
-    return len > window ? len - window : 0;
+// First position the tiles of a sequence of (valid) length len cover.
+__device__ __forceinline__ int seq_window_start(int len, int window, int walign) {
+    return len > window ? (len - window) & ~walign : 0;
 }
 
 // The cost model's weights: W = kCostTile per tile (a power of two, so the
@@ -149,7 +157,7 @@ __device__ inline void sched_find(LenView lens, int B, int Lmax, int tile, int s
     int tcarry = 0;  // tiles of one segment of every sequence so far
     for (int base = 0; base < B && !(got0 && got1); base += 32) {
         const int b = base + lane;
-        const int nt = (b < B) ? seq_ntiles(lens[b], Lmax, tile, lens.window) : 0;
+        const int nt = (b < B) ? seq_ntiles(lens[b], Lmax, tile, lens.window, lens.walign) : 0;
         const int incl = warp_incl_scan(nt);
         const int before = tcarry + incl - nt;
         const int segc = nt * kCostTile + w.P;  // one segment of sequence b
@@ -183,7 +191,7 @@ __device__ inline void sched_totals(LenView lens, int B, int Lmax, int tile, int
                                     int *ctas_eff) {
     const int lane = threadIdx.x & 31;
     int nt_lane = 0;
-    for (int b = lane; b < B; b += 32) nt_lane += seq_ntiles(lens[b], Lmax, tile, lens.window);
+    for (int b = lane; b < B; b += 32) nt_lane += seq_ntiles(lens[b], Lmax, tile, lens.window, lens.walign);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nt_lane += __shfl_xor_sync(0xffffffffu, nt_lane, o);
     const long long nt_sum = nt_lane;  // tiles of one segment of every sequence
@@ -254,7 +262,7 @@ __device__ inline void sched_split_record(LenView lens, int B, int Lmax, int til
         if (st.cost0 >= Tp) {
             SchedHit hp, unused;
             sched_find<1>(lens, B, Lmax, tile, segs_per_b, w, Tp, Tp, st.total, &hp, &unused);
-            const int nt = seq_ntiles(lens[st.b], Lmax, tile, lens.window);
+            const int nt = seq_ntiles(lens[st.b], Lmax, tile, lens.window, lens.walign);
             const long long last_cost = st.cost0 + (nt == 1 ? 0 : w.P + (long long)kCostTile * (nt - 1));
             const int c_last = sched_owner(last_cost, st.cost, st.ctas_eff);
             r0 = st.b;
@@ -300,13 +308,13 @@ struct TileIter {
         lens = lens_; B = B_; Lmax = Lmax_; tile = tile_; segs_per_b = segs_per_b_;
         b = s.b; seg = s.seg; t = s.t;
         len = lens[b];
-        nt = seq_ntiles(len, Lmax, tile, lens.window);
+        nt = seq_ntiles(len, Lmax, tile, lens.window, lens.walign);
     }
     __device__ __forceinline__ bool last_tile_of_segment() const { return t == nt - 1; }
     // First attended position of the current sequence, and the first
     // position that tile t adds.
     __device__ __forceinline__ int start() const {
-        return seq_window_start(seq_valid_len(len, Lmax), lens.window);
+        return seq_window_start(seq_valid_len(len, Lmax), lens.window, lens.walign);
     }
     __device__ __forceinline__ int first_pos() const { return start() + t * tile; }
     // First cache row of the tile's box.  A segment's last tile is moved back
@@ -323,7 +331,7 @@ struct TileIter {
         seg = 0;
         if (++b < B) {
             len = lens[b];
-            nt = seq_ntiles(len, Lmax, tile, lens.window);
+            nt = seq_ntiles(len, Lmax, tile, lens.window, lens.walign);
         }
     }
 };

@@ -219,6 +219,22 @@ KVATTN_API int gqa_decode_step_window(const void *q, const void *k_new, const vo
                                       float scale, int window, kvattn_stream_t stream);
 
 /*
+ * gqa_decode_attn_multi_window -- gqa_decode_attn_multi on a local layer:
+ * each of the T new tokens keeps its own window, so token t (at position
+ * e_t - 1, e_t = seq_lens[b] - T + 1 + t) attends positions
+ * [max(0, e_t - window), e_t), and gets a zero row when e_t <= 0.  The
+ * tiles cover the union of the T windows, window + T - 1 positions, read
+ * once for all tokens.  Arguments as for gqa_decode_attn_multi, plus window
+ * as for gqa_decode_attn_window (>= 1; >= Lmax is gqa_decode_attn_multi).
+ * Rows in [0, seq_lens[b]) must hold finite values.
+ */
+KVATTN_API int gqa_decode_attn_multi_window(const void *q, const void *k_cache,
+                                            const void *v_cache, const int32_t *seq_lens,
+                                            float *out, int B, int T, int Hq, int Hkv, int D,
+                                            int Lmax, float scale, int window,
+                                            kvattn_stream_t stream);
+
+/*
  * Paged KV cache.  Instead of one contiguous [Lmax] run of rows per sequence,
  * the cache is a pool of fixed-size blocks and each sequence keeps a block
  * table mapping its logical positions to physical blocks; sequences that
@@ -243,8 +259,9 @@ KVATTN_API int gqa_decode_step_window(const void *q, const void *k_new, const vo
  * sequence's output is then meaningless but no memory outside the pool is
  * touched.  Results are those of the contiguous calls on the cache the
  * table describes.  The attention calls need D in {128, 256} (the
- * tensor-core kernel; KVATTN_ERR_UNSUPPORTED otherwise) and attend every
- * position (no local window).
+ * tensor-core kernel; KVATTN_ERR_UNSUPPORTED otherwise);
+ * gqa_decode_attn_paged and gqa_decode_step_paged attend every position,
+ * their _window forms a local window.
  */
 
 /*
@@ -290,6 +307,36 @@ KVATTN_API int gqa_decode_step_paged(const void *q, const void *k_new, const voi
                                      const int32_t *seq_lens, float *out, int B, int Hq,
                                      int Hkv, int D, int num_blocks, int block_size,
                                      int max_blocks, float scale, kvattn_stream_t stream);
+
+/*
+ * gqa_decode_attn_paged_window, gqa_decode_step_paged_window -- the two
+ * paged calls on a local layer ("The Basics of Transformer Inference", the
+ * items on local attention layers and on ragged reads with Paged
+ * Attention): the queries attend what gqa_decode_attn_multi_window (T new
+ * tokens) and gqa_decode_step_window (one new token, appended first) attend,
+ * through the block table.  Arguments as for gqa_decode_attn_paged and
+ * gqa_decode_step_paged, plus
+ *   window : positions one query attends at most, >= 1
+ *            (KVATTN_ERR_INVALID_ARG otherwise); >= max_blocks * block_size
+ *            is the full attention.
+ * A tile of a paged cache starts on a block boundary, so the first tile
+ * read starts at the 128-position boundary at or before the window and its
+ * rows before the window are masked: up to 127 positions before each
+ * window are read (not attended), and their table entries must be valid
+ * and their rows finite.
+ */
+KVATTN_API int gqa_decode_attn_paged_window(const void *q, const void *k_pool,
+                                            const void *v_pool, const int32_t *block_table,
+                                            const int32_t *seq_lens, float *out, int B, int T,
+                                            int Hq, int Hkv, int D, int num_blocks,
+                                            int block_size, int max_blocks, float scale,
+                                            int window, kvattn_stream_t stream);
+KVATTN_API int gqa_decode_step_paged_window(const void *q, const void *k_new, const void *v_new,
+                                            void *k_pool, void *v_pool,
+                                            const int32_t *block_table, const int32_t *seq_lens,
+                                            float *out, int B, int Hq, int Hkv, int D,
+                                            int num_blocks, int block_size, int max_blocks,
+                                            float scale, int window, kvattn_stream_t stream);
 
 /*
  * 8-bit KV cache (FP8 E4M3 codes with one fp32 scale per cached row).

@@ -65,6 +65,10 @@ def _bind(path):
     lib.oracle_gqa_decode_multi.argtypes = [u16p, u16p, u16p, i32p, f64p,
                                             i64, i64, i64, i64, i64, i64,
                                             ctypes.c_double, ctypes.c_int]
+    lib.oracle_gqa_decode_multi_window.restype = ctypes.c_int
+    lib.oracle_gqa_decode_multi_window.argtypes = [u16p, u16p, u16p, i32p, f64p,
+                                                   i64, i64, i64, i64, i64, i64,
+                                                   ctypes.c_double, i64, ctypes.c_int]
     u8p = ctypes.POINTER(ctypes.c_uint8)
     f32p = ctypes.POINTER(ctypes.c_float)
     lib.oracle_e4m3_encode_n.restype = None
@@ -202,13 +206,16 @@ class Oracle:
         return out
 
 
-    def gqa_decode_multi(self, q, k_cache, v_cache, seq_lens, scale, nthreads=1):
+    def gqa_decode_multi(self, q, k_cache, v_cache, seq_lens, scale, nthreads=1,
+                         window=None):
         """T new tokens per sequence, causal among themselves.
 
         q:        uint16 [B, T, Hq, D] (bf16 bits); token t of sequence b sits
                   at position seq_lens[b] - T + t and attends positions
-                  [0, seq_lens[b] - T + 1 + t) (a zero row when that is empty)
+                  [0, e) with e = seq_lens[b] - T + 1 + t (a zero row when
+                  that is empty)
         k_cache:  uint16 [B, Hkv, Lmax, D];  v_cache the same shape
+        window:   optional W >= 1: token t attends only [max(0, e - W), e)
         Returns float64 [B, T, Hq, D].
         """
         qa, q_p = _u16(q)
@@ -220,9 +227,14 @@ class Oracle:
         if Bk != B or Dk != D or va.shape != ka.shape or sl.shape != (B,):
             raise ValueError("shape mismatch")
         out = np.zeros((B, T, Hq, D), dtype=np.float64)
-        rc = self.lib.oracle_gqa_decode_multi(
-            q_p, k_p, v_p, sl_p, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
-            B, T, Hq, Hkv, D, Lmax, float(scale), int(nthreads))
+        out_p = out.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+        if window is None:
+            rc = self.lib.oracle_gqa_decode_multi(q_p, k_p, v_p, sl_p, out_p, B, T, Hq, Hkv,
+                                                  D, Lmax, float(scale), int(nthreads))
+        else:
+            rc = self.lib.oracle_gqa_decode_multi_window(q_p, k_p, v_p, sl_p, out_p, B, T,
+                                                         Hq, Hkv, D, Lmax, float(scale),
+                                                         int(window), int(nthreads))
         if rc != 0:
             raise ValueError("oracle_gqa_decode_multi: bad arguments (rc=%d)" % rc)
         return out
@@ -257,13 +269,17 @@ class Oracle:
         return out
 
     def gqa_decode_paged(self, q, k_pool, v_pool, block_table, seq_lens, block_size, scale,
-                         nthreads=1):
+                         nthreads=1, window=None):
         """Decode attention over a paged cache: the same softmax(scale q K^T) V
-        over the positions the block table maps, i.e. gqa_decode on the
-        gathered contiguous cache."""
+        over the positions the block table maps, i.e. gqa_decode (q [B, Hq,
+        D]) or gqa_decode_multi (q [B, T, Hq, D]) on the gathered contiguous
+        cache, with the same optional local window."""
         k = self.gather_paged(k_pool, block_table, seq_lens, block_size)
         v = self.gather_paged(v_pool, block_table, seq_lens, block_size)
-        return self.gqa_decode(q, k, v, seq_lens, scale, nthreads=nthreads)
+        if np.asarray(q).ndim == 4:
+            return self.gqa_decode_multi(q, k, v, seq_lens, scale, nthreads=nthreads,
+                                         window=window)
+        return self.gqa_decode(q, k, v, seq_lens, scale, nthreads=nthreads, window=window)
 
 
     # ------------------------------------------------------------ 8-bit cache

@@ -58,7 +58,11 @@
  *   positions 0 .. len_b - T + t, i.e. the cached prefix and the new tokens
  *   up to itself (causal among the new tokens; a reading, the pages give no
  *   formula).  A token with nothing to attend (len_b - T + t < 0) gets a zero
- *   row.  q and out are [B, T, Hq, D].
+ *   row.  q and out are [B, T, Hq, D].  On a local layer each new token
+ *   keeps its own window: token t attends the last W positions up to and
+ *   including itself, j = max(0, e_t - W) .. e_t - 1 with
+ *   e_t = len_b - T + 1 + t (the single-token rule above applied at each
+ *   token's own position; a reading, the pages give no formula).
  *
  *   8-bit KV cache: "The Basics of Transformer Inference", the item
  *   "Quantization" (quantizing the KV cache, e.g. to int8, int4 or fp8,
@@ -405,6 +409,18 @@ int oracle_gqa_decode_window(const uint16_t *q, const uint16_t *k_cache,
 {
     return oracle_run(q, k_cache, v_cache, &no_q8, seq_lens, out, B, 1, Hq, Hkv, D, Lmax,
                       scale, window, NULL, B * Hq, nthreads);
+}
+
+/* T new tokens on a local layer: token t attends the last `window`
+ * positions up to itself (window >= 1).  q and out are [B, T, Hq, D]. */
+int oracle_gqa_decode_multi_window(const uint16_t *q, const uint16_t *k_cache,
+                                   const uint16_t *v_cache, const int32_t *seq_lens,
+                                   double *out, int64_t B, int64_t T, int64_t Hq, int64_t Hkv,
+                                   int64_t D, int64_t Lmax, double scale, int64_t window,
+                                   int nthreads)
+{
+    return oracle_run(q, k_cache, v_cache, &no_q8, seq_lens, out, B, T, Hq, Hkv, D, Lmax,
+                      scale, window, NULL, B * T * Hq, nthreads);
 }
 
 /* Only the listed (b, h) rows: pairs is [npairs, 2] int64; out is still the

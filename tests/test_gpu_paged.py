@@ -41,16 +41,18 @@ def _case(B, Hq, Hkv, D, Lmax, bs, lens, seed, T=1, spare=5):
     return w, x, pg
 
 
-def _oracle_paged(w, x, pg, lens=None):
+def _oracle_paged(w, x, pg, lens=None, window=None):
     lens = x["attn_lens"].cpu().numpy() if lens is None else np.asarray(lens)
     table = pg["block_table"].cpu().numpy()
     k = oracle.gather_paged(bits(pg["k_pool"]), table, lens, w.block_size)
     v = oracle.gather_paged(bits(pg["v_pool"]), table, lens, w.block_size)
     q = bits(x["q"])
     if w.T > 1:
-        ref = oracle.gqa_decode_multi(q, k, v, lens, w.scale, nthreads=oracle_threads())
+        ref = oracle.gqa_decode_multi(q, k, v, lens, w.scale, nthreads=oracle_threads(),
+                                      window=window)
     else:
-        ref = oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=oracle_threads())
+        ref = oracle.gqa_decode(q, k, v, lens, w.scale, nthreads=oracle_threads(),
+                                window=window)
     return ref, v, lens
 
 
@@ -238,3 +240,105 @@ def test_llama70b_paged_workload_sampled():
     v = oracle.gather_paged(bits(pg["v_pool"]), table, lens, w.block_size)
     ref = oracle.gqa_decode(bits(x["q"])[sel], k, v, lens, w.scale, nthreads=oracle_threads())
     assert_close(out[sel], ref, v, list(lens))
+
+
+# ------------------------------------------------ local window over a paged cache
+# "The Basics of Transformer Inference", the items on local attention layers
+# and on ragged reads with Paged Attention: a local layer's queries attend
+# their last `window` positions through the block table.
+
+def _table_without_early_blocks(pg, lens, bs, span):
+    """The block table with every block that lies wholly more than 127
+    positions before a sequence's window span set to -1: the kernel may read
+    at most 127 positions before the span, so reading one of these blocks
+    would raise the device bounds error."""
+    tab = pg["block_table"].cpu().numpy().copy()
+    for b, n in enumerate(lens):
+        lo = int(n) - span - 127
+        for kb in range(tab.shape[1]):
+            if (kb + 1) * bs - 1 < lo:
+                tab[b, kb] = -1
+    return torch.from_numpy(tab).to(pg["block_table"].device).contiguous()
+
+
+def _attend_window(w, x, pg, window):
+    lens = x["attn_lens"].cpu().numpy()
+    table = _table_without_early_blocks(pg, lens, w.block_size, window + w.T - 1)
+    out = g.gqa_decode_attn_paged(x["q"], pg["k_pool"], pg["v_pool"], table, x["attn_lens"],
+                                  w.scale, window=window)
+    g.check_device_error()
+    ref, v, ls = _oracle_paged(w, x, pg, window=window)
+    if w.T > 1:
+        B, T, Hq, D = out.shape
+        return assert_close(out.reshape(B * T, Hq, D), ref.reshape(B * T, Hq, D), v, list(ls))
+    return assert_close(out, ref, v, list(ls))
+
+
+@pytest.mark.parametrize("bs", [16, 64, 128, 512])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 64, 8), (256, 16, 1), (256, 48, 1)])
+@pytest.mark.parametrize("window", [1, 5, 127, 128, 129, 300, 5000])
+def test_paged_local_window_matches_oracle(bs, D, Hq, Hkv, window):
+    Lmax = 1100
+    lens = _edge_lens(bs, Lmax)
+    w, x, pg = _case(len(lens), Hq, Hkv, D, Lmax, bs, lens, seed=bs + D + Hq + window)
+    _attend_window(w, x, pg, window)
+
+
+@pytest.mark.parametrize("bs", [16, 128])
+@pytest.mark.parametrize("ctas", [1, 3, 17, 152, 600])
+def test_paged_local_window_split_pieces_merge(bs, ctas):
+    g.set_tuning(0, ctas)
+    try:
+        w, x, pg = _case(4, 32, 4, 128, 3000, bs, (3000, 1, 1709, 130), seed=ctas + bs + 1)
+        _attend_window(w, x, pg, 1500)
+    finally:
+        g.set_tuning(0, 0)
+
+
+@pytest.mark.parametrize("bs", [16, 256])
+@pytest.mark.parametrize("T,window", [(2, 1), (2, 200), (4, 5), (4, 129), (8, 64)])
+def test_paged_new_tokens_with_a_local_window(bs, T, window):
+    lens = sorted({T, T + 1, bs + 3, 129, 700, 1000})
+    w, x, pg = _case(len(lens), 8, 1, 128, 1000, bs, lens, seed=T * 37 + bs + window, T=T)
+    _attend_window(w, x, pg, window)
+
+
+@pytest.mark.parametrize("ctas", [1, 19, 152])
+def test_paged_new_tokens_window_over_head_passes(ctas):
+    # the PaLM-540B head shape (48 heads on one K/V head, D = 256), 3 drafted
+    # tokens: 3 passes of 16 heads, each with its tile-aligned window span
+    g.set_tuning(0, ctas)
+    try:
+        w, x, pg = _case(2, 48, 1, 256, 3000, 64, (3000, 1291), seed=ctas + 7, T=3)
+        _attend_window(w, x, pg, 700)
+    finally:
+        g.set_tuning(0, 0)
+
+
+@pytest.mark.parametrize("bs", [16, 128])
+@pytest.mark.parametrize("window", [1, 100, 2000])
+def test_paged_local_window_fused_step(bs, window):
+    lens = (1, 16, 17, 128, 129, 500, 1024)   # attended, after the append
+    w, x, pg = _case(len(lens), 32, 4, 128, 1024, bs, lens, seed=bs + window)
+    k_ref, v_ref = bits(pg["k_pool"]), bits(pg["v_pool"])
+    table = pg["block_table"].cpu().numpy()
+    pos = x["append_pos"].cpu().numpy()
+    for b in range(w.B):
+        j = int(pos[b])
+        k_ref[table[b, j // bs], :, j % bs] = bits(x["k_new"])[b]
+        v_ref[table[b, j // bs], :, j % bs] = bits(x["v_new"])[b]
+    early = _table_without_early_blocks(pg, x["attn_lens"].cpu().numpy(), bs, window)
+    out = g.gqa_decode_step_paged(x["q"], x["k_new"], x["v_new"], pg["k_pool"], pg["v_pool"],
+                                  early, x["append_pos"], w.scale, window=window)
+    g.check_device_error()
+    assert np.array_equal(bits(pg["k_pool"]), k_ref)
+    assert np.array_equal(bits(pg["v_pool"]), v_ref)
+    ref, v, ls = _oracle_paged(w, x, pg, window=window)
+    assert_close(out, ref, v, list(ls))
+
+
+def test_paged_local_window_must_be_positive():
+    w, x, pg = _case(2, 16, 2, 128, 256, 16, (100, 30), seed=12)
+    with pytest.raises(g.KvAttnError):
+        g.gqa_decode_attn_paged(x["q"], pg["k_pool"], pg["v_pool"], pg["block_table"],
+                                x["attn_lens"], w.scale, window=0)

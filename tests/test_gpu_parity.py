@@ -453,7 +453,7 @@ def test_local_window_must_be_positive():
 # tokens scored in one pass; token t attends the prefix and the new tokens up
 # to itself.
 
-def _multi_case(B, T, Hq, Hkv, D, Lmax, lens, seed, nan_pad=True):
+def _multi_case(B, T, Hq, Hkv, D, Lmax, lens, seed, nan_pad=True, window=None):
     dev = torch.device("cuda")
     gen = torch.Generator(device="cpu").manual_seed(seed)
     q = torch.randn((B, T, Hq, D), generator=gen).to(torch.bfloat16).to(dev)
@@ -465,11 +465,11 @@ def _multi_case(B, T, Hq, Hkv, D, Lmax, lens, seed, nan_pad=True):
             k[b, :, n:] = float("nan")
             v[b, :, n:] = float("inf")
     scale = 1.0 / np.sqrt(D)
-    out = g.gqa_decode_attn_multi(q, k, v, lens_t, scale)
+    out = g.gqa_decode_attn_multi(q, k, v, lens_t, scale, window=window)
     g.check_device_error()
     lens_np = np.array(lens, np.int32)
     ref = oracle.gqa_decode_multi(bits(q), bits(k), bits(v), lens_np, scale,
-                                  nthreads=oracle_threads())
+                                  nthreads=oracle_threads(), window=window)
     assert_close(out.reshape(B * T, Hq, D), ref.reshape(B * T, Hq, D), bits(v), lens_np)
 
 
@@ -516,6 +516,26 @@ def test_new_tokens_with_split_pieces(ctas):
     g.set_tuning(0, ctas)
     try:
         _multi_case(3, 4, 32, 4, 128, 3000, (3000, 130, 2047), seed=ctas)
+    finally:
+        g.set_tuning(0, 0)
+
+
+# Several drafted tokens on a local layer: token t attends the `window`
+# positions that end at its own.
+@pytest.mark.parametrize("D,Hq,Hkv,T", [(128, 64, 8, 2), (128, 16, 16, 8), (256, 16, 1, 3),
+                                        (256, 16, 1, 8), (256, 48, 1, 2), (128, 4, 4, 64)])
+@pytest.mark.parametrize("window", [1, 7, 127, 128, 129, 500, 5000])
+def test_new_tokens_with_a_local_window(D, Hq, Hkv, T, window):
+    lens = (700, T, 129, 256, 1000, 383, max(1, T - 1), 128)
+    _multi_case(len(lens), T, Hq, Hkv, D, 1000, lens, seed=T * 11 + D + Hq + window,
+                window=window)
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 152, 400])
+def test_new_tokens_with_a_local_window_and_split_pieces(ctas):
+    g.set_tuning(0, ctas)
+    try:
+        _multi_case(3, 4, 48, 1, 256, 3000, (3000, 130, 2047), seed=ctas + 5, window=1500)
     finally:
         g.set_tuning(0, 0)
 

@@ -103,6 +103,24 @@ def pins_pass(orc) -> bool:
                 scale=scale, enable_gqa=True)[0, :, 0].numpy()
             if not np.allclose(om[b, t], ref, rtol=1e-12, atol=1e-13):
                 return False
+    # T new tokens on a local layer: token t attends the W positions that
+    # end at its own (torch's attention on those rows)
+    for W in (3, 6):
+        try:
+            ow = orc.gqa_decode_multi(qm, k, v, lm, scale=scale, window=W)
+        except ValueError:
+            return False
+        for b in range(B):
+            for t in range(T):
+                n = int(lm[b]) - T + 1 + t
+                j0 = max(0, n - W)
+                ref = F.scaled_dot_product_attention(
+                    torch.from_numpy(_unbits(qm[b:b + 1, t]))[:, :, None, :],
+                    torch.from_numpy(_unbits(k[b:b + 1, :, j0:n])),
+                    torch.from_numpy(_unbits(v[b:b + 1, :, j0:n])),
+                    scale=scale, enable_gqa=True)[0, :, 0].numpy()
+                if not np.allclose(ow[b, t], ref, rtol=1e-12, atol=1e-13):
+                    return False
     return True
 
 
@@ -137,6 +155,9 @@ MUTANTS = {
                                   "const int64_t j0 = len > window ? len - window + 1 : 0;"),
     "window one position long": ("const int64_t j0 = len > window ? len - window : 0;",
                                  "const int64_t j0 = len > window ? len - window - 1 : 0;"),
+    "new tokens share the last token's window": (
+        "const int64_t j0 = len > window ? len - window : 0;",
+        "const int64_t j0 = len > window ? seq_lens[b] - window : 0;"),
     "window values not shifted": ("oracle_cache_at(v_cache, q8->v, q8->v_scale, row0, j0 + j, D, d)",
                                   "oracle_cache_at(v_cache, q8->v, q8->v_scale, row0, j, D, d)"),
 }

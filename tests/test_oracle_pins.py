@@ -457,6 +457,62 @@ def test_new_tokens_before_the_start_of_the_sequence_get_zero_rows():
     assert np.array_equal(out[0, 2], unbits(v[0, 0, 0])[None].repeat(2, 0))  # sees one row
 
 
+# Several new tokens on a local layer: each token keeps its own window, the
+# last W positions up to and including itself.
+
+def test_new_tokens_with_a_window_covering_the_sequence_are_the_full_pass():
+    rng = np.random.default_rng(74)
+    B, T, Hq, Hkv, D, L = 3, 4, 6, 3, 8, 32
+    q = bits(rng.standard_normal((B, T, Hq, D)))
+    _, k, v, _ = rand_case(rng, B, Hq, Hkv, D, L)
+    lens = np.array([32, 11, 2], np.int32)
+    full = oracle.gqa_decode_multi(q, k, v, lens, 0.3)
+    for W in (32, 33, 10 ** 6):
+        assert np.array_equal(oracle.gqa_decode_multi(q, k, v, lens, 0.3, window=W), full)
+
+
+def test_window_of_one_gives_each_new_token_its_own_value_row():
+    rng = np.random.default_rng(75)
+    B, T, Hq, Hkv, D, L = 2, 3, 4, 2, 8, 20
+    q = bits(rng.standard_normal((B, T, Hq, D)))
+    _, k, v, _ = rand_case(rng, B, Hq, Hkv, D, L)
+    lens = np.array([20, 5], np.int32)
+    out = oracle.gqa_decode_multi(q, k, v, lens, 0.5, window=1)
+    for b in range(B):
+        for t in range(T):
+            pos = int(lens[b]) - T + t
+            for h in range(Hq):
+                assert np.array_equal(out[b, t, h], unbits(v[b, h // 2, pos]))
+
+
+@pytest.mark.parametrize("W", [1, 3, 9, 17])
+def test_new_tokens_with_a_window_match_torch_sdpa_with_a_band_mask(W):
+    rng = np.random.default_rng(76 + W)
+    B, T, Hq, Hkv, D, L = 3, 5, 8, 2, 16, 40
+    q = bits(rng.standard_normal((B, T, Hq, D)))
+    _, k, v, _ = rand_case(rng, B, Hq, Hkv, D, L)
+    lens = np.array([40, 13, 4], np.int32)
+    out = oracle.gqa_decode_multi(q, k, v, lens, 0.2, window=W)
+    for b in range(B):
+        n = int(lens[b])
+        # token t (end e = n - T + 1 + t) sees positions [e - W, e)
+        mask = torch.zeros(1, 1, T, n, dtype=torch.bool)
+        for t in range(T):
+            e = n - T + 1 + t
+            if e > 0:
+                mask[..., t, max(0, e - W):e] = True
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(unbits(q[b:b + 1])).permute(0, 2, 1, 3),
+            torch.from_numpy(unbits(k[b:b + 1, :, :n])),
+            torch.from_numpy(unbits(v[b:b + 1, :, :n])),
+            attn_mask=mask, scale=0.2, enable_gqa=True)[0].permute(1, 0, 2).numpy()
+        for t in range(T):
+            if n - T + 1 + t > 0:   # SDPA gives NaN for an all-masked row
+                np.testing.assert_allclose(out[b, t], ref[t], rtol=1e-12, atol=1e-13)
+            else:
+                assert np.all(out[b, t] == 0.0)
+
+
 # --------------------------------------------------------------- paged KV cache
 # "Machine Learning Engineering and AI Systems at Scale", "The key and value
 # cache" (PagedAttention):
@@ -507,6 +563,19 @@ def test_sequences_sharing_prefix_blocks_match_private_copies():
     priv = np.concatenate([shared, own[:1], shared, own[1:]])
     table2 = np.array([[0, 1, 2, 3], [4, 5, 6, 7]], np.int32)
     assert np.array_equal(out, oracle.gqa_decode_paged(q, priv, priv, table2, lens, bs, 0.3))
+
+
+def test_paged_window_is_the_contiguous_window():
+    rng = np.random.default_rng(84)
+    q, k, v, lens = rand_case(rng, 3, 8, 2, 16, 64, lens=[64, 37, 3])
+    kp, table = _pool_from_contiguous(k, 16)
+    vp, _ = _pool_from_contiguous(v, 16)
+    for W in (1, 20, 64):
+        out = oracle.gqa_decode_paged(q, kp, vp, table, lens, 16, 0.25, window=W)
+        assert np.array_equal(out, oracle.gqa_decode(q, k, v, lens, 0.25, window=W))
+    qm = bits(rng.standard_normal((3, 4, 8, 16)))
+    out = oracle.gqa_decode_paged(qm, kp, vp, table, lens, 16, 0.25, window=6)
+    assert np.array_equal(out, oracle.gqa_decode_multi(qm, k, v, lens, 0.25, window=6))
 
 
 def test_paged_rejects_tables_outside_the_pool():
