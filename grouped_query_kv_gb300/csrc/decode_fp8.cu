@@ -38,9 +38,12 @@
 //     power of two 2^cv that the CTA keeps per piece (the largest v_scale
 //     met so far times 2^cv in [32, 64)) and with p <= 4 between rescales
 //     (the running max is refreshed once a score passes it by 2), w 2^cv
-//     stays <= 256, inside E4M3's range, and goes in as three E4M3 parts
-//     hi + mid + lo (each the rounded remainder of the previous), about 12
-//     significant bits -- the f16 P of a widening design carries 11.  The
+//     stays <= 256, inside E4M3's range.  It is rounded to binary16 (11
+//     significant bits, as the f16 P of a widening design) and goes in as
+//     three E4M3 parts hi + mid + lo (each the rounded remainder of the
+//     previous, taken in binary16, where the remainders are exact), which
+//     carry its 11 bits whole (4 + 4 + 3; a remainder below E4M3's
+//     smallest step, 2^-9, is lost as before).  The
 //     parts sit side by side as the 3 NP columns of the B operand (P stored
 //     position-major, no swizzle), so 4 MMAs per tile accumulate three
 //     partial O^T blocks; the epilogue adds them and divides by 2^cv.  A
@@ -86,6 +89,7 @@ struct Q8Cfg {
     static constexpr int NSK = NS / 2;                             // K staging slots
     static constexpr int NSV = NS - NSK;                           // V staging slots
     static_assert(NSV >= 2 && NSK >= 2, "staging rings must hold two tiles each");
+    static_assert(NP % (4 * kQWarps) == 0, "the q warps convert four heads at a time each");
 
     static constexpr int off_kst = 0;
     static constexpr int off_vst = off_kst + NSK * kStage;
@@ -128,6 +132,28 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
 __device__ __forceinline__ uint16_t e4m3x2_of(float a, float b) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// Two binary32 values -> f16x2 (a in the low half), nearest even.
+__device__ __forceinline__ uint32_t f16x2_of(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// f16x2 -> two E4M3 codes (nearest, ties to even, saturating), the low
+// half in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2_of_f16x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return r;
+}
+
+// a - b in f16x2 arithmetic (exact for the remainders it is used on).
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 
@@ -325,46 +351,75 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 const int h0 = kvh * p.G + hg * p.heads_per_seg;
                 const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
                 uint8_t *qb = qbuf + qs * C::QB;
-                for (int g = qw; g < NP; g += kQWarps) {
-                    // lane l holds columns 128 sl + 4l .. 128 sl + 4l + 3 of each slab sl
-                    float x[SL][4];
+                // eight lanes per head, each with VPL consecutive head dims;
+                // a warp converts four heads at a time and first loads every
+                // head it converts, so their reads overlap
+                constexpr int VPL = D / 8;              // head dims per lane
+                constexpr int NV = VPL / 8;             // 16-byte loads per lane and head
+                constexpr int HPW = NP / kQWarps;       // heads per warp
+                constexpr int NIT = HPW / 4;            // four heads per pass of the warp
+                const int sub = lane & 7, d0 = sub * VPL;
+                uint4 raw[NIT][NV];
+#pragma unroll
+                for (int it4 = 0; it4 < NIT; ++it4) {
+                    const int g = (it4 * kQWarps + qw) * 4 + (lane >> 3);
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) raw[it4][v] = make_uint4(0u, 0u, 0u, 0u);
+                    if (g < gvalid) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            p.q + ((size_t)itq.b * p.Hq + h0 + g) * D + d0);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) raw[it4][v] = __ldg(src + v);
+                    }
+                }
+#pragma unroll
+                for (int it4 = 0; it4 < NIT; ++it4) {
+                    const int g = (it4 * kQWarps + qw) * 4 + (lane >> 3);
+                    float x[VPL];
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        const uint32_t w[4] = {raw[it4][v].x, raw[it4][v].y, raw[it4][v].z,
+                                               raw[it4][v].w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            x[8 * v + 2 * u] = __uint_as_float(w[u] << 16);
+                            x[8 * v + 2 * u + 1] = __uint_as_float(w[u] & 0xFFFF0000u);
+                        }
+                    }
                     float amax = 0.f;
 #pragma unroll
-                    for (int sl = 0; sl < SL; ++sl) {
-                        x[sl][0] = x[sl][1] = x[sl][2] = x[sl][3] = 0.f;
-                        if (g < gvalid) {
-                            const uint2 raw = reinterpret_cast<const uint2 *>(
-                                p.q)[((size_t)itq.b * p.Hq + h0 + g) * (D / 4) + sl * 32 + lane];
-                            x[sl][0] = __uint_as_float(raw.x << 16);
-                            x[sl][1] = __uint_as_float(raw.x & 0xFFFF0000u);
-                            x[sl][2] = __uint_as_float(raw.y << 16);
-                            x[sl][3] = __uint_as_float(raw.y & 0xFFFF0000u);
-                        }
-                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[sl][0]), fabsf(x[sl][1])),
-                                                 fmaxf(fabsf(x[sl][2]), fabsf(x[sl][3]))));
-                    }
-                    amax = warp_max(amax);
+                    for (int k = 0; k < VPL; ++k) amax = fmaxf(amax, fabsf(x[k]));
+#pragma unroll
+                    for (int o = 4; o > 0; o >>= 1)  // over the head's eight lanes
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
                     // c = 7 - floor(log2 amax), kept where 2^c and 2^-c are normal
                     int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
                     e = max(-119, min(e, 120));
                     const float sc = pow2i(7 - e);
-                    const int off = (((lane >> 2) ^ (g & 7)) << 4) + 4 * (lane & 3);
+                    // this lane's 16-code chunks of the head's row: slab d0 / 128,
+                    // 16-byte chunk (d0 mod 128) / 16 + j, swizzled by the row
+                    uint8_t *qs_b = qb + (d0 >> 7) * C::QSL;
 #pragma unroll
-                    for (int sl = 0; sl < SL; ++sl) {
-                        float y[4];
+                    for (int j = 0; j < VPL / 16; ++j) {
+                        uint32_t hw[4], lw[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) y[u] = x[sl][u] * sc;  // exact: a power of two
-                        const uint16_t h01 = e4m3x2_of(y[0], y[1]), h23 = e4m3x2_of(y[2], y[3]);
-                        const float2 v01 = e4m3x2_value(h01), v23 = e4m3x2_value(h23);
-                        const uint16_t l01 = e4m3x2_of(y[0] - v01.x, y[1] - v01.y);
-                        const uint16_t l23 = e4m3x2_of(y[2] - v23.x, y[3] - v23.y);
-                        uint8_t *qs_b = qb + sl * C::QSL;
-                        *reinterpret_cast<uint32_t *>(qs_b + g * 128 + off) =
-                            (uint32_t)h01 | ((uint32_t)h23 << 16);
-                        *reinterpret_cast<uint32_t *>(qs_b + (NP + g) * 128 + off) =
-                            (uint32_t)l01 | ((uint32_t)l23 << 16);
+                        for (int u = 0; u < 4; ++u) {
+                            const float a0 = x[16 * j + 4 * u] * sc, a1 = x[16 * j + 4 * u + 1] * sc;
+                            const float a2 = x[16 * j + 4 * u + 2] * sc, a3 = x[16 * j + 4 * u + 3] * sc;
+                            const uint16_t h01 = e4m3x2_of(a0, a1), h23 = e4m3x2_of(a2, a3);
+                            const float2 v01 = e4m3x2_value(h01), v23 = e4m3x2_value(h23);
+                            const uint16_t l01 = e4m3x2_of(a0 - v01.x, a1 - v01.y);
+                            const uint16_t l23 = e4m3x2_of(a2 - v23.x, a3 - v23.y);
+                            hw[u] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+                            lw[u] = (uint32_t)l01 | ((uint32_t)l23 << 16);
+                        }
+                        const int chunk = (((d0 & 127) >> 4) + j) ^ (g & 7);
+                        *reinterpret_cast<uint4 *>(qs_b + g * 128 + (chunk << 4)) =
+                            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4 *>(qs_b + (NP + g) * 128 + (chunk << 4)) =
+                            make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
-                    if (lane == 0) qinv_s[qs * 64 + g] = (g < gvalid) ? pow2i(e - 7) : 0.f;
+                    if (sub == 0) qinv_s[qs * 64 + g] = (g < gvalid) ? pow2i(e - 7) : 0.f;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -648,8 +703,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 }
             }
 
-            // probabilities p (summed into l); the weights p v_scale 2^cv as
-            // three E4M3 parts, each the rounded remainder of the previous
+            // probabilities p (summed into l); the weights p v_scale 2^cv in
+            // binary16 as three E4M3 parts, each the rounded remainder of the
+            // previous
             const float vs2 = vsc * vsf;
             uint32_t ph[NP / 4], pm[NP / 4], pl[NP / 4];
 #pragma unroll
@@ -663,13 +719,14 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                     const float p1 = (s[g + 1] == -INFINITY) ? 0.f : fast_exp2(s[g + 1] - mm[h + 1]);
                     l[g] += p0;
                     l[g + 1] += p1;
-                    const float w0 = p0 * vs2, w1 = p1 * vs2;
-                    const uint16_t c1 = e4m3x2_of(w0, w1);
-                    const float2 d1 = e4m3x2_value(c1);
-                    const float r0 = w0 - d1.x, r1 = w1 - d1.y;
-                    const uint16_t c2 = e4m3x2_of(r0, r1);
-                    const float2 d2 = e4m3x2_value(c2);
-                    const uint16_t c3 = e4m3x2_of(r0 - d2.x, r1 - d2.y);
+                    // w rounded to binary16; its 11 significant bits split
+                    // exactly into three 4-bit E4M3 parts (each remainder is
+                    // a binary16 value, so the subtractions are exact)
+                    const uint32_t w = f16x2_of(p0 * vs2, p1 * vs2);
+                    const uint16_t c1 = e4m3x2_of_f16x2(w);
+                    const uint32_t r1 = f16x2_sub(w, e4m3x2_to_f16x2(c1));
+                    const uint16_t c2 = e4m3x2_of_f16x2(r1);
+                    const uint16_t c3 = e4m3x2_of_f16x2(f16x2_sub(r1, e4m3x2_to_f16x2(c2)));
                     if (h == 0) {
                         ph[g4 / 4] = c1;
                         pm[g4 / 4] = c2;
