@@ -31,7 +31,7 @@
 //     partial scores 16 columns at a time.  (Running the lo part as 4 more
 //     MMAs into the same accumulator, as passes of more than 32 heads once
 //     did, took the PaLM-540B-shaped step from 58.0 to 59.4 us.)
-//     Warps 6-7 write the parts; the softmax scales the score by
+//     Warps 10-11 write the parts; the softmax scales the score by
 //     2^-c k_scale[j].
 //   * P V.  The weight of position j for head g is w = p v_scale[j]
 //     (p = 2^(s - m) the unnormalised probability).  Scaled by a
@@ -65,9 +65,16 @@ namespace kvattn {
 namespace {
 
 constexpr int kBox = 16384;      // one TMA box: 128 positions x 128 codes
-constexpr int kQWarps = 2;       // warps 6-7 write the q parts
-constexpr int kQ8Threads = 192 + 32 * kQWarps;
-constexpr int kQ8EndThreads = 192;  // warps 0-5 meet before tensor memory is freed
+// Warps: 0 copies, 1 issues the MMAs, 2-9 the softmax in two groups of
+// four (group sg = (warp - 2) / 4 takes half of the pass's columns, so two
+// softmax warps share each SM sub-partition), 10-11 write the q parts.
+constexpr int kSoftWarps = 8;
+constexpr int kQWarp0 = 2 + kSoftWarps;
+constexpr int kQWarps = 2;
+constexpr int kQ8Threads = 32 * (kQWarp0 + kQWarps);
+constexpr int kQ8EndThreads = 32 * kQWarp0;  // warps 0-9 meet before tensor memory is freed
+constexpr int kBarQ8All = 1;     // named barrier: the 256 softmax threads
+constexpr int kBarQ8Grp = 3;     // named barriers 3, 4: the 128 threads of softmax group 0, 1
 constexpr float kTauQ8 = 2.f;    // rescale once a score passes the running max by 2 (log2 units)
 constexpr float kVHi = 64.f;     // v_scale[j] 2^cv stays <= 64
 constexpr int kCvNone = 1 << 20; // cv not chosen yet (piece start)
@@ -82,26 +89,28 @@ struct Q8Cfg {
     static constexpr int PST = 2;
     static constexpr int NS_MAX = 12;
     static constexpr int NBAR_MAX = 2 * NS_MAX + 14;
-    static constexpr int FIXED = 2 * QB + PST * PB + 4 * 64 * 4 + 3 * 64 * 4 + 2 * 64 * 4 + 16 +
-                                 64 + 1024 + NBAR_MAX * 8;
+    static constexpr int FIXED = 2 * QB + PST * PB + 2 * 4 * 64 * 4 + 3 * 64 * 4 + 2 * 64 * 4 +
+                                 32 + 64 + 1024 + NBAR_MAX * 8;
     static constexpr int NS_FIT = (kSmemLimit - FIXED) / kStage;
     static constexpr int NS = NS_FIT > NS_MAX ? NS_MAX : NS_FIT;   // staging slots, both rings
     static constexpr int NSK = NS / 2;                             // K staging slots
     static constexpr int NSV = NS - NSK;                           // V staging slots
     static_assert(NSV >= 2 && NSK >= 2, "staging rings must hold two tiles each");
     static_assert(NP % (4 * kQWarps) == 0, "the q warps convert four heads at a time each");
+    static constexpr int NPH = NP / 2;  // columns of one softmax group
+    static_assert(NPH % 8 == 0, "a group's columns come in tensor-memory loads of 8");
 
     static constexpr int off_kst = 0;
     static constexpr int off_vst = off_kst + NSK * kStage;
     static constexpr int off_q = off_vst + NSV * kStage;
     static constexpr int off_p = off_q + 2 * QB;
-    static constexpr int off_red = off_p + PST * PB;      // float [4][64]
-    static constexpr int off_ltot = off_red + 4 * 64 * 4;
+    static constexpr int off_red = off_p + PST * PB;      // float [2 groups][4][64]
+    static constexpr int off_ltot = off_red + 2 * 4 * 64 * 4;
     static constexpr int off_mref = off_ltot + 64 * 4;
     static constexpr int off_alpha = off_mref + 64 * 4;
     static constexpr int off_qinv = off_alpha + 64 * 4;   // float [2][64]: 2^-c per head
-    static constexpr int off_vred = off_qinv + 2 * 64 * 4;  // float [4]: a tile's largest v_scale
-    static constexpr int off_bar = off_vred + 16;
+    static constexpr int off_vred = off_qinv + 2 * 64 * 4;  // float [2][4]: a tile's largest v_scale
+    static constexpr int off_bar = off_vred + 32;
     static constexpr int nbar = 2 * NS + 14;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int bytes = off_misc + 64;
@@ -162,6 +171,50 @@ __device__ __forceinline__ float2 e4m3x2_value(uint16_t two) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
+// N columns (a multiple of 8) of this warp's 32 TMEM lanes from taddr.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]) {
+#pragma unroll
+    for (int c = 0; c + 16 <= N; c += 16) {
+        float t[16];
+        tmem_ld16(taddr + c, t);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[c + k] = t[k];
+    }
+    if constexpr (N % 16 == 8) {
+        float t[8];
+        tmem_ld8(taddr + N - 8, t);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[N - 8 + k] = t[k];
+    }
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&v)[N]) {
+#pragma unroll
+    for (int c = 0; c + 16 <= N; c += 16) {
+        float t[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) t[k] = v[c + k];
+        tmem_st16(taddr + c, t);
+    }
+    if constexpr (N % 16 == 8) {
+        float t[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = v[N - 8 + k];
+        tmem_st8(taddr + N - 8, t);
+    }
+}
+
+// Totals over the warp's lanes of N columns (a multiple of 8), column c's
+// total stored to out[c] (by every lane that ends with it).
+template <int N, class Op>
+__device__ __forceinline__ void warp_cols_n(const float (&v)[N], float *out, int lane, Op op) {
+#pragma unroll
+    for (int c0 = 0; c0 + 32 <= N; c0 += 32) warp_cols<32>(v + c0, out + c0, lane, op);
+    if constexpr (N % 32 >= 16) warp_cols<16>(v + N / 32 * 32, out + N / 32 * 32, lane, op);
+    if constexpr (N % 16 == 8) warp_cols<8>(v + N - 8, out + N - 8, lane, op);
+}
+
 // 2^e as a binary32 value, e in [-126, 127].
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
@@ -193,8 +246,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::off_misc + 16);
 
     // kst_*: the K staging ring (TMA -> Q K^T); vst_*: the V staging ring
-    // (TMA -> P V); q_full/q_empty: the q parts and 2^-c (written by warps
-    // 6-7, freed by the last Q K^T of the piece and the 4 softmax warps)
+    // (TMA -> P V); q_full/q_empty: the q parts and 2^-c (written by the q
+    // warps, freed by the last Q K^T of the piece and the 8 softmax warps)
     uint64_t *kst_full = bar_base, *kst_empty = kst_full + NSK;
     uint64_t *vst_full = kst_empty + NSK, *vst_empty = vst_full + NSV;
     uint64_t *q_full = vst_empty + NSV, *q_empty = q_full + 2;
@@ -217,13 +270,13 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&q_full[s], kQWarps);
-            mbar_init(&q_empty[s], 1 + 4);  // the MMA commit and the 4 softmax warps
+            mbar_init(&q_empty[s], 1 + kSoftWarps);  // the MMA commit and the softmax warps
             mbar_init(&s_full[s], 1);
-            mbar_init(&s_empty[s], 4);
-            mbar_init(&p_full[s], 4);
+            mbar_init(&s_empty[s], kSoftWarps);
+            mbar_init(&p_full[s], kSoftWarps);
             mbar_init(&pv_done[s], 1);
         }
-        mbar_init(o_free, 4);
+        mbar_init(o_free, kSoftWarps);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -330,8 +383,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     }
 
     // ======================================================== q parts (6, 7)
-    if (warp >= 6) {
-        const int qw = warp - 6;
+    if (warp >= kQWarp0) {
+        const int qw = warp - kQWarp0;
         TileIter itq;
         itq.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
         int piece = 0;
@@ -551,9 +604,19 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     }
 
     // ============================================================== softmax
+    // Two groups of four warps; group sg owns columns [cg0, cg0 + NPH) of
+    // the pass (heads cg0 .. cg0 + NPH - 1) for all 128 positions of a tile.
+    // Votes (the running-max refresh, aborts) are taken by all 256 threads,
+    // so both groups move their maxima and the V unit together.
+    constexpr int NPH = C::NPH;
+    const int sg = (warp - 2) >> 2;
+    const int cg0 = sg * NPH;
+    const int bar_grp = kBarQ8Grp + sg;
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    float *redg = red + sg * 256;
+    float *vredg = vred_s + sg * 4;
 
     TileIter it;
     it.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
@@ -562,7 +625,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     bool first_piece = true;
     bool aborted = false;
     bool carry_fail = false;
-    float l[NP];
+    float l[NPH];
 
     while (i < ntiles && !aborted) {
         const int b = it.b;
@@ -570,22 +633,22 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         const int hg = it.seg % p.head_groups;
         const int len = seq_valid_len(it.len, p.Lmax);
         const int t0 = it.t;
-        if (row == 0 && q4 == 0 && t0 == 0 && (it.len < 0 || it.len > p.Lmax))
+        if (row == 0 && q4 == 0 && sg == 0 && t0 == 0 && (it.len < 0 || it.len > p.Lmax))
             set_error(p.err, DEV_ERR_BOUNDS);
         const int h0 = kvh * p.G + hg * p.heads_per_seg;
         const int gvalid = min(p.heads_per_seg, p.G - hg * p.heads_per_seg);
         const size_t zrow = ((size_t)b * p.Hkv + kvh) * p.Lmax;  // first scale of this block
         const long long i0 = i;
         const int qs = spiece & 1;
-        const float *qinv = qinv_s + qs * 64;
+        const float *qinv = qinv_s + qs * 64 + cg0;
         int cv = kCvNone;  // the piece's V weights run in units of 2^-cv (same in every thread)
         float vsf = 0.f;   // 2^cv
 #pragma unroll
-        for (int g = 0; g < NP; ++g) l[g] = 0.f;
-        if (row < NP) mref_s[row] = -INFINITY;
-        // the piece's 2^-c (written by warps 6-7)
+        for (int g = 0; g < NPH; ++g) l[g] = 0.f;
+        if (row < NPH) mref_s[cg0 + row] = -INFINITY;
+        // the piece's 2^-c (written by the q warps)
         carry_fail = carry_fail || !wait_bar(&q_full[qs], (uint32_t)((spiece >> 1) & 1), abort_flag);
-        named_bar_sync(kBarSoftmax, 128);
+        named_bar_sync(bar_grp, 128);
 
         while (true) {
             const int sb = (int)(i & 1);
@@ -610,22 +673,24 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 vsc = __ldcg(p.v_scale + zrow + pos);
             }
             tc_fence_after();
-            float s[NP];
-#pragma unroll
-            for (int c = 0; c < NP / 16; ++c) {  // hi-part scores (all of it when not side by side)
-                float v[16];
-                tmem_ld16(lane_base + sb * C::SW + c * 16, v);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) s[c * 16 + k] = v[k];
-            }
+            // the group's scores: hi-part plus lo-part columns
+            float s[NPH];
+            tmem_ld_n<NPH>(lane_base + sb * C::SW + cg0, s);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < (C::SBS ? NP / 16 : 0); ++c) {  // plus the lo-part scores
+            for (int c = 0; c + 16 <= NPH; c += 16) {
                 float v[16];
-                tmem_ld16(lane_base + sb * C::SW + NP + c * 16, v);
+                tmem_ld16(lane_base + sb * C::SW + NP + cg0 + c, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) s[c * 16 + k] += v[k];
+                for (int k = 0; k < 16; ++k) s[c + k] += v[k];
+            }
+            if constexpr (NPH % 16 == 8) {
+                float v[8];
+                tmem_ld8(lane_base + sb * C::SW + NP + cg0 + NPH - 8, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) s[NPH - 8 + k] += v[k];
             }
             tc_fence_before();
             __syncwarp();
@@ -634,8 +699,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             const float sl = p.scale_log2 * ksc;
             bool over = vsc * vsf > kVHi;
 #pragma unroll
-            for (int g = 0; g < NP; g += 4) {
-                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g);
+            for (int g = 0; g < NPH; g += 4) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + cg0 + g);
                 const float4 c4 = *reinterpret_cast<const float4 *>(qinv + g);
                 s[g] = valid ? s[g] * (c4.x * sl) : -INFINITY;
                 s[g + 1] = valid ? s[g + 1] * (c4.y * sl) : -INFINITY;
@@ -644,19 +709,19 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 over |= (s[g] > m4.x + kTauQ8) | (s[g + 1] > m4.y + kTauQ8) |
                         (s[g + 2] > m4.z + kTauQ8) | (s[g + 3] > m4.w + kTauQ8);
             }
-            if (named_bar_sync_or(kBarSoftmax, 128, over || fail)) {
-                if (named_bar_sync_or(kBarSoftmax, 128, fail || *abort_flag != 0)) {
+            if (named_bar_sync_or(kBarQ8All, 256, over || fail)) {
+                if (named_bar_sync_or(kBarQ8All, 256, fail || *abort_flag != 0)) {
                     aborted = true;
                     break;
                 }
-                warp_cols_np<NP>(s, red + q4 * 64, lane, OpMax());
+                warp_cols_n<NPH>(s, redg + q4 * 64, lane, OpMax());
                 const float vm = warp_max(vsc);  // 0 on rows past the length
-                if (lane == 0) vred_s[q4] = vm;
-                named_bar_sync(kBarSoftmax, 128);
-                if (row < NP) {
-                    const int g = row;
-                    const float tmax = fmaxf(fmaxf(red[g], red[64 + g]),
-                                             fmaxf(red[128 + g], red[192 + g]));
+                if (lane == 0) vredg[q4] = vm;
+                named_bar_sync(bar_grp, 128);
+                if (row < NPH) {
+                    const int g = cg0 + row;
+                    const float tmax = fmaxf(fmaxf(redg[row], redg[64 + row]),
+                                             fmaxf(redg[128 + row], redg[192 + row]));
                     const float m_old = mref_s[g];
                     const float m_new = fmaxf(m_old, tmax);
                     alpha_s[g] = (m_new == -INFINITY || m_old == m_new) ? 1.f
@@ -664,8 +729,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                     mref_s[g] = m_new;
                 }
                 // the V unit: the tile's largest v_scale times 2^cv in [32, 64),
-                // lowered only (the accumulator follows by the same power of two)
-                const float tv = fmaxf(fmaxf(vred_s[0], vred_s[1]), fmaxf(vred_s[2], vred_s[3]));
+                // lowered only (the accumulator follows by the same power of
+                // two); both groups see the same rows, so they agree on it
+                const float tv = fmaxf(fmaxf(vredg[0], vredg[1]), fmaxf(vredg[2], vredg[3]));
                 float fv = 1.f;
                 if (tv > 0.f) {
                     int e = (int)((__float_as_uint(tv) >> 23) & 0xFF) - 127;
@@ -681,23 +747,24 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                     cv = 0;
                 }
                 vsf = pow2i(cv);
-                named_bar_sync(kBarSoftmax, 128);
+                named_bar_sync(bar_grp, 128);
 #pragma unroll
-                for (int g = 0; g < NP; ++g) l[g] *= alpha_s[g];
+                for (int g = 0; g < NPH; ++g) l[g] *= alpha_s[cg0 + g];
                 if (i > i0) {
                     const long long j = i - 1;
                     if (!wait_bar(&pv_done[j & 1], (uint32_t)((j >> 1) & 1), abort_flag))
                         fail = true;
                     tc_fence_after();
+                    // the group's columns of every part of every O^T block
 #pragma unroll
-                    for (int c = 0; c < SL * 3 * NP / 16; ++c) {
-                        float v[16];
-                        const uint32_t a = lane_base + C::OA + c * 16;
-                        tmem_ld16(a, v);
+                    for (int blk = 0; blk < SL * 3; ++blk) {
+                        float v[NPH];
+                        const uint32_t a = lane_base + C::OA + blk * NP + cg0;
+                        tmem_ld_n<NPH>(a, v);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) v[k] *= alpha_s[(c * 16 + k) % NP] * fv;
-                        tmem_st16(a, v);
+                        for (int k = 0; k < NPH; ++k) v[k] *= alpha_s[cg0 + k] * fv;
+                        tmem_st_n<NPH>(a, v);
                     }
                     tmem_st_wait();
                 }
@@ -707,10 +774,10 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             // binary16 as three E4M3 parts, each the rounded remainder of the
             // previous
             const float vs2 = vsc * vsf;
-            uint32_t ph[NP / 4], pm[NP / 4], pl[NP / 4];
+            uint32_t ph[NPH / 4], pm[NPH / 4], pl[NPH / 4];
 #pragma unroll
-            for (int g4 = 0; g4 < NP; g4 += 4) {
-                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g4);
+            for (int g4 = 0; g4 < NPH; g4 += 4) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + cg0 + g4);
                 const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
                 for (int h = 0; h < 4; h += 2) {
@@ -743,17 +810,20 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 if (!wait_bar(&pv_done[jp & 1], (uint32_t)((jp >> 1) & 1), abort_flag))
                     fail = true;
             }
-            // P stage: column block n / 16 at 2048 n / 16, position row at
-            // 128 (row / 8) + 16 (row mod 8); columns hi 0..NP-1, mid, lo
+            // P stage: column n's byte at 2048 (n / 16) + n mod 16 of its
+            // position row, rows at 128 (row / 8) + 16 (row mod 8); columns
+            // hi 0..NP-1, mid NP.., lo 2 NP..; the group's columns go in as
+            // 8-byte runs (column starts are multiples of 8)
             uint8_t *pdst = pbuf + (int)(i % C::PST) * C::PB + (row >> 3) * 128 + (row & 7) * 16;
 #pragma unroll
-            for (int c = 0; c < NP / 16; ++c) {
-                *reinterpret_cast<uint4 *>(pdst + c * 2048) =
-                    make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-                *reinterpret_cast<uint4 *>(pdst + (NP / 16 + c) * 2048) =
-                    make_uint4(pm[4 * c], pm[4 * c + 1], pm[4 * c + 2], pm[4 * c + 3]);
-                *reinterpret_cast<uint4 *>(pdst + (2 * NP / 16 + c) * 2048) =
-                    make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+            for (int u = 0; u < NPH / 8; ++u) {
+                const int ch = cg0 + 8 * u, cm = NP + cg0 + 8 * u, cl = 2 * NP + cg0 + 8 * u;
+                *reinterpret_cast<uint2 *>(pdst + (ch >> 4) * 2048 + (ch & 15)) =
+                    make_uint2(ph[2 * u], ph[2 * u + 1]);
+                *reinterpret_cast<uint2 *>(pdst + (cm >> 4) * 2048 + (cm & 15)) =
+                    make_uint2(pm[2 * u], pm[2 * u + 1]);
+                *reinterpret_cast<uint2 *>(pdst + (cl >> 4) * 2048 + (cl & 15)) =
+                    make_uint2(pl[2 * u], pl[2 * u + 1]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -776,51 +846,65 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         bool fail = carry_fail || !wait_bar(&pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag);
         carry_fail = false;
         tc_fence_after();
-        warp_cols_np<NP>(l, red + q4 * 64, lane, OpSum());
-        named_bar_sync(kBarSoftmax, 128);
-        if (row < NP) ltot_s[row] = red[row] + red[64 + row] + red[128 + row] + red[192 + row];
-        named_bar_sync(kBarSoftmax, 128);
+        warp_cols_n<NPH>(l, redg + q4 * 64, lane, OpSum());
+        named_bar_sync(bar_grp, 128);
+        if (row < NPH)
+            ltot_s[cg0 + row] = redg[row] + redg[64 + row] + redg[128 + row] + redg[192 + row];
+        named_bar_sync(bar_grp, 128);
         const bool complete = (t0 == 0) && it.last_tile_of_segment();
         const size_t slot = 2 * (size_t)blockIdx.x + (first_piece ? 0 : 1);
         const float vinv = (cv == kCvNone) ? 1.f : ldexpf(1.f, -cv);
 #pragma unroll
         for (int sl = 0; sl < SL; ++sl) {  // head dims 128 sl + row
-            const uint32_t oa = lane_base + C::OA + sl * 3 * NP;
-            float o[NP];
+            const uint32_t oa = lane_base + C::OA + sl * 3 * NP + cg0;
+            float o[NPH];
 #pragma unroll
-            for (int c = 0; c < NP / 16; ++c) {  // O^T = (hi + mid + lo parts) 2^-cv
+            for (int c = 0; c + 16 <= NPH; c += 16) {  // O^T = (hi + mid + lo parts) 2^-cv
                 float v[16], w[16], x[16];
-                tmem_ld16(oa + c * 16, v);
-                tmem_ld16(oa + NP + c * 16, w);
-                tmem_ld16(oa + 2 * NP + c * 16, x);
+                tmem_ld16(oa + c, v);
+                tmem_ld16(oa + NP + c, w);
+                tmem_ld16(oa + 2 * NP + c, x);
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) o[c * 16 + k] = (v[k] + w[k] + x[k]) * vinv;
+                for (int k = 0; k < 16; ++k) o[c + k] = (v[k] + w[k] + x[k]) * vinv;
+            }
+            if constexpr (NPH % 16 == 8) {
+                float v[8], w[8], x[8];
+                tmem_ld8(oa + NPH - 8, v);
+                tmem_ld8(oa + NP + NPH - 8, w);
+                tmem_ld8(oa + 2 * NP + NPH - 8, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) o[NPH - 8 + k] = (v[k] + w[k] + x[k]) * vinv;
             }
             const int d = sl * 128 + row;
             if (complete) {
 #pragma unroll
-                for (int g = 0; g < NP; ++g) {
+                for (int k = 0; k < NPH; ++k) {
+                    const int g = cg0 + k;
                     if (g < gvalid) {
                         const float lt = ltot_s[g];
-                        p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (lt > 0.f) ? o[g] / lt : 0.f;
+                        p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (lt > 0.f) ? o[k] / lt : 0.f;
                     }
                 }
             } else {
 #pragma unroll
-                for (int g = 0; g < NP; ++g)
-                    if (g < gvalid) p.ws_o[(slot * p.heads_per_seg + g) * D + d] = o[g];
+                for (int k = 0; k < NPH; ++k) {
+                    const int g = cg0 + k;
+                    if (g < gvalid) p.ws_o[(slot * p.heads_per_seg + g) * D + d] = o[k];
+                }
             }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free);
-        if (!complete && row < gvalid) {
-            p.ws_ml[(slot * p.heads_per_seg + row) * 2 + 0] = mref_s[row];
-            p.ws_ml[(slot * p.heads_per_seg + row) * 2 + 1] = ltot_s[row];
+        if (!complete && row < NPH && cg0 + row < gvalid) {
+            const int g = cg0 + row;
+            p.ws_ml[(slot * p.heads_per_seg + g) * 2 + 0] = mref_s[g];
+            p.ws_ml[(slot * p.heads_per_seg + g) * 2 + 1] = ltot_s[g];
         }
         first_piece = false;
-        if (named_bar_sync_or(kBarSoftmax, 128, fail)) {
+        if (named_bar_sync_or(kBarQ8All, 256, fail)) {
             *abort_flag = 1;
             aborted = true;
             break;
