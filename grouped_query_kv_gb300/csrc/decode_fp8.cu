@@ -171,50 +171,6 @@ __device__ __forceinline__ float2 e4m3x2_value(uint16_t two) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
-// N columns (a multiple of 8) of this warp's 32 TMEM lanes from taddr.
-template <int N>
-__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]) {
-#pragma unroll
-    for (int c = 0; c + 16 <= N; c += 16) {
-        float t[16];
-        tmem_ld16(taddr + c, t);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[c + k] = t[k];
-    }
-    if constexpr (N % 16 == 8) {
-        float t[8];
-        tmem_ld8(taddr + N - 8, t);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[N - 8 + k] = t[k];
-    }
-}
-template <int N>
-__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&v)[N]) {
-#pragma unroll
-    for (int c = 0; c + 16 <= N; c += 16) {
-        float t[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) t[k] = v[c + k];
-        tmem_st16(taddr + c, t);
-    }
-    if constexpr (N % 16 == 8) {
-        float t[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) t[k] = v[N - 8 + k];
-        tmem_st8(taddr + N - 8, t);
-    }
-}
-
-// Totals over the warp's lanes of N columns (a multiple of 8), column c's
-// total stored to out[c] (by every lane that ends with it).
-template <int N, class Op>
-__device__ __forceinline__ void warp_cols_n(const float (&v)[N], float *out, int lane, Op op) {
-#pragma unroll
-    for (int c0 = 0; c0 + 32 <= N; c0 += 32) warp_cols<32>(v + c0, out + c0, lane, op);
-    if constexpr (N % 32 >= 16) warp_cols<16>(v + N / 32 * 32, out + N / 32 * 32, lane, op);
-    if constexpr (N % 16 == 8) warp_cols<8>(v + N - 8, out + N - 8, lane, op);
-}
-
 // 2^e as a binary32 value, e in [-126, 127].
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 

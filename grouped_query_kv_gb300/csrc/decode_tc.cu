@@ -13,7 +13,10 @@ int tc_heads_per_seg(int G, int D) {
 }
 int tc_np(int G, int D) { return (tc_heads_per_seg(G, D) + 15) / 16 * 16; }
 int tc_tile() { return kT; }
-int tc_threads() { return kThreads; }
+int tc_threads(int np, bool several_tokens) {
+    return np == 32 || (several_tokens && np > 32) ? TcGroups<32, false>::THREADS
+                                                   : TcGroups<16, false>::THREADS;
+}
 bool tc_supported(int D, int G) { return (D == 128 || D == 256) && G >= 1; }
 
 template <int D, int NP>

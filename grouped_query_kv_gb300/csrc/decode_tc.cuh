@@ -40,13 +40,13 @@ namespace kvattn {
 
 namespace {
 
-constexpr int kThreads = 192;
 constexpr int kT = 128;             // positions per tile
 constexpr int kChunk = 32768;       // one ring chunk: 2 boxes of 64 columns x 128 rows
 constexpr int kSmemLimit = 232448;  // 227 KB per CTA
 constexpr float kTau = 8.0f;        // log2 headroom before the running max must move
-constexpr int kBarSoftmax = 1;      // named barrier: the 128 softmax threads
+constexpr int kBarSoftmax = 1;      // named barrier: all softmax threads (128 or 256)
 constexpr int kBarEnd = 2;          // named barrier: all warps before TMEM is freed
+constexpr int kBarGroup = 3;        // named barriers 3, 4: softmax group 0, 1 (128 threads each)
 constexpr uint32_t kMmaIdleLimit = 1u << 23;  // ~seconds of polling with nothing ready
 
 __host__ __device__ constexpr int pow2_at_least(int x) {
@@ -90,6 +90,21 @@ struct TcCfg {
     static constexpr int TMEM_COLS = pow2_at_least(TMEM_NEED);
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, NP, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 2 * NP, true, true);
+};
+
+// Softmax warps: one group of four, or two groups (each with half of the
+// columns, so two softmax warps share each SM sub-partition).  Two groups
+// leave 168 registers a thread (ten warps: three on some sub-partitions):
+// enough for 16 columns a group, not for 24 or 32 without spilling, so the
+// one-token passes of 48 and 64 columns keep one group (measured on GB300:
+// the 48-head pass ran 0.6 % slower split, the 32-column one 2 % faster,
+// the several-token passes of 32 and 48 columns 25 % and 8 % faster).
+template <int NP, bool MT>
+struct TcGroups {
+    static constexpr int SG = (NP == 32 || (MT && NP > 32)) ? 2 : 1;
+    static constexpr int NPH = NP / SG;            // columns of one softmax group
+    static constexpr int THREADS = 64 + 128 * SG;
+    static constexpr int RS = SG == 1 ? 64 : 32;   // stride of a warp's column totals in red
 };
 
 struct Bars {
@@ -174,6 +189,50 @@ __device__ __forceinline__ void warp_cols_np(const float (&v)[NP], float *out, i
     if (NP % 32 == 16) warp_cols<16>(v + NP - 16, out + NP - 16, lane, op);
 }
 
+// N columns (a multiple of 8) of this warp's 32 TMEM lanes from taddr.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]) {
+#pragma unroll
+    for (int c = 0; c + 16 <= N; c += 16) {
+        float t[16];
+        tmem_ld16(taddr + c, t);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[c + k] = t[k];
+    }
+    if constexpr (N % 16 == 8) {
+        float t[8];
+        tmem_ld8(taddr + N - 8, t);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[N - 8 + k] = t[k];
+    }
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&v)[N]) {
+#pragma unroll
+    for (int c = 0; c + 16 <= N; c += 16) {
+        float t[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) t[k] = v[c + k];
+        tmem_st16(taddr + c, t);
+    }
+    if constexpr (N % 16 == 8) {
+        float t[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = v[N - 8 + k];
+        tmem_st8(taddr + N - 8, t);
+    }
+}
+
+// Totals over the warp's lanes of N columns (a multiple of 8), column c's
+// total stored to out[c] (by every lane that ends with it).
+template <int N, class Op>
+__device__ __forceinline__ void warp_cols_n(const float (&v)[N], float *out, int lane, Op op) {
+#pragma unroll
+    for (int c0 = 0; c0 + 32 <= N; c0 += 32) warp_cols<32>(v + c0, out + c0, lane, op);
+    if constexpr (N % 32 >= 16) warp_cols<16>(v + N / 32 * 32, out + N / 32 * 32, lane, op);
+    if constexpr (N % 16 == 8) warp_cols<8>(v + N - 8, out + N - 8, lane, op);
+}
+
 // Ring order of the K/V chunks of a CTA's n tiles (KCH chunks per tile each):
 //     K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}
 // V_i goes in behind K_{i+1}: it is needed only after tile i's scores and
@@ -221,11 +280,12 @@ __device__ __forceinline__ bool chunk_is_v(long long m, long long n, long long *
 // blocks' placement in the pool; 16-byte cp.async copies issued by the one
 // producer warp were slower still.
 template <int D, int NP, bool MT, bool PG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcGroups<NP, MT>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tmq, const DecodeParams p) {
     using C = TcCfg<D, NP>;
+    using SGC = TcGroups<NP, MT>;
     constexpr int KCH = C::KCH;
     constexpr int NCH = C::NCH;
 
@@ -268,11 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bs.q_full[s], 1);
             mbar_init(&bs.q_empty[s], 1);
             mbar_init(&bs.s_full[s], 1);
-            mbar_init(&bs.s_empty[s], 4);
-            mbar_init(&bs.p_full[s], 4);
+            mbar_init(&bs.s_empty[s], 4 * SGC::SG);  // one arrival per softmax warp
+            mbar_init(&bs.p_full[s], 4 * SGC::SG);
             mbar_init(&bs.pv_done[s], 1);
         }
-        mbar_init(bs.o_free, 4);
+        mbar_init(bs.o_free, 4 * SGC::SG);
         mbar_init(bs.drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -455,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // be scheduled now -- late enough that its waiting blocks do not sit
         // beside this kernel for long, early enough to hide its launch
         pdl_launch_dependents();
-        named_bar_sync(kBarEnd, kThreads);
+        named_bar_sync(kBarEnd, SGC::THREADS);
         if (*abort_flag && lane == 0) {
             // a role gave up, so copies may still be in flight that no one
             // consumed: let them land before the CTA exits -- the last NCH
@@ -608,16 +668,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_bar(bs.drain, 0, &never);
         }
         __syncwarp();
-        named_bar_sync(kBarEnd, kThreads);
+        named_bar_sync(kBarEnd, SGC::THREADS);
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
         return;
     }
 
     // ============================================================== softmax
+    // SG groups of four warps; group sg owns columns [cg0, cg0 + NPH) of the
+    // pass for all 128 positions of a tile.  Votes (the running-max refresh,
+    // aborts) are taken by every softmax thread, so the groups refresh
+    // their maxima in the same tiles; the exchanges stay within a group.
+    constexpr int SG = SGC::SG;
+    constexpr int NPH = SGC::NPH;
+    constexpr int RS = SGC::RS;
+    const int sg = SG == 1 ? 0 : (warp - 2) >> 2;
+    const int cg0 = sg * NPH;
+    const int bar_grp = SG == 1 ? kBarSoftmax : kBarGroup + sg;
     const int q4 = warp & 3;             // TMEM lane quarter this warp may access
     const int row = q4 * 32 + lane;      // tile position / head-dim row in O^T
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    float *redg = red + sg * 4 * RS;     // this group's column totals, RS floats per warp
 
     TileIter it;
     it.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
@@ -626,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
     const uint32_t wlim = p.wait_limit ? p.wait_limit : KVATTN_SPIN_LIMIT;
     bool carry_fail = false;  // a failed wait late in a tile is voted on at the next barrier
-    float l[NP];
+    float l[NPH];
 
     while (i < ntiles && !aborted) {
         const int b = it.b;
@@ -634,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hg = it.seg % p.head_groups;
         const int len = seq_valid_len(it.len, p.Lmax);
         const int t0 = it.t;
-        if (row == 0 && q4 == 0 && t0 == 0 && (it.len < 0 || it.len > p.Lmax))
+        if (row == 0 && q4 == 0 && sg == 0 && t0 == 0 && (it.len < 0 || it.len > p.Lmax))
             set_error(p.err, DEV_ERR_BOUNDS);
         const int h0 = kvh * p.G + hg * p.hpg;
         // columns: (token, head) for T new tokens, heads of one group otherwise;
@@ -644,22 +715,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hvalid = min(p.hpg, p.G - hg * p.hpg);
         const long long i0 = i;
 #pragma unroll
-        for (int g = 0; g < NP; ++g) l[g] = 0.f;
-        if (row < NP) mref_s[row] = -INFINITY;
-        named_bar_sync(kBarSoftmax, 128);
+        for (int g = 0; g < NPH; ++g) l[g] = 0.f;
+        if (row < NPH) mref_s[cg0 + row] = -INFINITY;
+        named_bar_sync(bar_grp, 128);
 
         while (true) {
             const int sb = (int)(i & 1);
             bool fail = carry_fail || !wait_bar(&bs.s_full[sb], (uint32_t)((i >> 1) & 1), abort_flag, wlim);
             tc_fence_after();
-            float s[NP];
-#pragma unroll
-            for (int c = 0; c < NP / 16; ++c) {
-                float v[16];
-                tmem_ld16(lane_base + sb * NP + c * 16, v);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) s[c * 16 + k] = v[k];
-            }
+            float s[NPH];
+            tmem_ld_n<NPH>(lane_base + sb * NP + cg0, s);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
@@ -687,8 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (PG && !MT) valid = valid && pos >= len - p.qwin;
             bool over = false;
 #pragma unroll
-            for (int g = 0; g < NP; g += 4) {
-                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g);
+            for (int g = 0; g < NPH; g += 4) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + cg0 + g);
                 s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
                 s[g + 1] = valid ? s[g + 1] * p.scale_log2 : -INFINITY;
                 s[g + 2] = valid ? s[g + 2] * p.scale_log2 : -INFINITY;
@@ -700,9 +765,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the tile holds new tokens, or rows before the last token's
                 // window: token t sees positions [e - qwin, e), e = len - (T-1-t)
                 // (a column masked here after voting at most costs an exact max)
-                int t = 0, gg = 0;
+                int t = cg0 / p.hpg, gg = cg0 % p.hpg;
 #pragma unroll
-                for (int g = 0; g < NP; ++g) {
+                for (int g = 0; g < NPH; ++g) {
                     const int e = len - (p.T - 1 - t);
                     if (pos >= e || pos < e - p.qwin) s[g] = -INFINITY;
                     if (++gg == p.hpg) {
@@ -711,45 +776,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (named_bar_sync_or(kBarSoftmax, 128, over || fail)) {
-                if (named_bar_sync_or(kBarSoftmax, 128, fail || *abort_flag != 0)) {
+            if (named_bar_sync_or(kBarSoftmax, 128 * SG, over || fail)) {
+                if (named_bar_sync_or(kBarSoftmax, 128 * SG, fail || *abort_flag != 0)) {
                     aborted = true;
                     break;
                 }
                 // exact tile max per head, then move the running max
-                warp_cols_np<NP>(s, red + q4 * 64, lane, OpMax());
-                named_bar_sync(kBarSoftmax, 128);
-                if (row < NP) {
-                    const int g = row;
-                    const float tmax = fmaxf(fmaxf(red[g], red[64 + g]),
-                                             fmaxf(red[128 + g], red[192 + g]));
+                warp_cols_n<NPH>(s, redg + q4 * RS, lane, OpMax());
+                named_bar_sync(bar_grp, 128);
+                if (row < NPH) {
+                    const int g = cg0 + row;
+                    const float tmax = fmaxf(fmaxf(redg[row], redg[RS + row]),
+                                             fmaxf(redg[2 * RS + row], redg[3 * RS + row]));
                     const float m_old = mref_s[g];
                     const float m_new = fmaxf(m_old, tmax);
                     alpha_s[g] = (m_new == -INFINITY || m_old == m_new) ? 1.f
                                                                          : fast_exp2(m_old - m_new);
                     mref_s[g] = m_new;
                 }
-                named_bar_sync(kBarSoftmax, 128);
+                named_bar_sync(bar_grp, 128);
 #pragma unroll
-                for (int g = 0; g < NP; ++g) l[g] *= alpha_s[g];
+                for (int g = 0; g < NPH; ++g) l[g] *= alpha_s[cg0 + g];
                 if (i > i0) {
                     // O^T holds this piece's earlier tiles: scale column g by alpha[g]
                     const long long j = i - 1;
                     if (!wait_bar(&bs.pv_done[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, wlim))
                         fail = true;
                     tc_fence_after();
+                    if constexpr (SG == 1) {
+                        // hi and lo halves side by side: 2 NP columns per block
+#pragma unroll
+                        for (int db = 0; db < KCH; ++db) {
+#pragma unroll
+                            for (int c = 0; c < 2 * NP / 16; ++c) {
+                                float v[16];
+                                const uint32_t a = lane_base + 2 * NP + db * 2 * NP + c * 16;
+                                tmem_ld16(a, v);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) v[k] *= alpha_s[(c * 16 + k) % NP];
+                                tmem_st16(a, v);
+                            }
+                        }
+                    } else {
 #pragma unroll
                     for (int db = 0; db < KCH; ++db) {
 #pragma unroll
-                        for (int c = 0; c < 2 * NP / 16; ++c) {  // hi half, then lo half
-                            float v[16];
-                            const uint32_t a = lane_base + 2 * NP + db * 2 * NP + c * 16;
-                            tmem_ld16(a, v);
-                            tmem_ld_wait();
+                        for (int part = 0; part < 2; ++part) {  // the hi half, then the lo half
+                            const uint32_t a = lane_base + 2 * NP + db * 2 * NP + part * NP + cg0;
 #pragma unroll
-                            for (int k = 0; k < 16; ++k) v[k] *= alpha_s[(c * 16 + k) % NP];
-                            tmem_st16(a, v);
+                            for (int c = 0; c + 16 <= NPH; c += 16) {
+                                float v[16];
+                                tmem_ld16(a + c, v);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) v[k] *= alpha_s[cg0 + c + k];
+                                tmem_st16(a + c, v);
+                            }
+                            if constexpr (NPH % 16 == 8) {
+                                float v[8];
+                                tmem_ld8(a + NPH - 8, v);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) v[k] *= alpha_s[cg0 + NPH - 8 + k];
+                                tmem_st8(a + NPH - 8, v);
+                            }
                         }
+                    }
                     }
                     tmem_st_wait();
                 }
@@ -758,10 +851,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // probabilities as two bf16 parts, p = hi + lo (hi = p rounded to
             // bf16, lo = the remainder rounded to bf16): the P.V products then
             // carry ~16 significant bits of p instead of 8
-            uint32_t pk[NP / 2], pl[NP / 2];
+            uint32_t pk[NPH / 2], pl[NPH / 2];
 #pragma unroll
-            for (int g4 = 0; g4 < NP; g4 += 4) {
-                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + g4);
+            for (int g4 = 0; g4 < NPH; g4 += 4) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mref_s + cg0 + g4);
                 const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
                 for (int h = 0; h < 4; h += 2) {
@@ -783,9 +876,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(&bs.pv_done[jp & 1], (uint32_t)((jp >> 1) & 1), abort_flag, wlim))
                     fail = true;
             }
-            uint8_t *pdst = pbuf + 2 * (int)(i % C::PST) * C::PB + (row >> 3) * 128 + (row & 7) * 16;
+            // P^T: 8-column groups (core matrices of 8 positions x 8 heads)
+            // 2 KB apart; the group's columns start at group cg0 / 8
+            uint8_t *pdst = pbuf + 2 * (int)(i % C::PST) * C::PB + (row >> 3) * 128 + (row & 7) * 16 +
+                            (cg0 / 8) * (kT / 8) * 128;
 #pragma unroll
-            for (int c = 0; c < NP / 8; ++c) {
+            for (int c = 0; c < NPH / 8; ++c) {
                 *reinterpret_cast<uint4 *>(pdst + c * (kT / 8) * 128) =
                     make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 *reinterpret_cast<uint4 *>(pdst + C::PB + c * (kT / 8) * 128) =
@@ -808,34 +904,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool fail = carry_fail || !wait_bar(&bs.pv_done[e & 1], (uint32_t)((e >> 1) & 1), abort_flag, wlim);
         carry_fail = false;
         tc_fence_after();
-        warp_cols_np<NP>(l, red + q4 * 64, lane, OpSum());
-        named_bar_sync(kBarSoftmax, 128);
-        if (row < NP) ltot_s[row] = red[row] + red[64 + row] + red[128 + row] + red[192 + row];
-        named_bar_sync(kBarSoftmax, 128);
+        warp_cols_n<NPH>(l, redg + q4 * RS, lane, OpSum());
+        named_bar_sync(bar_grp, 128);
+        if (row < NPH)
+            ltot_s[cg0 + row] = redg[row] + redg[RS + row] + redg[2 * RS + row] + redg[3 * RS + row];
+        named_bar_sync(bar_grp, 128);
         const bool complete = (t0 == 0) && it.last_tile_of_segment();
         const size_t slot = 2 * (size_t)blockIdx.x + (first_piece ? 0 : 1);
 #pragma unroll
         for (int db = 0; db < KCH; ++db) {
-            float o[NP];
+            float o[NPH];
+            const uint32_t ob = lane_base + 2 * NP + db * 2 * NP + cg0;
 #pragma unroll
-            for (int c = 0; c < NP / 16; ++c) {
+            for (int c = 0; c + 16 <= NPH; c += 16) {
                 float v[16], w[16];
-                tmem_ld16(lane_base + 2 * NP + db * 2 * NP + c * 16, v);       // V.P_hi
-                tmem_ld16(lane_base + 2 * NP + db * 2 * NP + NP + c * 16, w);  // V.P_lo
+                tmem_ld16(ob + c, v);       // V.P_hi
+                tmem_ld16(ob + NP + c, w);  // V.P_lo
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) o[c * 16 + k] = v[k] + w[k];
+                for (int k = 0; k < 16; ++k) o[c + k] = v[k] + w[k];
+            }
+            if constexpr (NPH % 16 == 8) {
+                float v[8], w[8];
+                tmem_ld8(ob + NPH - 8, v);
+                tmem_ld8(ob + NP + NPH - 8, w);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) o[NPH - 8 + k] = v[k] + w[k];
             }
             const int d = db * 128 + row;
             if (complete && MT) {
                 // column (t, gg) -> out row (b*T + t)*Hq + h0 + gg
-                int t = 0, gg = 0;
+                int t = cg0 / p.hpg, gg = cg0 % p.hpg;
 #pragma unroll
-                for (int g = 0; g < NP; ++g) {
+                for (int k = 0; k < NPH; ++k) {
+                    const int g = cg0 + k;
                     if (g < gvalid && gg < hvalid) {
                         const float lt = ltot_s[g];
                         p.out[(((size_t)b * p.T + t) * p.Hq + h0 + gg) * D + d] =
-                            (lt > 0.f) ? o[g] / lt : 0.f;
+                            (lt > 0.f) ? o[k] / lt : 0.f;
                     }
                     if (++gg == p.hpg) {
                         gg = 0;
@@ -844,27 +951,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else if (complete) {
 #pragma unroll
-                for (int g = 0; g < NP; ++g) {
+                for (int k = 0; k < NPH; ++k) {
+                    const int g = cg0 + k;
                     if (g < gvalid) {
                         const float lt = ltot_s[g];
-                        p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (lt > 0.f) ? o[g] / lt : 0.f;
+                        p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (lt > 0.f) ? o[k] / lt : 0.f;
                     }
                 }
             } else {
 #pragma unroll
-                for (int g = 0; g < NP; ++g)
-                    if (g < gvalid) p.ws_o[(slot * p.heads_per_seg + g) * D + d] = o[g];
+                for (int k = 0; k < NPH; ++k) {
+                    const int g = cg0 + k;
+                    if (g < gvalid) p.ws_o[(slot * p.heads_per_seg + g) * D + d] = o[k];
+                }
             }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bs.o_free);
-        if (!complete && row < gvalid) {
-            p.ws_ml[(slot * p.heads_per_seg + row) * 2 + 0] = mref_s[row];
-            p.ws_ml[(slot * p.heads_per_seg + row) * 2 + 1] = ltot_s[row];
+        if (!complete && row < NPH && cg0 + row < gvalid) {
+            const int g = cg0 + row;
+            p.ws_ml[(slot * p.heads_per_seg + g) * 2 + 0] = mref_s[g];
+            p.ws_ml[(slot * p.heads_per_seg + g) * 2 + 1] = ltot_s[g];
         }
         first_piece = false;
-        if (named_bar_sync_or(kBarSoftmax, 128, fail)) {
+        if (named_bar_sync_or(kBarSoftmax, 128 * SG, fail)) {
             *abort_flag = 1;
             aborted = true;
             break;
@@ -873,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (aborted) set_error(p.err, DEV_ERR_TIMEOUT);
     tc_fence_before();
-    named_bar_sync(kBarEnd, kThreads);
+    named_bar_sync(kBarEnd, SGC::THREADS);
 }
 
 template <int D, int NP, bool MT, bool PG>
@@ -881,7 +992,7 @@ cudaError_t launch_t(const CUtensorMap &tmk, const CUtensorMap &tmv, const CUten
                      const DecodeParams &p, int num_ctas, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_ctas);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(TcGroups<NP, MT>::THREADS);
     cfg.dynamicSmemBytes = TcCfg<D, NP>::alloc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
