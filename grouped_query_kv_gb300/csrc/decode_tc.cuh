@@ -969,7 +969,7 @@ __global__ void __launch_bounds__(TcGroups<NP, MT>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bs.o_free);
-        if (!complete && row < NPH && cg0 + row < gvalid) {
+        if (!complete && (SG == 1 ? row < gvalid : (row < NPH && cg0 + row < gvalid))) {
             const int g = cg0 + row;
             p.ws_ml[(slot * p.heads_per_seg + g) * 2 + 0] = mref_s[g];
             p.ws_ml[(slot * p.heads_per_seg + g) * 2 + 1] = ltot_s[g];

@@ -42,7 +42,9 @@ def _expect_timeout():
     g.check_device_error()  # the word was cleared by the first check
 
 
-@pytest.mark.parametrize("D,Hq,Hkv,ctas", [(128, 16, 2, 0), (256, 48, 1, 0), (128, 64, 8, 37)])
+# (the 32-head pass runs its softmax in two groups of warps, the others in one)
+@pytest.mark.parametrize("D,Hq,Hkv,ctas", [(128, 16, 2, 0), (256, 48, 1, 0), (128, 64, 8, 37),
+                                           (128, 32, 1, 0), (128, 32, 1, 37)])
 def test_a_wait_that_runs_out_reports_a_timeout_and_the_next_call_is_clean(D, Hq, Hkv, ctas):
     dev = torch.device("cuda")
     lens = (700, 5, 300, 129)
@@ -92,6 +94,33 @@ def test_a_timed_out_call_inside_a_chain_leaves_later_calls_correct():
                             lens_np[sel], w.scale)
     for k in (3, 4):
         assert_close(outs[k][sel], ref, bits(x["v_cache"])[sel], lens_np[sel])
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,T", [(128, 64, 8, 4), (256, 48, 1, 2)])
+def test_several_token_pass_that_times_out_reports_it_and_the_next_call_is_clean(D, Hq, Hkv, T):
+    # passes of 32 and 48 (token, head) columns: softmax in two groups of warps
+    dev = torch.device("cuda")
+    lens = (600, T, 129, 300)
+    gen = torch.Generator(device="cpu").manual_seed(T + D)
+    q = torch.randn((len(lens), T, Hq, D), generator=gen).to(torch.bfloat16).to(dev)
+    k = torch.randn((len(lens), Hkv, 600, D), generator=gen).to(torch.bfloat16).to(dev)
+    v = torch.randn((len(lens), Hkv, 600, D), generator=gen).to(torch.bfloat16).to(dev)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+    scale = 1.0 / np.sqrt(D)
+    g.check_device_error()
+    try:
+        g.set_wait_limit(1)
+        g.gqa_decode_attn_multi(q, k, v, lens_t, scale)
+        _expect_timeout()
+        g.set_wait_limit(0)
+        out = g.gqa_decode_attn_multi(q, k, v, lens_t, scale)
+        g.check_device_error()
+    finally:
+        g.set_wait_limit(0)
+    lens_np = np.array(lens, np.int32)
+    ref = oracle.gqa_decode_multi(bits(q), bits(k), bits(v), lens_np, scale)
+    B = len(lens)
+    assert_close(out.reshape(B * T, Hq, D), ref.reshape(B * T, Hq, D), bits(v), lens_np)
 
 
 def test_wait_limit_knob_round_trips():
