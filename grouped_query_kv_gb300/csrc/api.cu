@@ -212,7 +212,7 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl, in
         // one pass takes hpg of the group's heads for all T tokens as its
         // columns; a group whose G x T query rows exceed one pass is split
         // into passes of (nearly) equal head counts, each re-reading the K/V
-        const int maxcols = tc_heads_per_seg(1 << 20, D);  // columns one pass holds
+        const int maxcols = tc_max_cols_several(D);  // columns one pass holds
         if (T > maxcols)
             return fail(KVATTN_ERR_UNSUPPORTED, "T = %d new tokens exceed one pass (%d at D=%d)",
                         T, maxcols, D);

@@ -12,6 +12,9 @@ int tc_heads_per_seg(int G, int D) {
     return (G + groups - 1) / groups;
 }
 int tc_np(int G, int D) { return (tc_heads_per_seg(G, D) + 15) / 16 * 16; }
+// Columns one several-token pass holds: 64 at either head width (at D = 256
+// the 64-column configuration keeps one probability stage to fit)
+int tc_max_cols_several(int D) { return D == 256 || D == 128 ? 64 : 0; }
 int tc_tile() { return kT; }
 int tc_threads(int np, bool several_tokens) {
     return np == 32 || (several_tokens && np > 32) ? TcGroups<32, false>::THREADS

@@ -1027,6 +1027,7 @@ cudaError_t prepare_t() {
         case 256 * 1000 + 16: return FN<256, 16>(__VA_ARGS__); \
         case 256 * 1000 + 32: return FN<256, 32>(__VA_ARGS__); \
         case 256 * 1000 + 48: return FN<256, 48>(__VA_ARGS__); \
+        case 256 * 1000 + 64: return FN<256, 64>(__VA_ARGS__); \
         default: break;                                   \
     }
 // the same, choosing the one-token or the several-token kernel (mt) for a
@@ -1042,6 +1043,9 @@ cudaError_t prepare_t() {
         KVATTN_TC_CASE_MT(FN, 256, 16, mt, pg, __VA_ARGS__)          \
         KVATTN_TC_CASE_MT(FN, 256, 32, mt, pg, __VA_ARGS__)          \
         KVATTN_TC_CASE_MT(FN, 256, 48, mt, pg, __VA_ARGS__)          \
+        case 256 * 1000 + 64:                                        \
+            if (mt) return FN<256, 64, true, pg>(__VA_ARGS__);       \
+            break;                                                   \
         default: break;                                              \
     }
 

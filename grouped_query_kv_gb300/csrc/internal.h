@@ -95,6 +95,7 @@ cudaError_t fma_prepare(int D, int heads_per_seg, int smem_bytes);
 // per pass rounded up to a multiple of 16 (tc_np).
 int tc_np(int G, int D);
 int tc_heads_per_seg(int G, int D);
+int tc_max_cols_several(int D);
 int tc_tile();
 int tc_threads(int np, bool several_tokens);  // threads of a CTA for np columns per pass
 int tc_smem_bytes(int D, int np);

@@ -90,8 +90,8 @@ WORKLOADS = {w.name: w for w in [
     Workload("palm540b_spec4", B=8, Hq=48, Hkv=1, D=256, Lmax=32768,
              scale=1.0 / 16.0, lens=(32768,), k_scale=0.5, T=4,
              note="PaLM-540B-shaped MQA scoring 4 drafted tokens per sequence in one "
-                  "pass: 48 heads x 4 tokens = 192 query rows per K/V head, four passes "
-                  "of 12 heads"),
+                  "pass: 48 heads x 4 tokens = 192 query rows per K/V head, three passes "
+                  "of 16 heads"),
     Workload("local_gqa_w4096", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
              scale=1.0 / math.sqrt(128), lens=(8192,), window=4096,
              note="Llama-70B-shaped GQA decode through a local attention layer: "

@@ -173,19 +173,18 @@ KVATTN_API int kv_append_multi(void *k_cache, void *v_cache, const void *k_new,
  * token t attends positions [0, seq_lens[b] - T + 1 + t) -- the cached prefix
  * and the new tokens up to itself -- and gets a zero row when that is empty.
  * A pass of the kernel takes hpg of a K/V head's G query heads for all T
- * tokens (hpg x T query rows, at most 64 at D = 128 and 48 at D = 256) and
- * reads each K/V tile once for all of them; when G x T rows do not fit one
- * pass, the heads are split over ceil(G / floor(max / T)) passes of nearly
- * equal size, each of which reads the K/V head's tiles again (e.g. 48 heads
- * sharing one K/V head at D = 256: 2 passes of 24 heads for T = 2, 8 of 6
- * for T = 8).
+ * tokens (hpg x T query rows, at most 64) and reads each K/V tile once for
+ * all of them; when G x T rows do not fit one pass, the heads are split over
+ * ceil(G / floor(64 / T)) passes of nearly equal size, each of which reads
+ * the K/V head's tiles again (e.g. 48 heads sharing one K/V head: 2 passes
+ * of 24 heads for T = 2, 3 of 16 for T = 4, 6 of 8 for T = 8).
  *
  *   q        : bf16 [B, T, Hq, D]
  *   k_cache, v_cache, seq_lens : as for gqa_decode_attn (seq_lens counts the
  *              new tokens too)
  *   out      : fp32 [B, T, Hq, D]
- *   T        : 1 .. 64 and at most one pass's rows (64 at D = 128, 48 at
- *              D = 256); needs D in {128, 256}, else KVATTN_ERR_UNSUPPORTED.
+ *   T        : 1 .. 64 (one pass's rows); needs D in {128, 256}, else
+ *              KVATTN_ERR_UNSUPPORTED.
  *              T = 1 is gqa_decode_attn.
  * Ownership, streams and device-side errors are those of gqa_decode_attn.
  */

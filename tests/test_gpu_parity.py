@@ -485,13 +485,13 @@ def test_new_tokens_attend_causally(D, Hq, Hkv, T):
 # G x T rows beyond one pass: the heads split over several passes, each pass
 # re-reading the K/V head ("Efficiently Scaling Transformer Inference", §3:
 # 48 query heads sharing one K/V head; PaLM-8B's 16 heads of 256)
-@pytest.mark.parametrize("D,Hq,Hkv,T", [(256, 16, 1, 4), (256, 16, 1, 8), (256, 48, 1, 2),
+@pytest.mark.parametrize("D,Hq,Hkv,T", [(256, 16, 1, 5), (256, 16, 1, 8), (256, 48, 1, 2),
                                         (256, 48, 1, 4), (256, 48, 1, 8), (256, 96, 2, 3),
                                         (128, 64, 4, 5), (128, 16, 1, 9), (128, 32, 1, 64),
-                                        (256, 13, 1, 7), (256, 4, 1, 48)])
+                                        (256, 13, 1, 7), (256, 4, 1, 48), (256, 4, 1, 64)])
 def test_new_tokens_over_several_head_passes(D, Hq, Hkv, T):
     G = Hq // Hkv
-    cols = 48 if D == 256 else 64
+    cols = 64  # (token, head) columns one pass holds, at D = 128 and 256
     passes = -(-G // (cols // T))
     assert G * T > cols or T == cols  # the shapes need several passes (or a full one)
     plan_hpg = -(-G // passes)
@@ -502,7 +502,7 @@ def test_new_tokens_over_several_head_passes(D, Hq, Hkv, T):
 
 @pytest.mark.parametrize("ctas", [1, 19, 152, 500])
 def test_new_tokens_over_head_passes_with_split_pieces(ctas):
-    # the PaLM-540B head shape, 4 drafted tokens: 4 passes of 12 heads, each
+    # the PaLM-540B head shape, 4 drafted tokens: 3 passes of 16 heads, each
     # sequence's passes cut into pieces by the forced grid
     g.set_tuning(0, ctas)
     try:
@@ -544,7 +544,7 @@ def test_new_tokens_reject_what_one_pass_cannot_hold():
     # more tokens than one pass has rows, or a head width without the
     # tensor-core kernel
     dev = torch.device("cuda")
-    for (B, T, Hq, Hkv, D) in [(1, 49, 16, 1, 256), (1, 2, 4, 1, 64)]:
+    for (B, T, Hq, Hkv, D) in [(1, 65, 16, 1, 256), (1, 65, 8, 1, 128), (1, 2, 4, 1, 64)]:
         q = torch.zeros((B, T, Hq, D), dtype=torch.bfloat16, device=dev)
         k = torch.zeros((B, Hkv, 256, D), dtype=torch.bfloat16, device=dev)
         lens = torch.full((B,), 100, dtype=torch.int32, device=dev)
