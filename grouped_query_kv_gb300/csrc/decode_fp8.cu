@@ -65,16 +65,13 @@ namespace kvattn {
 namespace {
 
 constexpr int kBox = 16384;      // one TMA box: 128 positions x 128 codes
-// Warps: 0 copies, 1 issues the MMAs, 2-9 the softmax in two groups of
-// four (group sg = (warp - 2) / 4 takes half of the pass's columns, so two
-// softmax warps share each SM sub-partition), 10-11 write the q parts.
-constexpr int kSoftWarps = 8;
-constexpr int kQWarp0 = 2 + kSoftWarps;
+// Warps: 0 copies, 1 issues the MMAs, then the softmax in SG groups of four
+// (group sg = (warp - 2) / 4 takes NP / SG of the pass's columns, so SG
+// softmax warps share each SM sub-partition), then two that write the q
+// parts (Q8Cfg: SG, THREADS).
 constexpr int kQWarps = 2;
-constexpr int kQ8Threads = 32 * (kQWarp0 + kQWarps);
-constexpr int kQ8EndThreads = 32 * kQWarp0;  // warps 0-9 meet before tensor memory is freed
-constexpr int kBarQ8All = 1;     // named barrier: the 256 softmax threads
-constexpr int kBarQ8Grp = 3;     // named barriers 3, 4: the 128 threads of softmax group 0, 1
+constexpr int kBarQ8All = 1;     // named barrier: all softmax threads
+constexpr int kBarQ8Grp = 3;     // named barriers 3, 4, ...: the 128 threads of group 0, 1, ...
 constexpr float kTauQ8 = 2.f;    // rescale once a score passes the running max by 2 (log2 units)
 constexpr float kVHi = 64.f;     // v_scale[j] 2^cv stays <= 64
 constexpr int kCvNone = 1 << 20; // cv not chosen yet (piece start)
@@ -89,28 +86,34 @@ struct Q8Cfg {
     static constexpr int PST = 2;
     static constexpr int NS_MAX = 12;
     static constexpr int NBAR_MAX = 2 * NS_MAX + 14;
-    static constexpr int FIXED = 2 * QB + PST * PB + 2 * 4 * 64 * 4 + 3 * 64 * 4 + 2 * 64 * 4 +
-                                 32 + 64 + 1024 + NBAR_MAX * 8;
+    static constexpr int FIXED = 2 * QB + PST * PB + (NP == 48 ? 3 : 2) * 4 * 64 * 4 +
+                                 3 * 64 * 4 + 2 * 64 * 4 + 64 + 64 + 1024 + NBAR_MAX * 8;
     static constexpr int NS_FIT = (kSmemLimit - FIXED) / kStage;
     static constexpr int NS = NS_FIT > NS_MAX ? NS_MAX : NS_FIT;   // staging slots, both rings
     static constexpr int NSK = NS / 2;                             // K staging slots
     static constexpr int NSV = NS - NSK;                           // V staging slots
     static_assert(NSV >= 2 && NSK >= 2, "staging rings must hold two tiles each");
     static_assert(NP % (4 * kQWarps) == 0, "the q warps convert four heads at a time each");
-    static constexpr int NPH = NP / 2;  // columns of one softmax group
+    // softmax groups: three at 48 columns (16 each), else two
+    static constexpr int SG = NP == 48 ? 3 : 2;
+    static constexpr int NPH = NP / SG;  // columns of one softmax group
     static_assert(NPH % 8 == 0, "a group's columns come in tensor-memory loads of 8");
+    static constexpr int SOFTW = 4 * SG;              // softmax warps
+    static constexpr int QWARP0 = 2 + SOFTW;          // first q-part warp
+    static constexpr int THREADS = 32 * (QWARP0 + kQWarps);
+    static constexpr int END_THREADS = 32 * QWARP0;   // warps that meet before TMEM is freed
 
     static constexpr int off_kst = 0;
     static constexpr int off_vst = off_kst + NSK * kStage;
     static constexpr int off_q = off_vst + NSV * kStage;
     static constexpr int off_p = off_q + 2 * QB;
-    static constexpr int off_red = off_p + PST * PB;      // float [2 groups][4][64]
-    static constexpr int off_ltot = off_red + 2 * 4 * 64 * 4;
+    static constexpr int off_red = off_p + PST * PB;      // float [groups][4][64]
+    static constexpr int off_ltot = off_red + (NP == 48 ? 3 : 2) * 4 * 64 * 4;
     static constexpr int off_mref = off_ltot + 64 * 4;
     static constexpr int off_alpha = off_mref + 64 * 4;
     static constexpr int off_qinv = off_alpha + 64 * 4;   // float [2][64]: 2^-c per head
-    static constexpr int off_vred = off_qinv + 2 * 64 * 4;  // float [2][4]: a tile's largest v_scale
-    static constexpr int off_bar = off_vred + 32;
+    static constexpr int off_vred = off_qinv + 2 * 64 * 4;  // float [groups][4]: a tile's largest v_scale
+    static constexpr int off_bar = off_vred + 64;
     static constexpr int nbar = 2 * NS + 14;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int bytes = off_misc + 64;
@@ -175,7 +178,7 @@ __device__ __forceinline__ float2 e4m3x2_value(uint16_t two) {
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
 template <int D, int NP>
-__global__ void __launch_bounds__(kQ8Threads, 1)
+__global__ void __launch_bounds__(Q8Cfg<D, NP>::THREADS, 1)
     decode_q8_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
     using C = Q8Cfg<D, NP>;
@@ -226,13 +229,13 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&q_full[s], kQWarps);
-            mbar_init(&q_empty[s], 1 + kSoftWarps);  // the MMA commit and the softmax warps
+            mbar_init(&q_empty[s], 1 + C::SOFTW);  // the MMA commit and the softmax warps
             mbar_init(&s_full[s], 1);
-            mbar_init(&s_empty[s], kSoftWarps);
-            mbar_init(&p_full[s], kSoftWarps);
+            mbar_init(&s_empty[s], C::SOFTW);
+            mbar_init(&p_full[s], C::SOFTW);
             mbar_init(&pv_done[s], 1);
         }
-        mbar_init(o_free, kSoftWarps);
+        mbar_init(o_free, C::SOFTW);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         }
         __syncwarp();
         pdl_launch_dependents();
-        named_bar_sync(kBarEnd, kQ8EndThreads);
+        named_bar_sync(kBarEnd, C::END_THREADS);
         if (*abort_flag && lane == 0) {
             // a role gave up, so copies may still be in flight that no one
             // consumed: let them land before the CTA exits
@@ -339,8 +342,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     }
 
     // ======================================================== q parts (6, 7)
-    if (warp >= kQWarp0) {
-        const int qw = warp - kQWarp0;
+    if (warp >= C::QWARP0) {
+        const int qw = warp - C::QWARP0;
         TileIter itq;
         itq.init(lens, p.B, p.Lmax, kT, segs_per_b, st);
         int piece = 0;
@@ -553,17 +556,17 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             wait_bar(drain, 0, &never);
         }
         __syncwarp();
-        named_bar_sync(kBarEnd, kQ8EndThreads);
+        named_bar_sync(kBarEnd, C::END_THREADS);
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
         return;
     }
 
     // ============================================================== softmax
-    // Two groups of four warps; group sg owns columns [cg0, cg0 + NPH) of
+    // SG groups of four warps; group sg owns columns [cg0, cg0 + NPH) of
     // the pass (heads cg0 .. cg0 + NPH - 1) for all 128 positions of a tile.
-    // Votes (the running-max refresh, aborts) are taken by all 256 threads,
-    // so both groups move their maxima and the V unit together.
+    // Votes (the running-max refresh, aborts) are taken by all softmax
+    // threads, so the groups move their maxima and the V unit together.
     constexpr int NPH = C::NPH;
     const int sg = (warp - 2) >> 2;
     const int cg0 = sg * NPH;
@@ -665,8 +668,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 over |= (s[g] > m4.x + kTauQ8) | (s[g + 1] > m4.y + kTauQ8) |
                         (s[g + 2] > m4.z + kTauQ8) | (s[g + 3] > m4.w + kTauQ8);
             }
-            if (named_bar_sync_or(kBarQ8All, 256, over || fail)) {
-                if (named_bar_sync_or(kBarQ8All, 256, fail || *abort_flag != 0)) {
+            if (named_bar_sync_or(kBarQ8All, 128 * C::SG, over || fail)) {
+                if (named_bar_sync_or(kBarQ8All, 128 * C::SG, fail || *abort_flag != 0)) {
                     aborted = true;
                     break;
                 }
@@ -860,7 +863,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             p.ws_ml[(slot * p.heads_per_seg + g) * 2 + 1] = ltot_s[g];
         }
         first_piece = false;
-        if (named_bar_sync_or(kBarQ8All, 256, fail)) {
+        if (named_bar_sync_or(kBarQ8All, 128 * C::SG, fail)) {
             *abort_flag = 1;
             aborted = true;
             break;
@@ -869,7 +872,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     }
     if (aborted) set_error(p.err, DEV_ERR_TIMEOUT);
     tc_fence_before();
-    named_bar_sync(kBarEnd, kQ8EndThreads);
+    named_bar_sync(kBarEnd, C::END_THREADS);
 }
 
 template <int D, int NP>
@@ -887,7 +890,7 @@ cudaError_t launch_q8(const CUtensorMap &tmk, const CUtensorMap &tmv, const Deco
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_ctas);
-    cfg.blockDim = dim3(kQ8Threads);
+    cfg.blockDim = dim3(Q8Cfg<D, NP>::THREADS);
     cfg.dynamicSmemBytes = Q8Cfg<D, NP>::alloc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
