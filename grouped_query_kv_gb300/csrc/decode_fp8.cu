@@ -31,7 +31,7 @@
 //     partial scores 16 columns at a time.  (Running the lo part as 4 more
 //     MMAs into the same accumulator, as passes of more than 32 heads once
 //     did, took the PaLM-540B-shaped step from 58.0 to 59.4 us.)
-//     Warps 10-11 write the parts; the softmax scales the score by
+//     The last two warps write the parts; the softmax scales the score by
 //     2^-c k_scale[j].
 //   * P V.  The weight of position j for head g is w = p v_scale[j]
 //     (p = 2^(s - m) the unnormalised probability).  Scaled by a
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, NP>::THREADS, 1)
 
     // kst_*: the K staging ring (TMA -> Q K^T); vst_*: the V staging ring
     // (TMA -> P V); q_full/q_empty: the q parts and 2^-c (written by the q
-    // warps, freed by the last Q K^T of the piece and the 8 softmax warps)
+    // warps, freed by the last Q K^T of the piece and the softmax warps)
     uint64_t *kst_full = bar_base, *kst_empty = kst_full + NSK;
     uint64_t *vst_full = kst_empty + NSK, *vst_empty = vst_full + NSV;
     uint64_t *q_full = vst_empty + NSV, *q_empty = q_full + 2;
