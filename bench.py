@@ -327,7 +327,7 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 # the other target shapes (and the built extensions), timed in the same run
 PER_CONFIG = ["palm8b_mqa", "llama70b_gqa_ragged", "palm540b_long_mqa", "sweep_hkv32_b256",
               "sweep_hkv8_b256", "sweep_hkv1_b256", "local_gqa_w4096", "llama70b_spec4",
-              "palm540b_spec4", "llama70b_paged64", "llama70b_paged16", "llama70b_fp8",
+              "palm540b_spec4", "palm8b_spec4", "llama70b_paged64", "llama70b_paged16", "llama70b_fp8",
               "palm8b_fp8", "palm540b_fp8"]
 
 

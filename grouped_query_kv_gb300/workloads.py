@@ -92,6 +92,10 @@ WORKLOADS = {w.name: w for w in [
              note="PaLM-540B-shaped MQA scoring 4 drafted tokens per sequence in one "
                   "pass: 48 heads x 4 tokens = 192 query rows per K/V head, three passes "
                   "of 16 heads"),
+    Workload("palm8b_spec4", B=64, Hq=16, Hkv=1, D=256, Lmax=2048,
+             scale=1.0 / 16.0, lens=(2048,), T=4,
+             note="PaLM-8B-shaped MQA scoring 4 drafted tokens per sequence: 16 heads "
+                  "x 4 tokens = 64 query rows per K/V head, one pass"),
     Workload("local_gqa_w4096", B=32, Hq=64, Hkv=8, D=128, Lmax=8192,
              scale=1.0 / math.sqrt(128), lens=(8192,), window=4096,
              note="Llama-70B-shaped GQA decode through a local attention layer: "

@@ -552,6 +552,27 @@ def test_new_tokens_reject_what_one_pass_cannot_hold():
             g.gqa_decode_attn_multi(q, k, k, lens, 0.1)
 
 
+@pytest.mark.parametrize("name,nsel", [("llama70b_spec4", 8), ("palm8b_spec4", 8),
+                                       ("palm540b_spec4", 2)])
+def test_drafted_token_workloads_at_full_size_sampled(name, nsel):
+    # the benchmark's drafted-token shapes as it runs them; a seeded sample
+    # of sequences checked against the oracle, every token and head of each
+    w = wl.WORKLOADS[name]
+    dev = torch.device("cuda")
+    x = wl.make_inputs(w, seed=0, device=dev)
+    out = g.gqa_decode_attn_multi(x["q"], x["k_cache"], x["v_cache"], x["attn_lens"], w.scale)
+    g.check_device_error()
+    rng = np.random.default_rng(11)
+    sel = sorted(rng.choice(w.B, nsel, replace=False).tolist())
+    lens = x["attn_lens"].cpu().numpy()[sel]
+    k = bits(x["k_cache"][sel])
+    v = bits(x["v_cache"][sel])
+    ref = oracle.gqa_decode_multi(bits(x["q"][sel]), k, v, lens, w.scale,
+                                  nthreads=oracle_threads())
+    n = len(sel)
+    assert_close(out[sel].reshape(n * w.T, w.Hq, w.D), ref.reshape(n * w.T, w.Hq, w.D), v, lens)
+
+
 @pytest.mark.parametrize("T", [1, 3, 8])
 def test_appending_several_tokens_is_bit_exact(T):
     # T single-row appends in the oracle, one call on the GPU; then the same
