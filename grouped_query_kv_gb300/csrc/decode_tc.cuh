@@ -146,11 +146,11 @@ struct OpSum {
     __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
 };
 
-// Totals over the warp's 32 lanes of N columns (N = 16 or 32), column c's
-// total stored to out[c]: a reduce-scatter in which each butterfly step
+// Totals over the warp's 32 lanes of N columns (N = 8, 16 or 32), column
+// c's total stored to out[c]: a reduce-scatter in which each butterfly step
 // keeps half of a lane's columns and adds its partner's copy of them, so N/2
-// + N/4 + ... shuffles instead of 5 per column.  For N = 16 two lanes end
-// with each column (both store it).  (Compile-time steps: every index is a
+// + N/4 + ... shuffles instead of 5 per column.  For N < 32, 32 / N lanes
+// end with each column (all store it).  (Compile-time steps: every index is a
 // constant, so the columns stay in registers.)
 template <int M, int O, class Op>
 __device__ __forceinline__ void warp_cols_step(float (&a)[32], int lane, int &col, Op op) {
@@ -179,14 +179,6 @@ __device__ __forceinline__ void warp_cols(const float *v, float *out, int lane, 
     int col = 0;
     warp_cols_step<N, 16>(a, lane, col, op);
     out[col] = a[0];
-}
-
-// NP columns (a multiple of 16) in blocks of 32 and 16.
-template <int NP, class Op>
-__device__ __forceinline__ void warp_cols_np(const float (&v)[NP], float *out, int lane, Op op) {
-#pragma unroll
-    for (int c0 = 0; c0 + 32 <= NP; c0 += 32) warp_cols<32>(v + c0, out + c0, lane, op);
-    if (NP % 32 == 16) warp_cols<16>(v + NP - 16, out + NP - 16, lane, op);
 }
 
 // N columns (a multiple of 8) of this warp's 32 TMEM lanes from taddr.
