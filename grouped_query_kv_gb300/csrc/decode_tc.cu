@@ -17,8 +17,8 @@ int tc_np(int G, int D) { return (tc_heads_per_seg(G, D) + 15) / 16 * 16; }
 int tc_max_cols_several(int D) { return D == 256 || D == 128 ? 64 : 0; }
 int tc_tile() { return kT; }
 int tc_threads(int np, bool several_tokens) {
-    return np == 32 || (several_tokens && np > 32) ? TcGroups<32, false>::THREADS
-                                                   : TcGroups<16, false>::THREADS;
+    (void)several_tokens;
+    return np >= 32 ? TcGroups<32, false>::THREADS : TcGroups<16, false>::THREADS;
 }
 bool tc_supported(int D, int G) { return (D == 128 || D == 256) && G >= 1; }
 
@@ -36,8 +36,13 @@ int tc_stages(int D, int np) {
     return -1;
 }
 
+// The one-token 16-column kernels (the PaLM-8B and Llama-70B passes) are
+// compiled in decode_tc16.cu, so that changes to the other passes' code do
+// not move theirs: this kernel's speed has shifted by a percent or more with
+// code that never runs.
 cudaError_t tc_prepare(int D, int np, bool several_tokens) {
-    KVATTN_TC_DISPATCH_MT(prepare_t, several_tokens, false)
+    if (np == 16 && !several_tokens) return tc_prepare_one16(D);
+    KVATTN_TC_DISPATCH_MT_NOT16(prepare_t, several_tokens, false)
     return cudaErrorInvalidValue;
 }
 
@@ -45,7 +50,8 @@ cudaError_t launch_decode_tc(const CUtensorMap &tmk, const CUtensorMap &tmv,
                              const CUtensorMap &tmq, const DecodeParams &p, int np, int num_ctas,
                              cudaStream_t stream) {
     const int D = p.D;
-    KVATTN_TC_DISPATCH_MT(launch_t, p.T > 1, false, tmk, tmv, tmq, p, num_ctas, stream)
+    if (np == 16 && p.T == 1) return launch_decode_tc_one16(tmk, tmv, tmq, p, num_ctas, stream);
+    KVATTN_TC_DISPATCH_MT_NOT16(launch_t, p.T > 1, false, tmk, tmv, tmq, p, num_ctas, stream)
     return cudaErrorInvalidValue;
 }
 

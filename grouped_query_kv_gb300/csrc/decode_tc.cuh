@@ -92,16 +92,17 @@ struct TcCfg {
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 2 * NP, true, true);
 };
 
-// Softmax warps: one group of four, or two groups (each with half of the
-// columns, so two softmax warps share each SM sub-partition).  Two groups
-// leave 168 registers a thread (ten warps: three on some sub-partitions):
-// enough for 16 columns a group, not for 24 or 32 without spilling, so the
-// one-token passes of 48 and 64 columns keep one group (measured on GB300:
-// the 48-head pass ran 0.6 % slower split, the 32-column one 2 % faster,
-// the several-token passes of 32 and 48 columns 25 % and 8 % faster).
+// Softmax warps: one group of four for passes of 16 columns, else two
+// groups (each with half of the columns, so two softmax warps share each SM
+// sub-partition).  Two groups leave 168 registers a thread (ten warps:
+// three on some sub-partitions); the partial-output stores of a split
+// piece go 8 columns at a time so that 24 and 32 columns a group fit
+// (measured on GB300 against one group: the 48-head PaLM-540B pass 55.7 ->
+// 50.9 us, a 64-head one at D = 128 48.0 -> 37.4 us, the 32-column one 2 %
+// faster, the several-token passes of 32 and 48 columns 25 % and 8 %).
 template <int NP, bool MT>
 struct TcGroups {
-    static constexpr int SG = (NP == 32 || (MT && NP > 32)) ? 2 : 1;
+    static constexpr int SG = NP >= 32 ? 2 : 1;
     static constexpr int NPH = NP / SG;            // columns of one softmax group
     static constexpr int THREADS = 64 + 128 * SG;
     static constexpr int RS = SG == 1 ? 64 : 32;   // stride of a warp's column totals in red
@@ -903,6 +904,24 @@ __global__ void __launch_bounds__(TcGroups<NP, MT>::THREADS, 1)
         named_bar_sync(bar_grp, 128);
         const bool complete = (t0 == 0) && it.last_tile_of_segment();
         const size_t slot = 2 * (size_t)blockIdx.x + (first_piece ? 0 : 1);
+        if (SG == 2 && !complete) {
+            // partial pieces of two groups: 8 columns read and stored at a time
+#pragma unroll
+            for (int db = 0; db < KCH; ++db) {
+                const uint32_t ob = lane_base + 2 * NP + db * 2 * NP + cg0;
+                float *dst = p.ws_o + (slot * p.heads_per_seg + cg0) * D + db * 128 + row;
+#pragma unroll
+                for (int c = 0; c < NPH; c += 8) {
+                    float v[8], w[8];
+                    tmem_ld8(ob + c, v);
+                    tmem_ld8(ob + NP + c, w);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (cg0 + c + k < gvalid) dst[(c + k) * D] = v[k] + w[k];
+                }
+            }
+        } else
 #pragma unroll
         for (int db = 0; db < KCH; ++db) {
             float o[NPH];
@@ -950,12 +969,18 @@ __global__ void __launch_bounds__(TcGroups<NP, MT>::THREADS, 1)
                         p.out[((size_t)b * p.Hq + h0 + g) * D + d] = (lt > 0.f) ? o[k] / lt : 0.f;
                     }
                 }
-            } else {
+            } else if constexpr (SG == 1) {
 #pragma unroll
                 for (int k = 0; k < NPH; ++k) {
                     const int g = cg0 + k;
                     if (g < gvalid) p.ws_o[(slot * p.heads_per_seg + g) * D + d] = o[k];
                 }
+            } else {
+                // one base address, the columns' rows D floats apart
+                float *dst = p.ws_o + (slot * p.heads_per_seg + cg0) * D + d;
+#pragma unroll
+                for (int k = 0; k < NPH; ++k)
+                    if (cg0 + k < gvalid) dst[k * D] = o[k];
             }
         }
         tc_fence_before();
@@ -1026,6 +1051,26 @@ cudaError_t prepare_t() {
 // contiguous or a paged cache (pg, a constant)
 #define KVATTN_TC_CASE_MT(FN, d, n, mt, pg, ...) \
     case d * 1000 + n: return mt ? FN<d, n, true, pg>(__VA_ARGS__) : FN<d, n, false, pg>(__VA_ARGS__);
+// the same without the one-token 16-column kernels (contiguous cache: they
+// live in decode_tc16.cu, a translation unit of their own)
+#define KVATTN_TC_DISPATCH_MT_NOT16(FN, mt, pg, ...)                  \
+    switch (D * 1000 + np) {                                         \
+        case 128 * 1000 + 16:                                        \
+            if (mt) return FN<128, 16, true, pg>(__VA_ARGS__);       \
+            break;                                                   \
+        KVATTN_TC_CASE_MT(FN, 128, 32, mt, pg, __VA_ARGS__)          \
+        KVATTN_TC_CASE_MT(FN, 128, 48, mt, pg, __VA_ARGS__)          \
+        KVATTN_TC_CASE_MT(FN, 128, 64, mt, pg, __VA_ARGS__)          \
+        case 256 * 1000 + 16:                                        \
+            if (mt) return FN<256, 16, true, pg>(__VA_ARGS__);       \
+            break;                                                   \
+        KVATTN_TC_CASE_MT(FN, 256, 32, mt, pg, __VA_ARGS__)          \
+        KVATTN_TC_CASE_MT(FN, 256, 48, mt, pg, __VA_ARGS__)          \
+        case 256 * 1000 + 64:                                        \
+            if (mt) return FN<256, 64, true, pg>(__VA_ARGS__);       \
+            break;                                                   \
+        default: break;                                              \
+    }
 #define KVATTN_TC_DISPATCH_MT(FN, mt, pg, ...)                        \
     switch (D * 1000 + np) {                                         \
         KVATTN_TC_CASE_MT(FN, 128, 16, mt, pg, __VA_ARGS__)          \

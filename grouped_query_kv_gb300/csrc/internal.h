@@ -104,6 +104,11 @@ cudaError_t tc_prepare(int D, int np, bool several_tokens);
 cudaError_t launch_decode_tc(const CUtensorMap &tmk, const CUtensorMap &tmv,
                              const CUtensorMap &tmq, const DecodeParams &p, int np, int num_ctas,
                              cudaStream_t stream);
+// the one-token 16-column instantiations (compiled in their own unit)
+cudaError_t tc_prepare_one16(int D);
+cudaError_t launch_decode_tc_one16(const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   const CUtensorMap &tmq, const DecodeParams &p, int num_ctas,
+                                   cudaStream_t stream);
 // the same kernel reading a paged cache (p.block_table set; the K/V maps are
 // over the pools, box rows min(block size, 128))
 cudaError_t tc_prepare_paged(int D, int np, bool several_tokens);
