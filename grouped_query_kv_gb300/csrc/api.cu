@@ -223,14 +223,14 @@ int make_plan(int B, int Hq, int Hkv, int D, int Lmax, int num_sms, Plan *pl, in
         pl->np = (pl->heads_per_seg + 15) / 16 * 16;
         p.tile_positions = tc_tile();
         p.stages = tc_stages(D, pl->np);
-        p.threads = tc_threads(pl->np, true);
+        p.threads = tc_threads(D, pl->np);
         p.smem_bytes = tc_smem_bytes(D, pl->np);
     } else if (path == 2) {
         pl->heads_per_seg = pl->hpg = tc_heads_per_seg(G, D);
         pl->np = tc_np(G, D);
         p.tile_positions = tc_tile();
         p.stages = tc_stages(D, pl->np);
-        p.threads = tc_threads(pl->np, false);
+        p.threads = tc_threads(D, pl->np);
         p.smem_bytes = tc_smem_bytes(D, pl->np);
     } else {
         pl->heads_per_seg = pl->hpg = fma_heads_per_seg(G);

@@ -16,9 +16,9 @@ int tc_np(int G, int D) { return (tc_heads_per_seg(G, D) + 15) / 16 * 16; }
 // the 64-column configuration keeps one probability stage to fit)
 int tc_max_cols_several(int D) { return D == 256 || D == 128 ? 64 : 0; }
 int tc_tile() { return kT; }
-int tc_threads(int np, bool several_tokens) {
-    (void)several_tokens;
-    return np >= 32 ? TcGroups<32, false>::THREADS : TcGroups<16, false>::THREADS;
+int tc_threads(int D, int np) {
+    return np >= 32 || D == 256 ? TcGroups<256, 32, false>::THREADS
+                                : TcGroups<128, 16, false>::THREADS;
 }
 bool tc_supported(int D, int G) { return (D == 128 || D == 256) && G >= 1; }
 

@@ -92,17 +92,19 @@ struct TcCfg {
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 2 * NP, true, true);
 };
 
-// Softmax warps: one group of four for passes of 16 columns, else two
-// groups (each with half of the columns, so two softmax warps share each SM
-// sub-partition).  Two groups leave 168 registers a thread (ten warps:
-// three on some sub-partitions); the partial-output stores of a split
-// piece go 8 columns at a time so that 24 and 32 columns a group fit
-// (measured on GB300 against one group: the 48-head PaLM-540B pass 55.7 ->
-// 50.9 us, a 64-head one at D = 128 48.0 -> 37.4 us, the 32-column one 2 %
-// faster, the several-token passes of 32 and 48 columns 25 % and 8 %).
-template <int NP, bool MT>
+// Softmax warps: two groups of four (each with half of the columns, so two
+// softmax warps share each SM sub-partition), or one group for the passes
+// of 16 columns at D = 128.  Two groups leave 168 registers a thread (ten
+// warps: three on some sub-partitions); the partial-output stores of a split
+// piece go 8 columns at a time so that 24 and 32 columns a group fit.
+// Measured on GB300 against one group: the 48-head PaLM-540B pass 55.7 ->
+// 50.9 us, a 64-head one at D = 128 48.0 -> 37.4 us, the 16-head PaLM-8B
+// pass 30.8 -> 30.1 us, the 32-column one 2 % faster, the several-token
+// passes of 32 and 48 columns 25 % and 8 %; the 16-column passes at D = 128
+// (Llama-70B, the G = 4 sweep, the local window) ran ~1 % slower split.
+template <int D, int NP, bool MT>
 struct TcGroups {
-    static constexpr int SG = NP >= 32 ? 2 : 1;
+    static constexpr int SG = (NP >= 32 || D == 256) ? 2 : 1;
     static constexpr int NPH = NP / SG;            // columns of one softmax group
     static constexpr int THREADS = 64 + 128 * SG;
     static constexpr int RS = SG == 1 ? 64 : 32;   // stride of a warp's column totals in red
@@ -273,12 +275,12 @@ __device__ __forceinline__ bool chunk_is_v(long long m, long long n, long long *
 // blocks' placement in the pool; 16-byte cp.async copies issued by the one
 // producer warp were slower still.
 template <int D, int NP, bool MT, bool PG>
-__global__ void __launch_bounds__(TcGroups<NP, MT>::THREADS, 1)
+__global__ void __launch_bounds__(TcGroups<D, NP, MT>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tmq, const DecodeParams p) {
     using C = TcCfg<D, NP>;
-    using SGC = TcGroups<NP, MT>;
+    using SGC = TcGroups<D, NP, MT>;
     constexpr int KCH = C::KCH;
     constexpr int NCH = C::NCH;
 
@@ -1009,7 +1011,7 @@ cudaError_t launch_t(const CUtensorMap &tmk, const CUtensorMap &tmv, const CUten
                      const DecodeParams &p, int num_ctas, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_ctas);
-    cfg.blockDim = dim3(TcGroups<NP, MT>::THREADS);
+    cfg.blockDim = dim3(TcGroups<D, NP, MT>::THREADS);
     cfg.dynamicSmemBytes = TcCfg<D, NP>::alloc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -97,7 +97,7 @@ int tc_np(int G, int D);
 int tc_heads_per_seg(int G, int D);
 int tc_max_cols_several(int D);
 int tc_tile();
-int tc_threads(int np, bool several_tokens);  // threads of a CTA for np columns per pass
+int tc_threads(int D, int np);  // threads of a CTA for np columns per pass
 int tc_smem_bytes(int D, int np);
 int tc_stages(int D, int np);
 cudaError_t tc_prepare(int D, int np, bool several_tokens);
