@@ -11,7 +11,8 @@
 //     O^T [D x NP] += V_tile^T [D x T] . P^T [T x NP]        (M = 128 head dims)
 // with NP = G rounded up to a multiple of 16 (at most 64 heads per pass).
 //
-// Warp roles (192 threads, one persistent CTA per SM):
+// Warp roles (320 threads, or 192 where the softmax keeps one group; one
+// persistent CTA per SM):
 //   warp 0    TMA producer: per segment piece the group's q rows (2-D map,
 //             128-byte swizzle, double-buffered), and the K and V tiles of
 //             T = 128 positions as 32 KB chunks (two 64-column boxes) into a
@@ -19,14 +20,17 @@
 //   warp 1    allocates tensor memory; one thread issues every tcgen05.mma
 //             (QK of tile i, then PV of tile i-1) and the commits that release
 //             ring chunks, score buffers and probability buffers.
-//   warps 2-5 softmax: thread r owns tile position r (TMEM lane r): loads its
-//             NP scores, masks positions past the length, computes
-//             p = 2^(s - m) and writes it as two bf16 parts (hi + lo) into
-//             shared memory (the B operands of two PV products),
-//             and at the end of a piece reads O^T rows (lane = head dim).
+//   warps 2-9 softmax, in two groups of four that each take half of the
+//             pass's columns (warps 2-5 alone for the 16-column passes at
+//             D = 128; TcGroups): thread r of a group owns tile position r
+//             (TMEM lane r): loads its group's scores, masks positions past
+//             the length, computes p = 2^(s - m) and writes it as two bf16
+//             parts (hi + lo) into shared memory (the B operands of two PV
+//             products), and at the end of a piece reads O^T rows (lane =
+//             head dim).
 // The running max is only moved when a score exceeds it by more than 2^8
-// (a vote over the 128 threads); then the exact tile max is taken and O, l
-// are rescaled.  Between moves p stays below 2^8, so fp32 sums are safe and
+// (a vote over all softmax threads); then the exact tile max is taken and
+// O, l are rescaled.  Between moves p stays below 2^8, so fp32 sums are safe and
 // the result is the same softmax.
 #pragma once
 
