@@ -813,6 +813,27 @@ __global__ void __launch_bounds__(Q8Cfg<D, NP>::THREADS, 1)
         const bool complete = (t0 == 0) && it.last_tile_of_segment();
         const size_t slot = 2 * (size_t)blockIdx.x + (first_piece ? 0 : 1);
         const float vinv = (cv == kCvNone) ? 1.f : ldexpf(1.f, -cv);
+        if (D == 256 && NP == 48 && !complete) {
+            // (the 48-column pass at D = 256) a split piece's partial outputs, 8 columns
+            // read and stored at a time from one base address (the heads'
+            // rows D floats apart): fewer registers live than the loop below
+#pragma unroll
+            for (int sl = 0; sl < SL; ++sl) {
+                const uint32_t oa = lane_base + C::OA + sl * 3 * NP + cg0;
+                float *dst = p.ws_o + (slot * p.heads_per_seg + cg0) * D + sl * 128 + row;
+#pragma unroll
+                for (int c = 0; c < NPH; c += 8) {
+                    float v[8], w[8], x[8];
+                    tmem_ld8(oa + c, v);
+                    tmem_ld8(oa + NP + c, w);
+                    tmem_ld8(oa + 2 * NP + c, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (cg0 + c + k < gvalid) dst[(c + k) * D] = (v[k] + w[k] + x[k]) * vinv;
+                }
+            }
+        } else
 #pragma unroll
         for (int sl = 0; sl < SL; ++sl) {  // head dims 128 sl + row
             const uint32_t oa = lane_base + C::OA + sl * 3 * NP + cg0;
